@@ -1,0 +1,271 @@
+// api.cu -- the extern "C" boundary: argument validation, schedule plans,
+// per-device state (SM count, device error word), tensor-map encoding.
+// Nothing here allocates device memory or synchronizes, except
+// r4_device_error(), which is documented as synchronous.
+
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "r4_internal.h"
+
+namespace r4 {
+
+__device__ int g_device_error;  // first error code any kernel recorded (0 = none)
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];
+int *g_err_ptr[kMaxDevices];
+std::mutex g_mu;
+thread_local const char *t_last_kernel = "";
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return 0;
+  return d;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+}  // namespace
+
+Options &options() {
+  static Options o;
+  return o;
+}
+
+int device_sm_count() {
+  const int d = current_device();
+  if (g_sms[d] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d);
+    g_sms[d] = v > 0 ? v : 1;
+  }
+  return g_sms[d];
+}
+
+int *device_error_word() {
+  const int d = current_device();
+  if (g_err_ptr[d] == nullptr) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess) g_err_ptr[d] = static_cast<int *>(p);
+  }
+  return g_err_ptr[d];
+}
+
+void set_last_kernel(const char *name) { t_last_kernel = name; }
+
+cudaError_t ensure_smem_attr(const void *func, int bytes) {
+  static std::set<std::pair<int, const void *>> done;
+  const int d = current_device();
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (done.count({d, func})) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({d, func});
+  return e;
+}
+
+CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank, void *gaddr, const uint64_t *dims,
+                      const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle) {
+  if (g_encode == nullptr) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode == nullptr) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return CUDA_ERROR_NOT_FOUND;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  cuuint64_t d[5];
+  cuuint64_t s[4];
+  cuuint32_t b[5], e[5];
+  for (uint32_t i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  return g_encode(map, dtype, rank, gaddr, d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace r4
+
+using namespace r4;
+
+extern "C" {
+
+int r4_version(void) { return (0 << 16) | 1; }
+
+const char *r4_status_string(int status) {
+  switch (status) {
+    case R4_OK: return "ok";
+    case R4_ERR_INVALID_ARG: return "invalid argument (null pointer or bad size)";
+    case R4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case R4_ERR_MISALIGNED: return "misaligned pointer or stride";
+    case R4_ERR_WORKSPACE: return "workspace or prepack buffer too small";
+    case R4_ERR_CUDA: return "CUDA error";
+    case R4_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char *r4_last_kernel_name(void) { return t_last_kernel; }
+
+int r4_device_error(int *error_out, int clear) {
+  if (error_out == nullptr) return R4_ERR_INVALID_ARG;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return R4_ERR_CUDA;
+  *error_out = v;
+  if (clear && v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return R4_ERR_CUDA;
+  }
+  return v != 0 ? R4_ERR_DEVICE_TIMEOUT : R4_OK;
+}
+
+int r4_set_option(int key, int64_t value) {
+  switch (key) {
+    case 1: options().w4a8_splits = static_cast<int>(value); return R4_OK;
+    case 2:
+      if (value != 0 && value != 16 && value != 32 && value != 64 && value != 128 && value != 256)
+        return R4_ERR_INVALID_ARG;
+      options().w4a8_token_tile = static_cast<int>(value);
+      return R4_OK;
+    case 3: options().fp8_splits = static_cast<int>(value); return R4_OK;
+    default: return R4_ERR_INVALID_ARG;
+  }
+}
+
+int r4_quant_fp8_per_token(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int64_t group, uint8_t *q, float *s,
+                           r4_stream_t stream) {
+  if (!x || !q || !s) return R4_ERR_INVALID_ARG;
+  if (M < 1 || K < 8 || ldx < K || M > 0x7fffffff || K > 0x7fffffff) return R4_ERR_INVALID_ARG;
+  if (K % 8 || ldx % 8) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!(group == K || (group == 128 && K % 128 == 0))) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(s, 4)) return R4_ERR_MISALIGNED;
+  return launch_quant_act(x, M, K, ldx, group, q, s, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? R4_OK
+             : R4_ERR_CUDA;
+}
+
+int r4_quantize_mxfp4_weight(const float *w, int64_t N, int64_t K, uint8_t *packed, uint8_t *scale,
+                             r4_stream_t stream) {
+  if (!w || !packed || !scale || N < 1 || K < 32) return R4_ERR_INVALID_ARG;
+  if (K % 32) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(w, 16) || !aligned(packed, 16)) return R4_ERR_MISALIGNED;
+  return launch_quant_mxfp4_weight(w, N, K, packed, scale, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? R4_OK
+             : R4_ERR_CUDA;
+}
+
+int r4_quantize_blockfp8_weight(const float *w, int64_t N, int64_t K, uint8_t *q, float *s, r4_stream_t stream) {
+  if (!w || !q || !s || N < 1 || K < 1) return R4_ERR_INVALID_ARG;
+  if (N % 128 || K % 128) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(w, 16) || !aligned(q, 4) || !aligned(s, 4)) return R4_ERR_MISALIGNED;
+  return launch_quant_blockfp8_weight(w, N, K, q, s, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? R4_OK
+             : R4_ERR_CUDA;
+}
+
+size_t r4_prepack_mxfp4_bytes(int64_t N, int64_t K) {
+  if (N < 1 || K < 32 || K % 32) return 0;
+  return mx_packed_bytes(N, K);
+}
+
+int r4_prepack_mxfp4(const uint8_t *w, const uint8_t *w_scale, int64_t N, int64_t K, void *packed,
+                     size_t packed_bytes, r4_stream_t stream) {
+  if (!w || !w_scale || !packed || N < 1 || K < 32) return R4_ERR_INVALID_ARG;
+  if (K % 32) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(w, 16) || !aligned(packed, 256)) return R4_ERR_MISALIGNED;
+  if (packed_bytes < mx_packed_bytes(N, K)) return R4_ERR_WORKSPACE;
+  return launch_prepack_mxfp4(w, w_scale, N, K, static_cast<uint8_t *>(packed),
+                              reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? R4_OK
+             : R4_ERR_CUDA;
+}
+
+size_t r4_prepack_blockfp8_bytes(int64_t N, int64_t K) {
+  if (N < 128 || K < 128 || N % 128 || K % 128) return 0;
+  return fp8_packed_bytes(N, K);
+}
+
+int r4_prepack_blockfp8(const uint8_t *w, const float *w_scale, int64_t N, int64_t K, void *packed,
+                        size_t packed_bytes, r4_stream_t stream) {
+  if (!w || !w_scale || !packed || N < 1 || K < 1) return R4_ERR_INVALID_ARG;
+  if (N % 128 || K % 128) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(w, 16) || !aligned(packed, 256) || !aligned(w_scale, 4)) return R4_ERR_MISALIGNED;
+  if (packed_bytes < fp8_packed_bytes(N, K)) return R4_ERR_WORKSPACE;
+  return launch_prepack_blockfp8(w, w_scale, N, K, static_cast<uint8_t *>(packed),
+                                 reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? R4_OK
+             : R4_ERR_CUDA;
+}
+
+size_t r4_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || N < 1 || K < 1) return 0;
+  switch (op) {
+    case R4_OP_W4A8_MXFP4:
+      if (K % 32 || K < 128) return 0;
+      return plan_w4a8(M, N, K, device_sm_count()).ws_bytes;
+    case R4_OP_BLOCKFP8:
+      if (N % 128 || K % 128) return 0;
+      return plan_blockfp8(M, N, K, device_sm_count()).ws_bytes;
+    default: return 0;
+  }
+}
+
+int r4_gemm_w4a8_mxfp4(const uint8_t *q, const float *s, const void *packed, int64_t M, int64_t N, int64_t K,
+                       uint16_t *c, int64_t ldc, void *workspace, size_t workspace_bytes, r4_stream_t stream) {
+  if (!q || !s || !packed || !c) return R4_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldc < N || M > (1 << 30) || N > (1 << 30)) return R4_ERR_INVALID_ARG;
+  if (K % 32 || K < 128) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(q, 16) || !aligned(packed, 256) || !aligned(s, 4) || !aligned(c, 2)) return R4_ERR_MISALIGNED;
+  const GemmPlan pl = plan_w4a8(M, N, K, device_sm_count());
+  if (pl.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < pl.ws_bytes) return R4_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return R4_ERR_MISALIGNED;
+  }
+  if (device_error_word() == nullptr) return R4_ERR_CUDA;
+  return launch_gemm_w4a8(q, s, static_cast<const uint8_t *>(packed), M, N, K, c, ldc,
+                          pl.ws_bytes ? workspace : nullptr, pl, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int r4_gemm_blockfp8(const uint8_t *q, const float *As, const void *packed, int64_t M, int64_t N, int64_t K,
+                     uint16_t *c, int64_t ldc, void *workspace, size_t workspace_bytes, r4_stream_t stream) {
+  if (!q || !As || !packed || !c) return R4_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldc < N || M > (1 << 30) || N > (1 << 30)) return R4_ERR_INVALID_ARG;
+  if (N % 128 || K % 128) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(q, 16) || !aligned(packed, 256) || !aligned(As, 4) || !aligned(c, 2)) return R4_ERR_MISALIGNED;
+  const GemmPlan pl = plan_blockfp8(M, N, K, device_sm_count());
+  if (pl.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < pl.ws_bytes) return R4_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return R4_ERR_MISALIGNED;
+  }
+  if (device_error_word() == nullptr) return R4_ERR_CUDA;
+  return launch_gemm_blockfp8(q, As, static_cast<const uint8_t *>(packed), M, N, K, c, ldc,
+                              pl.ws_bytes ? workspace : nullptr, pl, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int r4_gemm_bf16_nt_skinny(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N, int64_t K, uint16_t *c,
+                           int64_t ldc, void *workspace, size_t workspace_bytes, r4_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (!x || !w || !c) return R4_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldc < N || N > (1 << 30) || K > (1 << 30)) return R4_ERR_INVALID_ARG;
+  if (M > 64 || K % 256) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(c, 2)) return R4_ERR_MISALIGNED;
+  return launch_gemm_skinny(x, w, M, N, K, c, ldc, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? R4_OK
+             : R4_ERR_CUDA;
+}
+
+}  // extern "C"

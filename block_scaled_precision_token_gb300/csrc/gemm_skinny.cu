@@ -1,0 +1,215 @@
+// gemm_skinny.cu -- skinny bf16 NT GEMM, C = bf16(x W^T), fp32 accumulation,
+// for tiny projections (M <= 64 tokens, N of a few hundred, K of a few
+// thousand): "radiance_gemm.py", module docstring.
+//
+// The page's diagnosis: a sub-megabyte weight gives a library GEMM only a
+// handful of CTAs, each walking all of K while the rest of the GPU idles; the
+// cure is split-K. Here the split is across a thread-block cluster:
+//  * grid = (KS, ceil(N/16)), cluster = (KS, 1, 1): each CTA owns 16 weight
+//    rows (the mma M dimension -- weight-stationary, tokens are the mma N) and
+//    a contiguous K range; KS <= 8 CTAs of a cluster share one row tile.
+//  * operands are staged in shared memory with cp.async (16-byte chunks,
+//    rows padded by 16 bytes so ldmatrix is conflict-free) and multiplied
+//    with mma.sync m16n8k16 bf16 -> fp32. The problem is latency- and
+//    HBM-bound (about 2 flops per weight byte at M = 8), not tensor-bound, so
+//    the warp-level MMA is sufficient; tcgen05 setup (TMEM allocation,
+//    descriptor pipeline) would only add latency here.
+//  * reduction: 4 warps -> shared memory -> one CTA partial; the cluster's
+//    partials are written into rank 0's shared memory through distributed
+//    shared memory, and rank 0 sums them in rank order (deterministic), rounds
+//    to bf16 and stores. No global workspace, no atomics, no second kernel.
+
+#include <cuda_bf16.h>
+
+#include "r4_internal.h"
+
+namespace r4 {
+namespace skinny {
+
+constexpr int kThreads = 128;
+constexpr int kRows = 16;
+constexpr int kIter = 512;              // K staged per iteration
+constexpr int kStride = kIter + 8;      // padded row, in bf16 elements
+constexpr int kMaxM = 64;
+constexpr int kMaxKS = 8;
+
+constexpr size_t kSmemW = kRows * kStride * 2;
+constexpr size_t kSmemX = kMaxM * kStride * 2;
+constexpr size_t kSmemRed = 4 * kRows * kMaxM * 4;
+constexpr size_t kSmemCluster = kMaxKS * kRows * kMaxM * 4;
+constexpr size_t kSmemBytes = kSmemW + kSmemX + kSmemRed + kSmemCluster;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+template <int NG2>  // token groups of 16 (Mpad = 16 * NG2)
+__global__ void __launch_bounds__(kThreads, 1)
+    skinny_bf16_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w, int M, int N, int K,
+                       int chunks_per_cta, uint16_t *__restrict__ c, int ldc) {
+  constexpr int kMpad = 16 * NG2;
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t *sW = reinterpret_cast<uint16_t *>(smem);
+  uint16_t *sX = reinterpret_cast<uint16_t *>(smem + kSmemW);
+  float *sRed = reinterpret_cast<float *>(smem + kSmemW + kSmemX);             // [4][16][kMaxM]
+  float *sCl = reinterpret_cast<float *>(smem + kSmemW + kSmemX + kSmemRed);   // [KS][16][kMaxM]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  const int KS = gridDim.x;
+  const int n0 = blockIdx.y * kRows;
+  const int kbeg = static_cast<int>(rank) * chunks_per_cta * 256;
+  const int kend = min(K, kbeg + chunks_per_cta * 256);
+
+  // Let the cluster's CTAs start; the matching wait precedes the DSMEM writes.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
+  float acc[2 * NG2][4];
+#pragma unroll
+  for (int g = 0; g < 2 * NG2; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
+
+  for (int kk = kbeg; kk < kend; kk += kIter) {
+    const int klen = min(kIter, kend - kk);      // multiple of 256
+    const int cpr = klen / 8;                     // 16-byte chunks per row
+    for (int i = tid; i < kRows * cpr; i += kThreads) {
+      const int r = i / cpr, ch = i - r * cpr;
+      uint16_t *dst = sW + r * kStride + ch * 8;
+      if (n0 + r < N)
+        cp_async16(dst, w + static_cast<size_t>(n0 + r) * K + kk + ch * 8);
+      else
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    for (int i = tid; i < kMpad * cpr; i += kThreads) {
+      const int r = i / cpr, ch = i - r * cpr;
+      uint16_t *dst = sX + r * kStride + ch * 8;
+      if (r < M)
+        cp_async16(dst, x + static_cast<size_t>(r) * K + kk + ch * 8);
+      else
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const int nsteps = klen / 16;
+    for (int ks = warp; ks < nsteps; ks += 4) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(smem_addr(sW + (lane & 15) * kStride + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+#pragma unroll
+      for (int g2 = 0; g2 < NG2; ++g2) {
+        uint32_t b0, b1, b2, b3;
+        const int tok = g2 * 16 + (lane >> 4) * 8 + (lane & 7);
+        ldsm_x4(smem_addr(sX + tok * kStride + ks * 16 + ((lane >> 3) & 1) * 8), b0, b1, b2, b3);
+        mma_bf16(acc[2 * g2], a0, a1, a2, a3, b0, b1);
+        mma_bf16(acc[2 * g2 + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+    __syncthreads();
+  }
+
+  // warp partials -> shared memory (D fragment: rows lane/4 and lane/4 + 8,
+  // token columns 8g + 2(lane%4) + {0,1})
+  float *red = sRed + warp * kRows * kMaxM;
+#pragma unroll
+  for (int g = 0; g < 2 * NG2; ++g) {
+    const int r = lane >> 2, t = 8 * g + 2 * (lane & 3);
+    red[r * kMaxM + t] = acc[g][0];
+    red[r * kMaxM + t + 1] = acc[g][1];
+    red[(r + 8) * kMaxM + t] = acc[g][2];
+    red[(r + 8) * kMaxM + t + 1] = acc[g][3];
+  }
+  __syncthreads();
+
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  const uint32_t dst_base = map_rank(smem_addr(sCl + rank * kRows * kMaxM), 0);
+  for (int i = tid; i < kRows * kMpad; i += kThreads) {
+    const int r = i % kRows, t = i / kRows;
+    const float v = sRed[r * kMaxM + t] + sRed[kRows * kMaxM + r * kMaxM + t] +
+                    sRed[2 * kRows * kMaxM + r * kMaxM + t] + sRed[3 * kRows * kMaxM + r * kMaxM + t];
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst_base + 4u * (r * kMaxM + t)), "f"(v) : "memory");
+  }
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (rank == 0) {
+    for (int i = tid; i < kRows * kMpad; i += kThreads) {
+      const int r = i % kRows, t = i / kRows;
+      float v = 0.f;
+      for (int s = 0; s < KS; ++s) v += sCl[s * kRows * kMaxM + r * kMaxM + t];
+      if (t < M && n0 + r < N) {
+        __nv_bfloat16 h = __float2bfloat16_rn(v);
+        c[static_cast<size_t>(t) * ldc + n0 + r] = *reinterpret_cast<uint16_t *>(&h);
+      }
+    }
+  }
+}
+
+template <int NG2>
+cudaError_t launch_ng(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N, int64_t K, uint16_t *c,
+                      int64_t ldc, cudaStream_t st) {
+  const int chunks = static_cast<int>(K / 256);
+  const int ks = chunks < kMaxKS ? chunks : kMaxKS;
+  const int cpc = (chunks + ks - 1) / ks;
+  auto kern = skinny_bf16_kernel<NG2>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ks), static_cast<unsigned>(ceil_div(N, kRows)), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(ks);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, x, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), cpc, c,
+                         static_cast<int>(ldc));
+  set_last_kernel(NG2 == 1 ? "skinny_bf16_kernel<1>" : NG2 == 2 ? "skinny_bf16_kernel<2>"
+                  : NG2 == 3 ? "skinny_bf16_kernel<3>" : "skinny_bf16_kernel<4>");
+  return e;
+}
+
+}  // namespace skinny
+
+cudaError_t launch_gemm_skinny(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N, int64_t K, uint16_t *c,
+                               int64_t ldc, cudaStream_t st) {
+  const int64_t ng2 = ceil_div(M, 16);
+  switch (ng2) {
+    case 1: return skinny::launch_ng<1>(x, w, M, N, K, c, ldc, st);
+    case 2: return skinny::launch_ng<2>(x, w, M, N, K, c, ldc, st);
+    case 3: return skinny::launch_ng<3>(x, w, M, N, K, c, ldc, st);
+    default: return skinny::launch_ng<4>(x, w, M, N, K, c, ldc, st);
+  }
+}
+
+}  // namespace r4

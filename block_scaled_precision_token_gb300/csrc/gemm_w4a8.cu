@@ -1,0 +1,437 @@
+// gemm_w4a8.cu -- W4A8 MXFP4 linear on tcgen05 block-scaled MMA.
+//
+//   C[m, n] = bf16( s[m] * sum_k e4m3(q[m,k]) * e2m1(w[n,k]) * 2^(e[n,k/32]-127) )
+//
+// ("radiance_mxfp4.py": module docstring -- fp8 activations against e2m1
+// weights with a ue8m0 scale per 32 K -- and _exact_ref.)
+//
+// Design (GB300, sm_103a):
+//  * Weight-stationary orientation ("swap AB"): the MMA's 128-row A operand is
+//    128 weight rows, its N operand is a tile of BT tokens (16..256). One
+//    kernel serves decode (M <= 64: BT = 16/32/64, the weight stream is the
+//    whole cost) and prefill (BT = 128/256, tensor-bound).
+//  * kind::mxf8f6f4 with .scale_vec::1X: A = e2m1 (weights) with its ue8m0
+//    scale per 32 K, B = e4m3 (activations) with a constant scale 127 (x1).
+//    The hardware applies the MX block scale exactly; the per-token fp32
+//    scale s[m] is applied in the epilogue.
+//  * TMA: the prepacked 8 KiB weight tile is loaded with the 16U4_ALIGN16B
+//    data type, which expands 16 packed nibbles to the 16-byte smem slot the
+//    MMA reads for 4-bit operands (HBM traffic stays 0.5 B per weight); the
+//    activation tile is a 2-D e4m3 box; both in the 128-byte swizzle. The
+//    512-byte scale atom of the tile is a plain bulk copy, then tcgen05.cp
+//    places it in tensor memory (one 4-column slot per pipeline stage).
+//  * Roles: warp 0 issues TMA, warp 1 allocates tensor memory and issues MMAs
+//    (one thread), warps 2..5 drain the accumulator (tcgen05.ld), scale by
+//    s[m], round to bf16 and store. A multi-stage smem ring decouples TMA from
+//    MMA; double-buffered accumulators (BT <= 128) let the epilogue of one
+//    unit overlap the MMAs of the next.
+//  * Split-K when the output has too few tiles to fill 152 SMs: fp32 partials
+//    go to the caller's workspace and the last CTA to arrive at a tile (one
+//    atomic counter per tile) sums them in split order -- deterministic -- and
+//    resets the counter. No CTA ever waits for another.
+//  * Every mbarrier wait is bounded (see r4_device.cuh).
+
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "r4_device.cuh"
+#include "r4_internal.h"
+
+namespace r4 {
+namespace w4a8 {
+
+constexpr int kThreads = 192;
+constexpr int kBK = 128;
+constexpr uint32_t kWSmem = 128 * 128;  // expanded e2m1 tile: 128 rows x 128 one-byte slots
+// The 16U4_ALIGN16B tile load completes the mbarrier transaction with the
+// bytes it READS (8 KiB of packed nibbles), not the 16 KiB it writes to
+// shared memory (measured on GB300: a 16 KiB expectation never completes).
+constexpr uint32_t kWTxBytes = 8192;
+constexpr uint32_t kSfBytes = 512;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfaCol = 256;       // 4 columns per stage, up to 8 stages
+constexpr uint32_t kSfbCol = 288;       // 16 columns of constant 127
+
+struct Params {
+  int M, N, KB;
+  int t_tiles, splits, kb_per_split, units;
+  int ldc;
+  const float *s;
+  const uint8_t *sf;     // scale atoms of the prepacked weight
+  uint16_t *c;
+  float *partials;
+  int *counters;
+  int *err;
+};
+
+template <int BT>
+struct Cfg {
+  static constexpr uint32_t kXSmem = BT * 128;
+  static constexpr uint32_t kStageBytes = ((kWSmem + kXSmem + kSfBytes + 1023) / 1024) * 1024;
+  static constexpr int kStagesRaw = static_cast<int>((200u * 1024u) / kStageBytes);
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kNumAcc = BT <= 128 ? 2 : 1;
+  static constexpr uint32_t kTxBytes = kWTxBytes + kXSmem + kSfBytes;
+  static constexpr uint32_t kMiscBytes = 1024;
+  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kMiscBytes + 1024;  // + alignment slack
+};
+
+__device__ __forceinline__ void decode_unit(const Params &p, int u, int &nt, int &tt, int &sp) {
+  const int tile = u / p.splits;
+  sp = u - tile * p.splits;
+  nt = tile / p.t_tiles;
+  tt = tile - nt * p.t_tiles;
+}
+
+template <int BT>
+__global__ void __launch_bounds__(kThreads, 1)
+    w4a8_mxf8f6f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                         const Params p) {
+  using C = Cfg<BT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *misc = smem + C::kStages * C::kStageBytes;
+  uint8_t *sfb_const = misc;                                         // 512 B of 0x7F
+  uint64_t *full_bar = reinterpret_cast<uint64_t *>(misc + 512);     // [8]
+  uint64_t *empty_bar = full_bar + 8;                                // [8]
+  uint64_t *accf_bar = empty_bar + 8;                                // [2]
+  uint64_t *acce_bar = accf_bar + 2;                                 // [2]
+  uint64_t *drain_bar = acce_bar + 2;                                // [1]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain_bar + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *is_last = abort_flag + 1;
+  volatile int *epi_abort = abort_flag + 2;   // set and read by epilogue threads only
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  for (int i = threadIdx.x; i < 128; i += kThreads) reinterpret_cast<uint32_t *>(sfb_const)[i] = 0x7F7F7F7Fu;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&accf_bar[a], 1);
+      mbar_init(&acce_bar[a], 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *is_last = 0;
+    *epi_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_x);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        int nt, tt, sp;
+        decode_unit(p, u, nt, tt, sp);
+        const int kb0 = sp * p.kb_per_split;
+        const int kb1 = min(p.KB, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) {
+            ok = false;
+            break;
+          }
+          uint8_t *st = smem + stage * C::kStageBytes;
+          mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
+          tma_load_3d(st, &tm_w, &full_bar[stage], 0, 0, nt * p.KB + kb, pol_w);
+          tma_load_2d(st + kWSmem, &tm_x, &full_bar[stage], kb * kBK, tt * BT, pol_x);
+          bulk_load(st + kWSmem + C::kXSmem, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
+                    &full_bar[stage], pol_w);
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Never leave a copy in flight: wait (bounded, even after an abort) for
+      // the last load issued into every stage.
+      for (int s = 0; s < C::kStages; ++s)
+        if (issued_mask & (1u << s)) {
+          volatile int dummy = 0;
+          mbar_wait(&full_bar[s], (issued_phase >> s) & 1u, &dummy, p.err, DEV_ERR_WAIT_DRAIN);
+        }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint64_t sfb_desc = sdesc_sf_32x16(smem_u32(sfb_const));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tc_cp_32x128b_warpx4(tmem + kSfbCol + 4 * j, sfb_desc);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        int nt, tt, sp;
+        decode_unit(p, u, nt, tt, sp);
+        const int kb0 = sp * p.kb_per_split;
+        const int kb1 = min(p.KB, kb0 + p.kb_per_split);
+        if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_ACC_EMPTY)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BT);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.err, DEV_ERR_WAIT_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint8_t *st = smem + stage * C::kStageBytes;
+          const uint32_t sfa = tmem + kSfaCol + 4u * static_cast<uint32_t>(stage);
+          tc_cp_32x128b_warpx4(sfa, sdesc_sf_32x16(smem_u32(st + kWSmem + C::kXSmem)));
+          const uint32_t a_base = smem_u32(st);
+          const uint32_t b_base = smem_u32(st + kWSmem);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sdesc_sw128_kmajor(a_base + 32u * kk);
+            const uint64_t bd = sdesc_sw128_kmajor(b_base + 32u * kk);
+            const uint32_t idesc = idesc_mxf8f6f4_e2m1_e4m3(BT, kk, 0);
+            tc_mma_mxf8f6f4(d_tmem, ad, bd, idesc, sfa | (static_cast<uint32_t>(kk) << 30), tmem + kSfbCol,
+                            (kb > kb0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty_bar[stage]);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&accf_bar[acc]);
+        if (++acc == C::kNumAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // All MMAs this thread issued must be complete before tensor memory is freed.
+      tc_commit(drain_bar);
+      volatile int dummy = 0;
+      mbar_wait(drain_bar, 0, &dummy, p.err, DEV_ERR_WAIT_DRAIN);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;         // tensor-memory lane quarter this warp may access
+    const int ew = warp - 2;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    constexpr int CH = BT < 32 ? BT : 32;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      int nt, tt, sp;
+      decode_unit(p, u, nt, tt, sp);
+      // The decision to stop must be the same in all 128 epilogue threads
+      // (they meet at named barriers below): a failed wait is published
+      // before the barrier and read after it.
+      if (!mbar_wait(&accf_bar[acc], acc_phase, abort_flag, p.err, DEV_ERR_WAIT_ACC_FULL)) *epi_abort = 1;
+      named_bar_sync(1, 128);
+      if (*epi_abort) break;
+      tc_fence_after();
+      const int n = nt * 128 + q * 32 + lane;
+      const int t0 = tt * BT;
+      const int tile = nt * p.t_tiles + tt;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BT);
+      float *part = (p.splits > 1) ? p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (128 * BT) : nullptr;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BT; c0 += CH) {
+        uint32_t r[32];
+        if constexpr (CH == 32) {
+          tc_ld_32x32b_x32(taddr + c0, r);
+        } else {
+          tc_ld_32x32b_x16(taddr + c0, r);
+        }
+        tc_wait_ld();
+        if (c0 + CH >= BT) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce_bar[acc]);
+        }
+        if (p.splits == 1) {
+          if (n < p.N) {
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+              const int t = t0 + c0 + j;
+              if (t < p.M)
+                p.c[static_cast<size_t>(t) * p.ldc + n] = f32_to_bf16_rn(__uint_as_float(r[j]) * __ldg(p.s + t));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < CH; ++j) part[(c0 + j) * 128 + q * 32 + lane] = __uint_as_float(r[j]);
+        }
+      }
+      if (p.splits > 1) {
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (ew == 0 && lane == 0) {
+          const int prev = atomicAdd(p.counters + tile, 1);
+          *is_last = (prev == p.splits - 1) ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        if (*is_last) {
+          __threadfence();
+          const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (128 * BT);
+          const int tmax = min(BT, p.M - t0);
+          for (int tl = 0; tl < tmax; ++tl) {
+            float sum = 0.f;
+            for (int s2 = 0; s2 < p.splits; ++s2)
+              sum += ld_cg_f32(base + static_cast<size_t>(s2) * (128 * BT) + tl * 128 + q * 32 + lane);
+            if (n < p.N) p.c[static_cast<size_t>(t0 + tl) * p.ldc + n] = f32_to_bf16_rn(sum * __ldg(p.s + t0 + tl));
+          }
+          if (ew == 0 && lane == 0) p.counters[tile] = 0;
+        }
+        named_bar_sync(1, 128);
+      }
+      if (++acc == C::kNumAcc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int BT>
+int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M, int64_t N, int64_t K, uint16_t *c,
+              int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st) {
+  using C = Cfg<BT>;
+  const int64_t NT = ceil_div(N, 128);
+  CUtensorMap tm_w, tm_x;
+  {
+    const uint64_t dims[3] = {128, 128, static_cast<uint64_t>(NT * pl.KB)};
+    const uint64_t strides[2] = {64, 8192};
+    const uint32_t box[3] = {128, 128, 1};
+    if (encode_tiled(&tm_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t *>(packed), dims, strides,
+                     box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return R4_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(K)};
+    const uint32_t box[2] = {128, static_cast<uint32_t>(BT)};
+    if (encode_tiled(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(q), dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return R4_ERR_CUDA;
+  }
+  Params p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.KB = pl.KB;
+  p.t_tiles = pl.t_tiles;
+  p.splits = pl.splits;
+  p.kb_per_split = pl.kb_per_split;
+  p.units = pl.units;
+  p.ldc = static_cast<int>(ldc);
+  p.s = s;
+  p.sf = packed + mx_packed_codes_bytes(N, K);
+  p.c = c;
+  p.counters = reinterpret_cast<int *>(ws);
+  p.partials = ws ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) + pl.counters_bytes) : nullptr;
+  p.err = device_error_word();
+  auto kern = w4a8_mxf8f6f4_kernel<BT>;
+  if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::kSmemBytes) != cudaSuccess) return R4_ERR_CUDA;
+  kern<<<pl.grid, kThreads, C::kSmemBytes, st>>>(tm_w, tm_x, p);
+  set_last_kernel(BT == 16    ? "w4a8_mxf8f6f4_kernel<16>"
+                  : BT == 32  ? "w4a8_mxf8f6f4_kernel<32>"
+                  : BT == 64  ? "w4a8_mxf8f6f4_kernel<64>"
+                  : BT == 128 ? "w4a8_mxf8f6f4_kernel<128>"
+                              : "w4a8_mxf8f6f4_kernel<256>");
+  return cudaGetLastError() == cudaSuccess ? R4_OK : R4_ERR_CUDA;
+}
+
+}  // namespace w4a8
+
+// Token tile and split-K choice. A small wave model: every SM streams its
+// unit's weight bytes at an equal share of HBM bandwidth or runs its MMAs at
+// the per-SM FP8 rate, whichever is slower; split-K adds its partial traffic
+// and the serial final reduction of the last-arriving CTA.
+GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
+  GemmPlan pl;
+  int bt = options().w4a8_token_tile;
+  if (bt == 0) bt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  pl.BT = bt;
+  pl.n_tiles = static_cast<int>(ceil_div(N, 128));
+  pl.t_tiles = static_cast<int>(ceil_div(M, bt));
+  pl.KB = static_cast<int>(ceil_div(K, 128));
+  const int64_t tiles = static_cast<int64_t>(pl.n_tiles) * pl.t_tiles;
+  const double hbm = 6.5e12, sm_flops = 4.5e15 / 152.0, sm_l2 = 150e9;
+  const double kb_bytes = 128.0 * 128 * 0.5 + 512 + 128.0 * bt;      // weight + scales + activations
+  const double kb_flops = 2.0 * 128 * bt * 128;
+  int best_s = 1;
+  double best_t = 1e30;
+  const int forced = options().w4a8_splits;
+  for (int s = 1; s <= std::min(pl.KB, 64); ++s) {
+    const int kbps = static_cast<int>(ceil_div(pl.KB, s));
+    if (static_cast<int64_t>(s - 1) * kbps >= pl.KB) continue;   // would leave an empty split
+    const int64_t units = tiles * s;
+    const int64_t active = std::min<int64_t>(units, sms);
+    const double waves = std::ceil(static_cast<double>(units) / sms);
+    const double t_unit = std::max(kbps * kb_bytes / (hbm / active), kbps * kb_flops / sm_flops);
+    double t = waves * t_unit;
+    if (s > 1) {
+      const double pbytes = static_cast<double>(units) * 128 * bt * 4;
+      t += 2 * pbytes / hbm + s * 128.0 * bt * 4 / sm_l2;
+    }
+    if (forced ? (s == forced) : (t < best_t * 0.97)) {
+      best_t = t;
+      best_s = s;
+    }
+  }
+  if (forced && forced <= pl.KB) best_s = forced;
+  pl.splits = best_s;
+  pl.kb_per_split = static_cast<int>(ceil_div(pl.KB, best_s));
+  pl.splits = static_cast<int>(ceil_div(pl.KB, pl.kb_per_split));  // no empty split
+  pl.units = static_cast<int>(tiles * pl.splits);
+  pl.grid = std::min(pl.units, sms);
+  if (pl.splits > 1) {
+    pl.counters_bytes = round_up(static_cast<size_t>(tiles) * 4, 256);
+    pl.ws_bytes = pl.counters_bytes + static_cast<size_t>(pl.units) * 128 * bt * 4;
+  }
+  return pl;
+}
+
+int launch_gemm_w4a8(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M, int64_t N, int64_t K,
+                     uint16_t *c, int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st) {
+  switch (pl.BT) {
+    case 16: return w4a8::launch_bt<16>(q, s, packed, M, N, K, c, ldc, ws, pl, st);
+    case 32: return w4a8::launch_bt<32>(q, s, packed, M, N, K, c, ldc, ws, pl, st);
+    case 64: return w4a8::launch_bt<64>(q, s, packed, M, N, K, c, ldc, ws, pl, st);
+    case 128: return w4a8::launch_bt<128>(q, s, packed, M, N, K, c, ldc, ws, pl, st);
+    case 256: return w4a8::launch_bt<256>(q, s, packed, M, N, K, c, ldc, ws, pl, st);
+    default: return R4_ERR_INVALID_ARG;
+  }
+}
+
+}  // namespace r4

@@ -1,0 +1,264 @@
+// quant.cu -- e4m3 activation quantization (per token / per token per 128 K)
+// and the load-time weight quantizers (OCP MX FP4, 128x128 block e4m3).
+//
+// Activation rule ("radiance_mxfp4.py", _traced_quant and the comment above
+// it): s = max(amax/448, 1/(448*512)) in fp32, q = e4m3_rne_sat(x / s). Both
+// divisions are correctly rounded (__fdiv_rn) so the codes are bit-exact
+// against any other correctly rounded fp32 implementation.
+//
+// HBM-bound: 2 bytes read, 1 byte (+ scales) written per element. One CTA per
+// row keeps the whole row in registers (read once), with 16-byte vector loads.
+
+#include <cuda_bf16.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+
+#include "r4_device.cuh"
+#include "r4_internal.h"
+
+namespace r4 {
+namespace {
+
+constexpr float kFp8Max = 448.0f;
+constexpr float kMinScale = 1.0f / 229376.0f;  // 1 / (448 * 512)
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ float absmax8(const uint4 &v) {
+  const uint32_t m = 0x7FFF7FFFu;
+  float a = fmaxf(bf16lo(v.x & m), bf16hi(v.x & m));
+  a = fmaxf(a, fmaxf(bf16lo(v.y & m), bf16hi(v.y & m)));
+  a = fmaxf(a, fmaxf(bf16lo(v.z & m), bf16hi(v.z & m)));
+  a = fmaxf(a, fmaxf(bf16lo(v.w & m), bf16hi(v.w & m)));
+  return a;
+}
+
+__device__ __forceinline__ uint32_t e4m3_of(float v) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// 8 bf16 -> 8 e4m3 codes (element i in byte i), each x/s correctly rounded.
+__device__ __forceinline__ uint2 quant8(const uint4 &v, float sc) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t b[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    b[2 * i] = e4m3_of(__fdiv_rn(bf16lo(w[i]), sc));
+    b[2 * i + 1] = e4m3_of(__fdiv_rn(bf16hi(w[i]), sc));
+  }
+  uint2 r;
+  r.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+  r.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+  return r;
+}
+
+__device__ __forceinline__ float warp_max(float a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  return a;
+}
+
+// One CTA per row; VPT 16-byte vectors per thread stay in registers.
+template <int VPT>
+__global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restrict__ x, int K, int64_t ldx,
+                                                        int group, uint8_t *__restrict__ q,
+                                                        float *__restrict__ s) {
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nt = blockDim.x;
+  const uint16_t *xr = x + static_cast<size_t>(row) * ldx;
+  uint8_t *qr = q + static_cast<size_t>(row) * K;
+  uint4 v[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int k = (i * nt + tid) * 8;
+    v[i] = (k < K) ? __ldg(reinterpret_cast<const uint4 *>(xr + k)) : make_uint4(0, 0, 0, 0);
+  }
+  if (group == K) {
+    __shared__ float red[8];
+    float a = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) a = fmaxf(a, absmax8(v[i]));
+    a = warp_max(a);
+    if ((tid & 31) == 0) red[tid >> 5] = a;
+    __syncthreads();
+    a = red[0];
+    for (int w = 1; w < (nt >> 5); ++w) a = fmaxf(a, red[w]);
+    const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
+    if (tid == 0) s[row] = sc;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int k = (i * nt + tid) * 8;
+      if (k < K) *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc);
+    }
+  } else {
+    // group of 128 = 16 lanes x 8 elements; nt is a multiple of 32
+    const int groups = K / 128;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int k = (i * nt + tid) * 8;
+      float a = absmax8(v[i]);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
+      if (k < K) {
+        if ((tid & 15) == 0) s[static_cast<size_t>(row) * groups + (k >> 7)] = sc;
+        *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc);
+      }
+    }
+  }
+}
+
+// Two-pass variant for rows too long to hold in registers (re-reads x).
+__global__ void __launch_bounds__(256) quant_act_long_kernel(const uint16_t *__restrict__ x, int K, int64_t ldx,
+                                                             int group, uint8_t *__restrict__ q,
+                                                             float *__restrict__ s) {
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nt = blockDim.x;
+  const uint16_t *xr = x + static_cast<size_t>(row) * ldx;
+  uint8_t *qr = q + static_cast<size_t>(row) * K;
+  if (group == K) {
+    __shared__ float red[8];
+    float a = 0.f;
+    for (int k = tid * 8; k < K; k += nt * 8) a = fmaxf(a, absmax8(__ldg(reinterpret_cast<const uint4 *>(xr + k))));
+    a = warp_max(a);
+    if ((tid & 31) == 0) red[tid >> 5] = a;
+    __syncthreads();
+    a = red[0];
+    for (int w = 1; w < (nt >> 5); ++w) a = fmaxf(a, red[w]);
+    const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
+    if (tid == 0) s[row] = sc;
+    for (int k = tid * 8; k < K; k += nt * 8)
+      *reinterpret_cast<uint2 *>(qr + k) = quant8(__ldg(reinterpret_cast<const uint4 *>(xr + k)), sc);
+  } else {
+    const int groups = K / 128;
+    for (int base = 0; base < K; base += nt * 8) {
+      const int k = base + tid * 8;
+      const uint4 v = (k < K) ? __ldg(reinterpret_cast<const uint4 *>(xr + k)) : make_uint4(0, 0, 0, 0);
+      float a = absmax8(v);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
+      if (k < K) {
+        if ((tid & 15) == 0) s[static_cast<size_t>(row) * groups + (k >> 7)] = sc;
+        *reinterpret_cast<uint2 *>(qr + k) = quant8(v, sc);
+      }
+    }
+  }
+}
+
+// OCP MX FP4: one thread per 32-element block.
+__global__ void quant_mxfp4_weight_kernel(const float *__restrict__ w, int64_t N, int64_t K,
+                                          uint8_t *__restrict__ packed, uint8_t *__restrict__ scale) {
+  const int64_t nblk = K / 32;
+  const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (b >= N * nblk) return;
+  const int64_t row = b / nblk, kb = b % nblk;
+  const float4 *src = reinterpret_cast<const float4 *>(w + row * K + kb * 32);
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 f = __ldg(src + i);
+    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int X = 0;
+  if (amax > 0.f) {
+    int e;
+    frexpf(amax, &e);        // amax = m 2^e, 0.5 <= m < 1
+    X = (e - 1) - 2;         // floor(log2 amax) - emax(e2m1)
+  }
+  int code = X + 127;
+  code = code < 0 ? 0 : (code > 254 ? 254 : code);
+  X = code - 127;
+  uint32_t out[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t c =
+        static_cast<uint32_t>(__nv_cvt_float_to_fp4(ldexpf(v[i], -X), __NV_E2M1, cudaRoundNearest)) & 0xFu;
+    out[i / 8] |= c << (4 * (i % 8));
+  }
+  *reinterpret_cast<uint4 *>(packed + row * (K / 2) + kb * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+  scale[row * nblk + kb] = static_cast<uint8_t>(code);
+}
+
+// 128x128 block e4m3: one CTA (256 threads) per block.
+__global__ void __launch_bounds__(256) quant_blockfp8_weight_kernel(const float *__restrict__ w, int64_t N,
+                                                                    int64_t K, uint8_t *__restrict__ q,
+                                                                    float *__restrict__ s) {
+  const int64_t nb = blockIdx.y, kb = blockIdx.x;
+  const int tid = threadIdx.x;
+  __shared__ float red[8];
+  float a = 0.f;
+  for (int i = tid; i < 128 * 32; i += 256) {   // 128 rows x 32 float4
+    const int r = i / 32, c4 = i % 32;
+    const float4 f = __ldg(reinterpret_cast<const float4 *>(w + (nb * 128 + r) * K + kb * 128) + c4);
+    a = fmaxf(a, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+  }
+  a = warp_max(a);
+  if ((tid & 31) == 0) red[tid >> 5] = a;
+  __syncthreads();
+  a = red[0];
+  for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i]);
+  float sc = __fdiv_rn(a, kFp8Max);
+  if (sc == 0.f) sc = 1.f;
+  if (tid == 0) s[nb * (K / 128) + kb] = sc;
+  for (int i = tid; i < 128 * 32; i += 256) {
+    const int r = i / 32, c4 = i % 32;
+    const float4 f = __ldg(reinterpret_cast<const float4 *>(w + (nb * 128 + r) * K + kb * 128) + c4);
+    const uint32_t b = e4m3_of(__fdiv_rn(f.x, sc)) | (e4m3_of(__fdiv_rn(f.y, sc)) << 8) |
+                       (e4m3_of(__fdiv_rn(f.z, sc)) << 16) | (e4m3_of(__fdiv_rn(f.w, sc)) << 24);
+    *reinterpret_cast<uint32_t *>(q + (nb * 128 + r) * K + kb * 128 + c4 * 4) = b;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int64_t group, uint8_t *q,
+                             float *s, cudaStream_t st) {
+  const int64_t vecs = K / 8;
+  int threads = static_cast<int>(vecs < 256 ? ((vecs + 31) / 32) * 32 : 256);
+  if (threads < 32) threads = 32;
+  const int64_t per = ceil_div(vecs, threads);
+  const dim3 grid(static_cast<unsigned>(M));
+  const int g = static_cast<int>(group), k = static_cast<int>(K);
+  if (per <= 1) {
+    quant_act_kernel<1><<<grid, threads, 0, st>>>(x, k, ldx, g, q, s);
+    set_last_kernel("quant_act_kernel<1>");
+  } else if (per <= 2) {
+    quant_act_kernel<2><<<grid, threads, 0, st>>>(x, k, ldx, g, q, s);
+    set_last_kernel("quant_act_kernel<2>");
+  } else if (per <= 4) {
+    quant_act_kernel<4><<<grid, threads, 0, st>>>(x, k, ldx, g, q, s);
+    set_last_kernel("quant_act_kernel<4>");
+  } else if (per <= 9) {
+    quant_act_kernel<9><<<grid, threads, 0, st>>>(x, k, ldx, g, q, s);
+    set_last_kernel("quant_act_kernel<9>");
+  } else {
+    quant_act_long_kernel<<<grid, threads, 0, st>>>(x, k, ldx, g, q, s);
+    set_last_kernel("quant_act_long_kernel");
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_mxfp4_weight(const float *w, int64_t N, int64_t K, uint8_t *packed, uint8_t *scale,
+                                      cudaStream_t st) {
+  const int64_t blocks = N * (K / 32);
+  quant_mxfp4_weight_kernel<<<static_cast<unsigned>(ceil_div(blocks, 256)), 256, 0, st>>>(w, N, K, packed, scale);
+  set_last_kernel("quant_mxfp4_weight_kernel");
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_blockfp8_weight(const float *w, int64_t N, int64_t K, uint8_t *q, float *s,
+                                         cudaStream_t st) {
+  const dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
+  quant_blockfp8_weight_kernel<<<grid, 256, 0, st>>>(w, N, K, q, s);
+  set_last_kernel("quant_blockfp8_weight_kernel");
+  return cudaGetLastError();
+}
+
+}  // namespace r4

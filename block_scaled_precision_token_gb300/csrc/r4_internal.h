@@ -1,0 +1,89 @@
+// r4_internal.h -- host-side declarations shared by the library's translation
+// units: schedule plans, tensor-map encoding, kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/r4q.h"
+
+namespace r4 {
+
+// ------------------------------------------------------------------ device info
+int device_sm_count();           // SM count of the current device (cached per device)
+int *device_error_word();        // device address of the error word (current device)
+void set_last_kernel(const char *name);
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, kernel).
+cudaError_t ensure_smem_attr(const void *func, int bytes);
+
+// Encode a tiled tensor map through the driver entry point (no libcuda link).
+CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank, void *gaddr,
+                      const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                      CUtensorMapSwizzle swizzle);
+
+// ------------------------------------------------------------------ options
+struct Options {
+  int w4a8_splits = 0;      // 0 = automatic
+  int w4a8_token_tile = 0;  // 0 = automatic
+  int fp8_splits = 0;       // 0 = automatic
+};
+Options &options();
+
+// ------------------------------------------------------------------ plans
+// One output tile = 128 weight rows (n) x BT tokens (t). A work unit is a
+// tile and a contiguous range of 128-K blocks (its split).
+struct GemmPlan {
+  int BT = 0;            // token tile (MMA N)
+  int n_tiles = 0, t_tiles = 0;
+  int KB = 0;            // number of 128-K blocks (K padded to 128)
+  int splits = 1, kb_per_split = 0;
+  int units = 0, grid = 0;
+  size_t counters_bytes = 0;  // arrival counters (one int per tile), 256-B rounded
+  size_t ws_bytes = 0;        // total workspace (0 when splits == 1)
+};
+
+GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms);
+GemmPlan plan_blockfp8(int64_t M, int64_t N, int64_t K, int sms);
+
+// ------------------------------------------------------------------ prepack layout
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+constexpr int64_t kMxTileCodeBytes = 128 * 64;   // 128 rows x 128 K packed e2m1
+constexpr int64_t kMxTileSfBytes = 512;          // 128 rows x 4 ue8m0, copy order
+constexpr int64_t kFp8TileBytes = 128 * 128;     // 128 rows x 128 K e4m3
+
+inline size_t mx_packed_codes_bytes(int64_t N, int64_t K) {
+  return static_cast<size_t>(ceil_div(N, 128) * ceil_div(K, 128) * kMxTileCodeBytes);
+}
+inline size_t mx_packed_bytes(int64_t N, int64_t K) {
+  return mx_packed_codes_bytes(N, K) + static_cast<size_t>(ceil_div(N, 128) * ceil_div(K, 128) * kMxTileSfBytes);
+}
+inline size_t fp8_packed_codes_bytes(int64_t N, int64_t K) { return static_cast<size_t>(N * K); }
+inline size_t fp8_packed_bytes(int64_t N, int64_t K) {
+  return round_up(fp8_packed_codes_bytes(N, K) + static_cast<size_t>((N / 128) * (K / 128) * 4), 256);
+}
+
+// ------------------------------------------------------------------ launchers
+// All return cudaSuccess or the launch error; arguments are already validated.
+cudaError_t launch_quant_act(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int64_t group, uint8_t *q,
+                             float *s, cudaStream_t st);
+cudaError_t launch_quant_mxfp4_weight(const float *w, int64_t N, int64_t K, uint8_t *packed, uint8_t *scale,
+                                      cudaStream_t st);
+cudaError_t launch_quant_blockfp8_weight(const float *w, int64_t N, int64_t K, uint8_t *q, float *s,
+                                         cudaStream_t st);
+cudaError_t launch_prepack_mxfp4(const uint8_t *w, const uint8_t *ws, int64_t N, int64_t K, uint8_t *packed,
+                                 cudaStream_t st);
+cudaError_t launch_prepack_blockfp8(const uint8_t *w, const float *ws, int64_t N, int64_t K, uint8_t *packed,
+                                   cudaStream_t st);
+// Returns an r4_status (tensor-map encoding can fail with R4_ERR_CUDA).
+int launch_gemm_w4a8(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M, int64_t N, int64_t K,
+                     uint16_t *c, int64_t ldc, void *ws, const GemmPlan &plan, cudaStream_t st);
+int launch_gemm_blockfp8(const uint8_t *q, const float *As, const uint8_t *packed, int64_t M, int64_t N,
+                         int64_t K, uint16_t *c, int64_t ldc, void *ws, const GemmPlan &plan, cudaStream_t st);
+cudaError_t launch_gemm_skinny(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N, int64_t K, uint16_t *c,
+                               int64_t ldc, cudaStream_t st);
+
+}  // namespace r4

@@ -1,0 +1,203 @@
+/*
+ * r4q.h -- C ABI of the GB300 (sm_103a) block-scaled quantized linear library.
+ *
+ * The library computes the quantized linear-layer hot path described on the
+ * pages "radiance_mxfp4.py" (W4A8 MXFP4 linear with per-token e4m3
+ * activations), "radiance_kernels.py" (block-FP8 W8A8 GEMM, block_scaled_mm)
+ * and "radiance_gemm.py" (skinny bf16 NT GEMM), re-designed for tcgen05
+ * tensor cores, TMA and HBM3e.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise. All
+ *    buffers are allocated and owned by the caller; the library never
+ *    allocates device memory, never synchronizes the device or a stream, and
+ *    never throws. This keeps every call legal inside CUDA-graph capture.
+ *  - Every kernel is launched on `stream` (a cudaStream_t; 0 = legacy default
+ *    stream). Results are ready when the stream reaches that point.
+ *  - bf16 tensors are passed as uint16_t bit patterns, e4m3 / e2m1 / ue8m0
+ *    codes as uint8_t. Matrices are row-major; "ld" arguments are row strides
+ *    in elements.
+ *  - Every call returns an R4_* status. On an error nothing is launched, except
+ *    R4_ERR_CUDA, which reports a failure of the launch itself.
+ *  - A device-side wait that runs out (a TMA or tensor-core completion that
+ *    never arrives) makes the kernel stop early and set a device error word;
+ *    r4_device_error() reads and clears it.
+ */
+#ifndef R4Q_H
+#define R4Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *r4_stream_t; /* == cudaStream_t */
+
+enum r4_status {
+  R4_OK = 0,
+  R4_ERR_INVALID_ARG = 1,       /* null pointer, non-positive or inconsistent size */
+  R4_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported set (see each call) */
+  R4_ERR_MISALIGNED = 3,        /* pointer or stride alignment rule broken */
+  R4_ERR_WORKSPACE = 4,         /* workspace or prepack buffer too small */
+  R4_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed */
+  R4_ERR_DEVICE_TIMEOUT = 6     /* a kernel's bounded device-side wait ran out */
+};
+
+/* GEMM identifiers for r4_gemm_workspace_bytes(). */
+enum r4_gemm_op { R4_OP_W4A8_MXFP4 = 1, R4_OP_BLOCKFP8 = 2, R4_OP_BF16_SKINNY = 3 };
+
+int r4_version(void);                 /* (major << 16) | minor */
+const char *r4_status_string(int status);
+/* Name of the kernel the last successful launch on this host thread used. */
+const char *r4_last_kernel_name(void);
+
+/*
+ * r4_device_error -- read (and with clear != 0, reset) the device error word
+ * of the current device. 0 means no kernel has reported a timed-out wait.
+ * Synchronous (it copies one word from the device): not for use in capture.
+ */
+int r4_device_error(int *error_out, int clear);
+
+/*
+ * r4_quant_fp8_per_token -- dynamic e4m3 activation quantization.
+ * Source: "radiance_mxfp4.py", _traced_quant and the comment above it:
+ *   s = max(amax(|x|) / 448, 1/(448*512))   (fp32, correctly rounded division)
+ *   q = e4m3_rne(x / s), finite values saturate at +-448.
+ * With group == K there is one scale per row (token); with group == 128 there
+ * is one scale per token per 128 K, the activation side of block-FP8
+ * ("radiance_kernels.py", block_scaled_mm).
+ *   x     bf16 [M, ldx], row-major, first K columns used.  16-byte aligned.
+ *   q     e4m3 [M, K] row-major (row stride K).            16-byte aligned.
+ *   s     fp32 [M, K/group] row-major.
+ * Requirements: M >= 1, K >= 8, K % 8 == 0, ldx >= K, ldx % 8 == 0,
+ * group == K or (group == 128 and K % 128 == 0).
+ * Non-finite input gives unspecified codes for that row (NaN poisons the scale).
+ */
+int r4_quant_fp8_per_token(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                           int64_t group, uint8_t *q, float *s, r4_stream_t stream);
+
+/*
+ * r4_quantize_mxfp4_weight -- OCP MX FP4 quantization of a float32 weight
+ * (a load-time utility, not on the per-token path): per 32-element block of a
+ * row, X = floor(log2(amax)) - 2 (all-zero block: X = 0), scale code X + 127
+ * clamped to [0, 254], element = e2m1_rne_sat(w / 2^X).
+ *   w       fp32 [N, K] row-major.
+ *   packed  uint8 [N, K/2]: element 2j in the low nibble of byte j
+ *           ("radiance_mxfp4.py", _exact_ref).
+ *   scale   uint8 [N, K/32] ue8m0 (value 2^(code-127)).
+ * Requirements: N >= 1, K % 32 == 0.
+ */
+int r4_quantize_mxfp4_weight(const float *w, int64_t N, int64_t K, uint8_t *packed,
+                             uint8_t *scale, r4_stream_t stream);
+
+/*
+ * r4_quantize_blockfp8_weight -- 128x128 block e4m3 weight quantization
+ * (load-time utility): s = amax/448 in fp32 (1 for an all-zero block),
+ * q = e4m3_rne_sat(w / s).
+ *   w      fp32 [N, K];  q  uint8 [N, K];  s  fp32 [N/128, K/128] (multiplier).
+ * Requirements: N % 128 == 0, K % 128 == 0.
+ */
+int r4_quantize_blockfp8_weight(const float *w, int64_t N, int64_t K, uint8_t *q,
+                                float *s, r4_stream_t stream);
+
+/*
+ * r4_prepack_mxfp4 -- one-time permutation of a checkpoint-order MXFP4 weight
+ * into the GEMM-native layout (no re-quantization). Source of the idea:
+ * "radiance_mxfp4.py", permute_w (a byte permutation done once at load so the
+ * kernel's weight reads are contiguous). The layout here is the TMA/tcgen05
+ * one: 128-row x 128-K tiles of packed codes (8 KiB each, tile-major along K)
+ * followed by one 512-byte scale atom per tile in tensor-memory copy order.
+ * Rows beyond N and K beyond the true K are padded with code 0 / scale 127.
+ *   w        uint8 [N, K/2] packed e2m1, checkpoint order.
+ *   w_scale  uint8 [N, K/32] ue8m0, checkpoint order [N, K/32].
+ *   packed   output buffer of at least r4_prepack_mxfp4_bytes(N, K) bytes,
+ *            256-byte aligned. Opaque: only r4_gemm_w4a8_mxfp4 reads it.
+ * Requirements: N >= 1, K >= 32, K % 32 == 0.
+ */
+size_t r4_prepack_mxfp4_bytes(int64_t N, int64_t K);
+int r4_prepack_mxfp4(const uint8_t *w, const uint8_t *w_scale, int64_t N, int64_t K,
+                     void *packed, size_t packed_bytes, r4_stream_t stream);
+
+/*
+ * r4_prepack_blockfp8 -- one-time permutation of an e4m3 [N, K] weight into
+ * 128x128 K-major tiles (16 KiB each, tile-major along K), followed by a copy
+ * of the fp32 block scales. Source: "radiance_kernels.py", the preshuffle load
+ * hook (only genuine 128-block weights: N % 128 == 0, K % 128 == 0, scale
+ * [N/128, K/128]).
+ *   w        uint8 [N, K] e4m3.   w_scale  fp32 [N/128, K/128].
+ *   packed   >= r4_prepack_blockfp8_bytes(N, K) bytes, 256-byte aligned.
+ */
+size_t r4_prepack_blockfp8_bytes(int64_t N, int64_t K);
+int r4_prepack_blockfp8(const uint8_t *w, const float *w_scale, int64_t N, int64_t K,
+                        void *packed, size_t packed_bytes, r4_stream_t stream);
+
+/*
+ * r4_gemm_workspace_bytes -- device workspace a GEMM call needs for (M, N, K):
+ * split-K fp32 partials plus one int32 arrival counter per output tile. 0 when
+ * the chosen schedule needs none. The counters must be zero when the
+ * workspace is first used (e.g. cudaMemsetAsync once after allocation); every
+ * call leaves them zero again. One workspace must not serve two calls that can
+ * run at the same time (two streams).
+ */
+size_t r4_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
+
+/*
+ * r4_gemm_w4a8_mxfp4 -- C = bf16( s[m] * sum_k e4m3(q[m,k]) * e2m1(w[n,k]) * 2^(e[n,k/32]-127) ).
+ * Source: "radiance_mxfp4.py", module docstring and _exact_ref.
+ * Runs on tcgen05 block-scaled MMA (kind::mxf8f6f4, ue8m0 scale per 32 K) with
+ * the weight as the 128-row MMA operand; token tiles of 16..256; split-K with
+ * a last-arriving-CTA reduction when there are too few output tiles to fill
+ * the GPU. Decode (M <= 64) and prefill use the same kernel.
+ *   q       e4m3 [M, K] row-major (from r4_quant_fp8_per_token), 16-B aligned.
+ *   s       fp32 [M] per-token scale.
+ *   packed  prepacked weight from r4_prepack_mxfp4(N, K).
+ *   c       bf16 [M, ldc] row-major; columns [0, N) are written, nothing else.
+ * Requirements: M >= 1, N >= 1, K % 32 == 0, ldc >= N.
+ */
+int r4_gemm_w4a8_mxfp4(const uint8_t *q, const float *s, const void *packed, int64_t M,
+                       int64_t N, int64_t K, uint16_t *c, int64_t ldc, void *workspace,
+                       size_t workspace_bytes, r4_stream_t stream);
+
+/*
+ * r4_gemm_blockfp8 -- C = bf16( sum_kb As[m,kb] * Ws[n/128,kb] * sum_{k in kb} e4m3(q[m,k]) e4m3(w[n,k]) ).
+ * Source: "radiance_kernels.py", block_scaled_mm.
+ * tcgen05 kind::f8f6f4 MMA per 128-K block into a fresh tensor-memory
+ * accumulator, promoted into fp32 registers with the scale product by the
+ * epilogue warps (double-buffered so promotion overlaps the next block's MMA).
+ *   q   e4m3 [M, K];  As fp32 [M, K/128] row-major (from group-128 quant);
+ *   packed from r4_prepack_blockfp8(N, K);  c bf16 [M, ldc].
+ * Requirements: N % 128 == 0, K % 128 == 0, M >= 1, ldc >= N.
+ */
+int r4_gemm_blockfp8(const uint8_t *q, const float *As, const void *packed, int64_t M,
+                     int64_t N, int64_t K, uint16_t *c, int64_t ldc, void *workspace,
+                     size_t workspace_bytes, r4_stream_t stream);
+
+/*
+ * r4_gemm_bf16_nt_skinny -- C = bf16( x W^T ) with fp32 accumulation, for tiny
+ * projections. Source: "radiance_gemm.py", module docstring (C[M,N] =
+ * x[M,K] @ W[N,K]^T, split-K because a sub-megabyte weight otherwise leaves the
+ * GPU idle). Split-K across a thread-block cluster, reduced through
+ * distributed shared memory: needs no workspace (pass NULL, 0).
+ *   x  bf16 [M, K] row-major (row stride K);  w  bf16 [N, K] row-major;
+ *   c  bf16 [M, ldc].  x and w 16-byte aligned.
+ * Requirements: 1 <= M <= 64, N >= 1, K % 256 == 0, ldc >= N.
+ */
+int r4_gemm_bf16_nt_skinny(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N,
+                           int64_t K, uint16_t *c, int64_t ldc, void *workspace,
+                           size_t workspace_bytes, r4_stream_t stream);
+
+/*
+ * r4_set_option -- benchmarking overrides of the host-side schedule choice
+ * (process-wide, not thread-safe). key 1: force the W4A8 split-K factor
+ * (0 = automatic); key 2: force the W4A8 token tile (0 = automatic, else
+ * 16/32/64/128/256); key 3: force the block-FP8 split-K factor.
+ */
+int r4_set_option(int key, int64_t value);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* R4Q_H */

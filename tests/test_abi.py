@@ -1,0 +1,98 @@
+"""The C-ABI library builds, loads, exports every entry point the header
+declares, and rejects bad arguments on the host (no GPU needed)."""
+
+import ctypes
+import math
+
+import pytest
+
+from block_scaled_precision_token_gb300 import build as B
+
+
+@pytest.fixture(scope="module")
+def r4q():
+    B.build()
+    from block_scaled_precision_token_gb300 import r4q as mod
+    mod.lib()
+    return mod
+
+
+def test_every_header_symbol_is_exported(r4q):
+    syms = r4q.header_symbols()
+    assert len(syms) >= 16
+    lib = r4q.lib()
+    for name in syms:
+        assert hasattr(lib, name), name
+    assert set(syms) == set(r4q._SIGS), "binding and header disagree"
+
+
+def test_version_and_strings(r4q):
+    assert r4q.r4_version() >= 1
+    for st in range(7):
+        assert r4q.status_string(st) and r4q.status_string(st) != "unknown status"
+    assert r4q.status_string(99) == "unknown status"
+
+
+def test_prepack_sizes(r4q):
+    lib = r4q.lib()
+    for N, K in [(256, 2048), (34816, 5120), (300, 416), (1, 32)]:
+        want = math.ceil(N / 128) * math.ceil(K / 128) * (8192 + 512)
+        assert lib.r4_prepack_mxfp4_bytes(N, K) == want
+    assert lib.r4_prepack_mxfp4_bytes(256, 48) == 0          # K % 32
+    assert lib.r4_prepack_blockfp8_bytes(6144, 2048) == 6144 * 2048 + 48 * 16 * 4
+    assert lib.r4_prepack_blockfp8_bytes(100, 2048) == 0
+
+
+def test_options(r4q):
+    lib = r4q.lib()
+    assert lib.r4_set_option(99, 0) == r4q.R4_ERR_INVALID_ARG
+    assert lib.r4_set_option(2, 48) == r4q.R4_ERR_INVALID_ARG
+    assert lib.r4_set_option(2, 64) == 0 and lib.r4_set_option(2, 0) == 0
+    assert lib.r4_set_option(1, 0) == 0 and lib.r4_set_option(3, 0) == 0
+
+
+def test_validation_rejects_before_launch(r4q):
+    lib = r4q.lib()
+    P = ctypes.c_void_p
+    good = P(1 << 20)           # never dereferenced: validation fails first
+    odd = P((1 << 20) + 8)      # 8-byte aligned, not 16
+    S = P(0)
+    # null pointers
+    assert lib.r4_quant_fp8_per_token(None, 8, 2048, 2048, 2048, good, good, S) == r4q.R4_ERR_INVALID_ARG
+    assert lib.r4_gemm_w4a8_mxfp4(good, good, None, 8, 256, 2048, good, 256, None, 0, S) == r4q.R4_ERR_INVALID_ARG
+    assert lib.r4_gemm_bf16_nt_skinny(None, good, 8, 256, 2048, good, 256, None, 0, S) == r4q.R4_ERR_INVALID_ARG
+    # bad sizes
+    assert lib.r4_quant_fp8_per_token(good, 0, 2048, 2048, 2048, good, good, S) == r4q.R4_ERR_INVALID_ARG
+    assert lib.r4_quant_fp8_per_token(good, 8, 2048, 1024, 2048, good, good, S) == r4q.R4_ERR_INVALID_ARG
+    assert lib.r4_gemm_w4a8_mxfp4(good, good, good, 8, 256, 2048, good, 100, None, 0, S) == r4q.R4_ERR_INVALID_ARG
+    # unsupported shapes
+    assert lib.r4_quant_fp8_per_token(good, 8, 2044, 2048, 2044, good, good, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert lib.r4_quant_fp8_per_token(good, 8, 2048, 2048, 64, good, good, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert lib.r4_gemm_w4a8_mxfp4(good, good, good, 8, 256, 2000, good, 256, None, 0, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert lib.r4_gemm_blockfp8(good, good, good, 8, 200, 2048, good, 200, None, 0, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert lib.r4_gemm_bf16_nt_skinny(good, good, 65, 256, 2048, good, 256, None, 0, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert lib.r4_gemm_bf16_nt_skinny(good, good, 8, 256, 2000, good, 256, None, 0, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert lib.r4_prepack_blockfp8(good, good, 200, 256, good, 1 << 30, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    # misalignment
+    assert lib.r4_quant_fp8_per_token(odd, 8, 2048, 2048, 2048, good, good, S) == r4q.R4_ERR_MISALIGNED
+    assert lib.r4_prepack_mxfp4(good, good, 256, 2048, odd, 1 << 30, S) == r4q.R4_ERR_MISALIGNED
+    assert lib.r4_gemm_w4a8_mxfp4(good, good, odd, 8, 256, 2048, good, 256, None, 0, S) == r4q.R4_ERR_MISALIGNED
+    # short prepack buffer
+    assert lib.r4_prepack_mxfp4(good, good, 256, 2048, good, 100, S) == r4q.R4_ERR_WORKSPACE
+    assert lib.r4_prepack_blockfp8(good, good, 256, 256, good, 100, S) == r4q.R4_ERR_WORKSPACE
+
+
+def test_product_path_has_no_oracle_import():
+    """The package must not import the oracle (or any CPU fallback)."""
+    import ast
+    import os
+    pkg = os.path.dirname(B.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith(".py"):
+                tree = ast.parse(open(os.path.join(root, f)).read())
+                for node in ast.walk(tree):
+                    if isinstance(node, ast.Import):
+                        assert not any(a.name.split(".")[0] == "oracle" for a in node.names), f
+                    if isinstance(node, ast.ImportFrom):
+                        assert (node.module or "").split(".")[0] != "oracle", f

@@ -1,0 +1,95 @@
+"""GPU parity: block-FP8 W8A8 GEMM (tcgen05 kind::f8f6f4 + register promotion)."""
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_precision_token_gb300 import synth
+from oracle import gemm as G
+from oracle import quant as Q
+from tests.gpu_util import assert_gemm_matches, check_device_error, random_e4m3_codes, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def r4q():
+    m = require_gpu()
+    yield m
+    m.r4_set_option(3, 0)
+
+
+def _run(r4q, q_np, As_np, w_np, Ws_np, N, K):
+    q = torch.from_numpy(q_np).cuda()
+    As = torch.from_numpy(np.ascontiguousarray(As_np, np.float32)).cuda()
+    pk = r4q.prepack_blockfp8(torch.from_numpy(w_np).cuda(), torch.from_numpy(np.asarray(Ws_np, np.float32)).cuda(),
+                              N, K)
+    c = r4q.gemm_blockfp8(q, As, pk, N, K)
+    check_device_error(r4q)
+    return c
+
+
+def _inputs(M, N, K, seed=0):
+    x = synth.activations(M, K, synth.CFG_BLOCKFP8, outliers=False, seed=1000 + synth.CFG_BLOCKFP8 + seed)
+    q, As = Q.quant_act(x.float().numpy(), group=128)
+    w = synth.weights_fp32(N, K, synth.CFG_BLOCKFP8)
+    wq, Ws = Q.quant_blockfp8_w(w.numpy())
+    return q, As, wq, Ws
+
+
+def test_scale_placement_one_hot(r4q):
+    M, N, K = 8, 256, 384
+    q = np.zeros((M, K), np.uint8)
+    w = np.zeros((N, K), np.uint8)
+    q[:, 130] = 0x38
+    q[:, 300] = 0x40
+    w[200, 130] = 0x38
+    w[7, 300] = 0x30
+    As = np.arange(1, 1 + M * 3, dtype=np.float32).reshape(M, 3)
+    Ws = np.array([[13, 17, 19], [23, 29, 31]], np.float32)
+    c = _run(r4q, q, As, w, Ws, N, K)
+    c64, _ = G.gemm_blockfp8(q, As, w, Ws)
+    assert_gemm_matches(c, c64, "one-hot")
+
+
+@pytest.mark.parametrize("M", synth.BLOCKFP8_M)
+@pytest.mark.parametrize("N,K", synth.BLOCKFP8_NK)
+def test_workload_shapes(r4q, M, N, K):
+    q, As, wq, Ws = _inputs(M, N, K)
+    c = _run(r4q, q, As, wq, Ws, N, K)
+    rows = None if M <= 64 else synth.sample_indices(N, 256, 5).numpy()
+    c64, _ = G.gemm_blockfp8(q, As, wq, Ws, rows=rows)
+    got = c if rows is None else c[:, torch.from_numpy(rows).cuda()]
+    assert_gemm_matches(got, c64, f"M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 16])
+def test_forced_splits_ragged_m(r4q, splits):
+    M, N, K = 45, 384, 2048
+    q = random_e4m3_codes((M, K), seed=3)
+    As = np.random.default_rng(4).uniform(1e-3, 1e-2, (M, K // 128)).astype(np.float32)
+    w = random_e4m3_codes((N, K), seed=5)
+    Ws = np.random.default_rng(6).uniform(1e-4, 1e-3, (N // 128, K // 128)).astype(np.float32)
+    r4q.r4_set_option(3, splits)
+    try:
+        c = _run(r4q, q, As, w, Ws, N, K)
+        c2 = _run(r4q, q, As, w, Ws, N, K)
+    finally:
+        r4q.r4_set_option(3, 0)
+    c64, _ = G.gemm_blockfp8(q, As, w, Ws)
+    assert_gemm_matches(c, c64, f"splits={splits}")
+    assert torch.equal(c, c2)
+
+
+def test_end_to_end_group_quant(r4q):
+    M, N, K = 64, 2048, 6144
+    x = synth.activations(M, K, synth.CFG_BLOCKFP8)
+    w = synth.weights_fp32(N, K, synth.CFG_BLOCKFP8)
+    wq, Ws = Q.quant_blockfp8_w(w.numpy())
+    qg, Asg = r4q.quant_fp8(x.cuda(), group=128)
+    pk = r4q.prepack_blockfp8(torch.from_numpy(wq).cuda(), torch.from_numpy(Ws).cuda(), N, K)
+    c = r4q.gemm_blockfp8(qg, Asg, pk, N, K)
+    check_device_error(r4q)
+    q, As = Q.quant_act(x.float().numpy(), group=128)
+    c64, _ = G.gemm_blockfp8(q, As, wq, Ws)
+    assert_gemm_matches(c, c64, "end-to-end")

@@ -1,0 +1,89 @@
+"""GPU parity: e4m3 activation quantization and the weight quantizers must be
+bit-exact against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_precision_token_gb300 import synth
+from oracle import quant as Q
+from tests.gpu_util import check_device_error, np_f32, np_u8, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def r4q():
+    return require_gpu()
+
+
+def _x(M, K, cfg, outliers, seed=None):
+    return synth.activations(M, K, cfg, outliers=outliers, seed=seed)
+
+
+@pytest.mark.parametrize("M,K,outliers", [
+    (8, 2048, False),        # tiny W4A8 workload
+    (6, 5120, True), (64, 5120, True), (64, 17408, True),   # decode shapes
+    (37, 384, True),         # ragged M, short K
+    (1, 8, False),           # minimum
+    (3, 40000, False),       # row longer than the register-resident path
+    (256, 5120, True),
+])
+def test_per_token_bit_exact(r4q, M, K, outliers):
+    x = _x(M, K, synth.CFG_DECODE, outliers)
+    q_ref, s_ref = Q.quant_act(x.float().numpy())
+    q, s = r4q.quant_fp8(x.cuda())
+    check_device_error(r4q)
+    assert np.array_equal(np_f32(s), s_ref)
+    assert np.array_equal(np_u8(q), q_ref)
+
+
+@pytest.mark.parametrize("M,K", [(8, 2048), (64, 6144), (2048, 4096), (5, 128), (33, 4096 + 128)])
+def test_group128_bit_exact(r4q, M, K):
+    x = _x(M, K, synth.CFG_BLOCKFP8, False)
+    q_ref, s_ref = Q.quant_act(x.float().numpy(), group=128)
+    q, s = r4q.quant_fp8(x.cuda(), group=128)
+    check_device_error(r4q)
+    assert np.array_equal(np_f32(s), s_ref)
+    assert np.array_equal(np_u8(q), q_ref)
+
+
+def test_special_rows_and_row_stride(r4q):
+    M, K, ld = 6, 1024, 1040
+    base = _x(M, ld, synth.CFG_DECODE, False, seed=77).float()
+    base[1] = 0.0                      # zero row -> minimum scale
+    base[2] = 3.5                      # constant row -> every code 448
+    base[3] = -base[3].abs()           # all negative
+    base[4, :] = 0.0
+    base[4, 5] = 1e-30                 # tiny amax
+    xb = base.to(torch.bfloat16)
+    view = xb.cuda()[:, :K]            # row stride ld > K
+    q_ref, s_ref = Q.quant_act(xb[:, :K].float().numpy())
+    q, s = r4q.quant_fp8(view)
+    check_device_error(r4q)
+    assert np.array_equal(np_f32(s), s_ref)
+    assert np.array_equal(np_u8(q), q_ref)
+    assert np.all(np_u8(q)[2] == 0x7E)
+
+
+@pytest.mark.parametrize("N,K", [(256, 2048), (100, 96), (2048, 5120)])
+def test_mxfp4_weight_quant_bit_exact(r4q, N, K):
+    w = synth.weights_fp32(N, K, synth.CFG_TINY)
+    w[3, :32] = 0.0                    # an all-zero block
+    w[5, 40] = 10.0                    # saturating outlier block
+    p_ref, s_ref = Q.quant_mxfp4_ocp(w.numpy())
+    p, s = r4q.quantize_mxfp4_weight(w.cuda())
+    check_device_error(r4q)
+    assert np.array_equal(np_u8(s), s_ref)
+    assert np.array_equal(np_u8(p), p_ref)
+
+
+@pytest.mark.parametrize("N,K", [(256, 256), (2048, 6144)])
+def test_blockfp8_weight_quant_bit_exact(r4q, N, K):
+    w = synth.weights_fp32(N, K, synth.CFG_BLOCKFP8)
+    w[128:256, 128:256] = 0.0
+    c_ref, s_ref = Q.quant_blockfp8_w(w.numpy())
+    c, s = r4q.quantize_blockfp8_weight(w.cuda())
+    check_device_error(r4q)
+    assert np.array_equal(np_f32(s), s_ref)
+    assert np.array_equal(np_u8(c), c_ref)

@@ -1,0 +1,147 @@
+"""GPU parity: W4A8 MXFP4 GEMM (tcgen05 block-scaled MMA) against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_precision_token_gb300 import synth
+from oracle import formats as F
+from oracle import gemm as G
+from oracle import quant as Q
+from tests.gpu_util import assert_gemm_matches, bf16_to_np, check_device_error, random_e4m3_codes, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def r4q():
+    m = require_gpu()
+    yield m
+    m.r4_set_option(1, 0)
+    m.r4_set_option(2, 0)
+
+
+def _run(r4q, q_np, s_np, packed_np, scale_np, N, K, ldc=None):
+    M = q_np.shape[0]
+    q = torch.from_numpy(q_np).cuda()
+    s = torch.from_numpy(np.asarray(s_np, np.float32)).cuda()
+    pk = r4q.prepack_mxfp4(torch.from_numpy(packed_np).cuda(), torch.from_numpy(scale_np).cuda(), N, K)
+    full = out = None
+    if ldc is not None:
+        full = torch.full((M, ldc), 7.0, dtype=torch.bfloat16, device="cuda")
+        out = full[:, :N]
+    c = r4q.gemm_w4a8(q, s, pk, N, K, out=out)
+    check_device_error(r4q)
+    return c, full
+
+
+def _dense_inputs(M, N, K, cfg, outliers=True):
+    x = synth.activations(M, K, cfg, outliers=outliers)
+    q, s = Q.quant_act(x.float().numpy())
+    w = synth.weights_fp32(N, K, cfg)
+    p, sc = Q.quant_mxfp4_ocp(w.numpy())
+    return q, s, p, sc
+
+
+def test_one_hot_weights(r4q):
+    """One nonzero e2m1 code per weight row, at a row-dependent k (odd and
+    even), with a row-dependent scale: pins nibble order, the scale's 32-K
+    block, the scale's row placement in tensor memory and the transpose."""
+    M, N, K = 16, 256, 256
+    rng = np.random.default_rng(0)
+    q = random_e4m3_codes((M, K), seed=1)
+    s = rng.uniform(0.5, 2.0, M).astype(np.float32)
+    codes = np.zeros((N, K), np.uint8)
+    scale = np.full((N, K // 32), 127, np.uint8)
+    for n in range(N):
+        k = (n * 37 + n // 7) % K
+        codes[n, k] = [1, 2, 3, 4, 5, 6, 7, 9, 10, 11, 12, 13, 14, 15][n % 14]
+        scale[n, k // 32] = 118 + (n % 13)
+    packed = F.pack_e2m1(codes)
+    c, _ = _run(r4q, q, s, packed, scale, N, K)
+    c64, _ = G.gemm_w4a8(q, s, packed, scale)
+    assert_gemm_matches(c, c64, "one-hot")
+
+
+def test_tiny_workload(r4q):
+    M, N, K = synth.TINY["M"], synth.TINY["N"], synth.TINY["K"]
+    q, s, p, sc = _dense_inputs(M, N, K, synth.CFG_TINY, outliers=False)
+    c, _ = _run(r4q, q, s, p, sc, N, K)
+    c64, cb = G.gemm_w4a8(q, s, p, sc, exact_check=True)
+    assert_gemm_matches(c, c64, "tiny")
+    same = np.mean(bf16_to_np(c) == cb)
+    assert same > 0.9, f"only {same:.3f} of outputs equal the oracle's bf16 rounding"
+
+
+def test_ragged_shapes_and_guard_band(r4q):
+    M, N, K = 37, 300, 416
+    q, s, p, sc = _dense_inputs(M, N, K, synth.CFG_DECODE)
+    ldc = 320
+    c, full = _run(r4q, q, s, p, sc, N, K, ldc=ldc)
+    c64, _ = G.gemm_w4a8(q, s, p, sc)
+    assert_gemm_matches(c, c64, "ragged")
+    g = full.float().cpu().numpy()[:, N:]
+    assert np.all(g == 7.0), "kernel wrote outside columns [0, N)"
+
+
+@pytest.mark.parametrize("bt", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("splits", [1, 3, 8])
+def test_forced_tiles_and_splits(r4q, bt, splits):
+    M, N, K = 40, 384, 1024
+    q, s, p, sc = _dense_inputs(M, N, K, synth.CFG_DECODE)
+    r4q.r4_set_option(2, bt)
+    r4q.r4_set_option(1, splits)
+    try:
+        c, _ = _run(r4q, q, s, p, sc, N, K)
+        c2, _ = _run(r4q, q, s, p, sc, N, K)
+    finally:
+        r4q.r4_set_option(1, 0)
+        r4q.r4_set_option(2, 0)
+    c64, _ = G.gemm_w4a8(q, s, p, sc)
+    assert_gemm_matches(c, c64, f"bt={bt} splits={splits}")
+    assert torch.equal(c, c2), "not deterministic across calls"
+
+
+def _sampled_full_size(r4q, M, N, K, seed, nsample=384):
+    q = random_e4m3_codes((M, K), seed=seed)
+    s = (np.random.default_rng(seed).uniform(1e-3, 5e-2, M)).astype(np.float32)
+    packed = synth.uniform_bytes((N, K // 2), seed=seed + 1).numpy()
+    scale = synth.uniform_bytes((N, K // 32), seed=seed + 2, low=117, high=125).numpy()
+    c, _ = _run(r4q, q, s, packed, scale, N, K)
+    rows = synth.sample_indices(N, nsample, seed + 3).numpy()
+    rows = np.unique(np.concatenate([rows, [0, N - 1]]))
+    c64, _ = G.gemm_w4a8(q, s, packed, scale, rows=rows)
+    got = c[:, torch.from_numpy(rows).cuda()]
+    assert_gemm_matches(got, c64, f"M={M} N={N} K={K}")
+    assert torch.isfinite(c.float()).all()
+
+
+@pytest.mark.parametrize("M", [6, 64])
+@pytest.mark.parametrize("N,K", synth.DECODE_NK)
+def test_decode_full_size_sampled(r4q, M, N, K):
+    _sampled_full_size(r4q, M, N, K, seed=100 + M)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 5120, 17408), (256, 34816, 5120), (2048, 10240, 5120),
+                                   (8192, 34816, 5120)])
+def test_prefill_full_size_sampled(r4q, M, N, K):
+    _sampled_full_size(r4q, M, N, K, seed=200 + M, nsample=128)
+
+
+def test_end_to_end_with_gpu_quant(r4q):
+    """x -> GPU quant -> GPU GEMM equals oracle quant -> oracle GEMM (the quant
+    is bit-exact, so the GEMM tolerance applies unchanged)."""
+    M, N, K = 8, 2048, 5120
+    x = synth.activations(M, K, synth.CFG_DECODE, outliers=True)
+    w = synth.weights_fp32(N, K, synth.CFG_DECODE)
+    p, sc = Q.quant_mxfp4_ocp(w.numpy())
+    qg, sg = r4q.quant_fp8(x.cuda())
+    pk = r4q.prepack_mxfp4(torch.from_numpy(p).cuda(), torch.from_numpy(sc).cuda(), N, K)
+    c = r4q.gemm_w4a8(qg, sg, pk, N, K)
+    check_device_error(r4q)
+    q, s = Q.quant_act(x.float().numpy())
+    c64, _ = G.gemm_w4a8(q, s, p, sc)
+    assert_gemm_matches(c, c64, "end-to-end")
+    # the pages' own accuracy measure against the unquantized product
+    ref = x.float().numpy().astype(np.float64) @ Q.dequant_mxfp4(p, sc, K).T
+    assert G.rel_frobenius(bf16_to_np(c), ref) < 0.02
