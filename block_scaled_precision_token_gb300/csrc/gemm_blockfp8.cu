@@ -32,6 +32,7 @@ namespace fp8 {
 constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
 constexpr int kEpiThreads = 256;
 constexpr uint32_t kWSmem = 128 * 128;
+constexpr int kMaxStages = 16;
 
 struct Params {
   int M, KB;           // KB = K / 128 (blocks per row of As / Ws)
@@ -49,8 +50,8 @@ template <int BT>
 struct Cfg {
   static constexpr uint32_t kXSmem = BT * 128;
   static constexpr uint32_t kStageBytes = ((kWSmem + kXSmem + 1023) / 1024) * 1024;
-  static constexpr int kStagesRaw = static_cast<int>((192u * 1024u) / kStageBytes);
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kStagesRaw = static_cast<int>((220u * 1024u) / kStageBytes);
+  static constexpr int kStages = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
   static constexpr uint32_t kTxBytes = kWSmem + kXSmem;
   static constexpr uint32_t kTmemCols = (2 * BT) < 32 ? 32 : 2 * BT;
   static constexpr uint32_t kMiscBytes = 2048;  // barriers + 2 x BT scale products
@@ -76,8 +77,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *misc = smem + C::kStages * C::kStageBytes;
   float *sscale = reinterpret_cast<float *>(misc);                    // [2][BT]
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(misc + 1024);     // [8]
-  uint64_t *empty_bar = full_bar + 8;                                 // [8]
-  uint64_t *accf_bar = empty_bar + 8;                                 // [2]
+  uint64_t *empty_bar = full_bar + kMaxStages;                        // [16]
+  uint64_t *accf_bar = empty_bar + kMaxStages;                        // [2]
   uint64_t *acce_bar = accf_bar + 2;                                  // [2]
   uint64_t *drain_bar = acce_bar + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain_bar + 1);
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_x);
+    pdl_launch_dependents();
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -123,18 +125,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, issued_mask = 0, issued_phase = 0;
       bool ok = true;
+      // Weights first (independent of the preceding kernel), then wait for
+      // it before the first activation tile.
+      int pre = 0;
+      for (int u = blockIdx.x; u < p.units && pre < C::kStages; u += gridDim.x) {
+        int nt, tt, sp;
+        decode_unit(p, u, nt, tt, sp);
+        const int kb0 = sp * p.kb_per_split, kb1 = min(p.KB, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1 && pre < C::kStages; ++kb, ++pre) {
+          mbar_arrive_expect_tx(&full_bar[pre], C::kTxBytes);
+          tma_load_3d(smem + pre * C::kStageBytes, &tm_w, &full_bar[pre], 0, 0, nt * p.KB + kb, pol_w);
+        }
+      }
+      pdl_wait();
+      int it = 0;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         int nt, tt, sp;
         decode_unit(p, u, nt, tt, sp);
         const int kb0 = sp * p.kb_per_split, kb1 = min(p.KB, kb0 + p.kb_per_split);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) {
-            ok = false;
-            break;
-          }
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           uint8_t *st = smem + stage * C::kStageBytes;
-          mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
-          tma_load_3d(st, &tm_w, &full_bar[stage], 0, 0, nt * p.KB + kb, pol_w);
+          if (it >= pre) {
+            if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
+            tma_load_3d(st, &tm_w, &full_bar[stage], 0, 0, nt * p.KB + kb, pol_w);
+          }
           tma_load_2d(st + kWSmem, &tm_x, &full_bar[stage], kb * 128, tt * BT, pol_x);
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -196,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ promotion epilogue
+    pdl_wait();                        // As, C and the workspace follow the stream order
     const int e = threadIdx.x - 64;    // 0..255
     const int ew = warp - 2;           // 0..7
     const int q = warp & 3;            // lane quarter
@@ -278,14 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*is_last) {
           __threadfence();
           const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (128 * BT);
-          for (int j = 0; j < C::kHalf; ++j) {
-            const int t = tc0 + j;
-            if (t >= p.M) break;
-            float sum = 0.f;
-            for (int s2 = 0; s2 < p.splits; ++s2)
-              sum += ld_cg_f32(base + static_cast<size_t>(s2) * (128 * BT) + (h * C::kHalf + j) * 128 + q * 32 + lane);
-            p.c[static_cast<size_t>(t) * p.ldc + n] = f32_to_bf16_rn(sum);
-          }
+          reduce_partials_store<BT>(base, p.splits, min(BT, p.M - t0), nt * 128, nt * 128 + 128, nullptr, t0, p.c,
+                                    p.ldc, e, kEpiThreads);
           if (e == 0) p.counters[tile] = 0;
         }
         named_bar_sync(2, kEpiThreads);
@@ -338,7 +351,8 @@ int launch_bt(const uint8_t *q, const float *As, const uint8_t *packed, int64_t 
   p.err = device_error_word();
   auto kern = blockfp8_f8f6f4_kernel<BT>;
   if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::kSmemBytes) != cudaSuccess) return R4_ERR_CUDA;
-  kern<<<pl.grid, kThreads, C::kSmemBytes, st>>>(tm_w, tm_x, p);
+  if (launch_pdl(kern, dim3(pl.grid), dim3(kThreads), C::kSmemBytes, st, tm_w, tm_x, p) != cudaSuccess)
+    return R4_ERR_CUDA;
   set_last_kernel(BT == 32 ? "blockfp8_f8f6f4_kernel<32>"
                   : BT == 64 ? "blockfp8_f8f6f4_kernel<64>"
                              : "blockfp8_f8f6f4_kernel<128>");
@@ -355,7 +369,8 @@ GemmPlan plan_blockfp8(int64_t M, int64_t N, int64_t K, int sms) {
   pl.t_tiles = static_cast<int>(ceil_div(M, bt));
   pl.KB = static_cast<int>(K / 128);
   const int64_t tiles = static_cast<int64_t>(pl.n_tiles) * pl.t_tiles;
-  const double hbm = 6.5e12, sm_flops = 4.5e15 / 152.0, sm_l2 = 150e9;
+  // per-SM streaming rate is capped (bytes in flight / latency), not hbm/active
+  const double hbm = 6.5e12, sm_bw = 60e9, sm_flops = 4.5e15 / 152.0, sm_l2 = 150e9;
   const double kb_bytes = 128.0 * 128 + 128.0 * bt;
   const double kb_flops = 2.0 * 128 * bt * 128;
   int best_s = 1;
@@ -367,7 +382,7 @@ GemmPlan plan_blockfp8(int64_t M, int64_t N, int64_t K, int sms) {
     const int64_t units = tiles * s;
     const int64_t active = std::min<int64_t>(units, sms);
     const double waves = std::ceil(static_cast<double>(units) / sms);
-    const double t_unit = std::max(kbps * kb_bytes / (hbm / active), kbps * kb_flops / sm_flops);
+    const double t_unit = std::max(kbps * kb_bytes / std::min(hbm / active, sm_bw), kbps * kb_flops / sm_flops);
     double t = waves * t_unit;
     if (s > 1) {
       const double pbytes = static_cast<double>(units) * 128 * bt * 4;

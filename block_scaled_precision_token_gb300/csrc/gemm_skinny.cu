@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Let the cluster's CTAs start; the matching wait precedes the DSMEM writes.
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   float acc[2 * NG2][4];
 #pragma unroll
@@ -110,6 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
     }
+    // The weight is independent of the preceding kernel; x is not.
+    if (kk == kbeg) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int i = tid; i < kMpad * cpr; i += kThreads) {
       const int r = i / cpr, ch = i - r * cpr;
       uint16_t *dst = sX + r * kStride + ch * 8;
@@ -185,13 +188,15 @@ cudaError_t launch_ng(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(ks);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = options().pdl ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kern, x, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), cpc, c,
                          static_cast<int>(ldc));
   set_last_kernel(NG2 == 1 ? "skinny_bf16_kernel<1>" : NG2 == 2 ? "skinny_bf16_kernel<2>"

@@ -51,8 +51,9 @@ constexpr uint32_t kWSmem = 128 * 128;  // expanded e2m1 tile: 128 rows x 128 on
 constexpr uint32_t kWTxBytes = 8192;
 constexpr uint32_t kSfBytes = 512;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfaCol = 256;       // 4 columns per stage, up to 8 stages
-constexpr uint32_t kSfbCol = 288;       // 16 columns of constant 127
+constexpr uint32_t kSfaCol = 256;       // 4 columns per stage, up to 16 stages
+constexpr uint32_t kSfbCol = 320;       // 16 columns of constant 127
+constexpr int kMaxStages = 16;
 
 struct Params {
   int M, N, KB;
@@ -70,8 +71,8 @@ template <int BT>
 struct Cfg {
   static constexpr uint32_t kXSmem = BT * 128;
   static constexpr uint32_t kStageBytes = ((kWSmem + kXSmem + kSfBytes + 1023) / 1024) * 1024;
-  static constexpr int kStagesRaw = static_cast<int>((200u * 1024u) / kStageBytes);
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kStagesRaw = static_cast<int>((224u * 1024u) / kStageBytes);
+  static constexpr int kStages = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
   static constexpr int kNumAcc = BT <= 128 ? 2 : 1;
   static constexpr uint32_t kTxBytes = kWTxBytes + kXSmem + kSfBytes;
   static constexpr uint32_t kMiscBytes = 1024;
@@ -95,8 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *misc = smem + C::kStages * C::kStageBytes;
   uint8_t *sfb_const = misc;                                         // 512 B of 0x7F
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(misc + 512);     // [8]
-  uint64_t *empty_bar = full_bar + 8;                                // [8]
-  uint64_t *accf_bar = empty_bar + 8;                                // [2]
+  uint64_t *empty_bar = full_bar + kMaxStages;                       // [16]
+  uint64_t *accf_bar = empty_bar + kMaxStages;                       // [2]
   uint64_t *acce_bar = accf_bar + 2;                                 // [2]
   uint64_t *drain_bar = acce_bar + 2;                                // [1]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain_bar + 1);
@@ -126,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_x);
+    pdl_launch_dependents();   // let the next kernel in the stream start its own prologue
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -146,22 +148,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_phase = 0;
       bool ok = true;
+      // Weights do not depend on the preceding kernel: fill the ring with
+      // the first kStages weight tiles (+ scale atoms) before waiting for
+      // it, so under programmatic dependent launch the weight stream starts
+      // while the previous kernel is still running.
+      int pre = 0;
+      for (int u = blockIdx.x; u < p.units && pre < C::kStages; u += gridDim.x) {
+        int nt, tt, sp;
+        decode_unit(p, u, nt, tt, sp);
+        const int kb0 = sp * p.kb_per_split;
+        const int kb1 = min(p.KB, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1 && pre < C::kStages; ++kb, ++pre) {
+          uint8_t *st = smem + pre * C::kStageBytes;
+          mbar_arrive_expect_tx(&full_bar[pre], C::kTxBytes);
+          tma_load_3d(st, &tm_w, &full_bar[pre], 0, 0, nt * p.KB + kb, pol_w);
+          bulk_load(st + kWSmem + C::kXSmem, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
+                    &full_bar[pre], pol_w);
+        }
+      }
+      pdl_wait();   // activations come from the preceding kernel
+      int it = 0;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         int nt, tt, sp;
         decode_unit(p, u, nt, tt, sp);
         const int kb0 = sp * p.kb_per_split;
         const int kb1 = min(p.KB, kb0 + p.kb_per_split);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) {
-            ok = false;
-            break;
-          }
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           uint8_t *st = smem + stage * C::kStageBytes;
-          mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
-          tma_load_3d(st, &tm_w, &full_bar[stage], 0, 0, nt * p.KB + kb, pol_w);
+          if (it >= pre) {
+            if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
+            tma_load_3d(st, &tm_w, &full_bar[stage], 0, 0, nt * p.KB + kb, pol_w);
+            bulk_load(st + kWSmem + C::kXSmem, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
+                      &full_bar[stage], pol_w);
+          }
           tma_load_2d(st + kWSmem, &tm_x, &full_bar[stage], kb * kBK, tt * BT, pol_x);
-          bulk_load(st + kWSmem + C::kXSmem, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
-                    &full_bar[stage], pol_w);
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == C::kStages) {
@@ -238,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
+    pdl_wait();                     // s, C and the workspace belong to the kernel stream order
     const int q = warp & 3;         // tensor-memory lane quarter this warp may access
     const int ew = warp - 2;
     int acc = 0;
@@ -297,13 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*is_last) {
           __threadfence();
           const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (128 * BT);
-          const int tmax = min(BT, p.M - t0);
-          for (int tl = 0; tl < tmax; ++tl) {
-            float sum = 0.f;
-            for (int s2 = 0; s2 < p.splits; ++s2)
-              sum += ld_cg_f32(base + static_cast<size_t>(s2) * (128 * BT) + tl * 128 + q * 32 + lane);
-            if (n < p.N) p.c[static_cast<size_t>(t0 + tl) * p.ldc + n] = f32_to_bf16_rn(sum * __ldg(p.s + t0 + tl));
-          }
+          reduce_partials_store<BT>(base, p.splits, min(BT, p.M - t0), nt * 128, p.N, p.s, t0, p.c, p.ldc,
+                                    ew * 32 + lane, 128);
           if (ew == 0 && lane == 0) p.counters[tile] = 0;
         }
         named_bar_sync(1, 128);
@@ -362,7 +382,8 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
   p.err = device_error_word();
   auto kern = w4a8_mxf8f6f4_kernel<BT>;
   if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::kSmemBytes) != cudaSuccess) return R4_ERR_CUDA;
-  kern<<<pl.grid, kThreads, C::kSmemBytes, st>>>(tm_w, tm_x, p);
+  if (launch_pdl(kern, dim3(pl.grid), dim3(kThreads), C::kSmemBytes, st, tm_w, tm_x, p) != cudaSuccess)
+    return R4_ERR_CUDA;
   set_last_kernel(BT == 16    ? "w4a8_mxf8f6f4_kernel<16>"
                   : BT == 32  ? "w4a8_mxf8f6f4_kernel<32>"
                   : BT == 64  ? "w4a8_mxf8f6f4_kernel<64>"
@@ -386,7 +407,8 @@ GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
   pl.t_tiles = static_cast<int>(ceil_div(M, bt));
   pl.KB = static_cast<int>(ceil_div(K, 128));
   const int64_t tiles = static_cast<int64_t>(pl.n_tiles) * pl.t_tiles;
-  const double hbm = 6.5e12, sm_flops = 4.5e15 / 152.0, sm_l2 = 150e9;
+  // per-SM streaming rate is capped (bytes in flight / latency), not hbm/active
+  const double hbm = 6.5e12, sm_bw = 60e9, sm_flops = 4.5e15 / 152.0, sm_l2 = 150e9;
   const double kb_bytes = 128.0 * 128 * 0.5 + 512 + 128.0 * bt;      // weight + scales + activations
   const double kb_flops = 2.0 * 128 * bt * 128;
   int best_s = 1;
@@ -398,7 +420,7 @@ GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
     const int64_t units = tiles * s;
     const int64_t active = std::min<int64_t>(units, sms);
     const double waves = std::ceil(static_cast<double>(units) / sms);
-    const double t_unit = std::max(kbps * kb_bytes / (hbm / active), kbps * kb_flops / sm_flops);
+    const double t_unit = std::max(kbps * kb_bytes / std::min(hbm / active, sm_bw), kbps * kb_flops / sm_flops);
     double t = waves * t_unit;
     if (s > 1) {
       const double pbytes = static_cast<double>(units) * 128 * bt * 4;

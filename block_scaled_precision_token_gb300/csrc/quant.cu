@@ -64,6 +64,8 @@ template <int VPT>
 __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restrict__ x, int K, int64_t ldx,
                                                         int group, uint8_t *__restrict__ q,
                                                         float *__restrict__ s) {
+  if (threadIdx.x == 0) pdl_launch_dependents();   // the next kernel may start its weight stream
+  pdl_wait();                                       // x (and the q, s buffers) follow the stream order
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
   const int nt = blockDim.x;
@@ -114,6 +116,8 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
 __global__ void __launch_bounds__(256) quant_act_long_kernel(const uint16_t *__restrict__ x, int K, int64_t ldx,
                                                              int group, uint8_t *__restrict__ q,
                                                              float *__restrict__ s) {
+  if (threadIdx.x == 0) pdl_launch_dependents();   // the next kernel may start its weight stream
+  pdl_wait();                                       // x (and the q, s buffers) follow the stream order
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
   const int nt = blockDim.x;
@@ -227,19 +231,19 @@ cudaError_t launch_quant_act(const uint16_t *x, int64_t M, int64_t K, int64_t ld
   const dim3 grid(static_cast<unsigned>(M));
   const int g = static_cast<int>(group), k = static_cast<int>(K);
   if (per <= 1) {
-    quant_act_kernel<1><<<grid, threads, 0, st>>>(x, k, ldx, g, q, s);
+    { const cudaError_t e = launch_pdl(quant_act_kernel<1>, grid, dim3(threads), 0, st, x, k, ldx, g, q, s); if (e != cudaSuccess) return e; }
     set_last_kernel("quant_act_kernel<1>");
   } else if (per <= 2) {
-    quant_act_kernel<2><<<grid, threads, 0, st>>>(x, k, ldx, g, q, s);
+    { const cudaError_t e = launch_pdl(quant_act_kernel<2>, grid, dim3(threads), 0, st, x, k, ldx, g, q, s); if (e != cudaSuccess) return e; }
     set_last_kernel("quant_act_kernel<2>");
   } else if (per <= 4) {
-    quant_act_kernel<4><<<grid, threads, 0, st>>>(x, k, ldx, g, q, s);
+    { const cudaError_t e = launch_pdl(quant_act_kernel<4>, grid, dim3(threads), 0, st, x, k, ldx, g, q, s); if (e != cudaSuccess) return e; }
     set_last_kernel("quant_act_kernel<4>");
   } else if (per <= 9) {
-    quant_act_kernel<9><<<grid, threads, 0, st>>>(x, k, ldx, g, q, s);
+    { const cudaError_t e = launch_pdl(quant_act_kernel<9>, grid, dim3(threads), 0, st, x, k, ldx, g, q, s); if (e != cudaSuccess) return e; }
     set_last_kernel("quant_act_kernel<9>");
   } else {
-    quant_act_long_kernel<<<grid, threads, 0, st>>>(x, k, ldx, g, q, s);
+    { const cudaError_t e = launch_pdl(quant_act_long_kernel, grid, dim3(threads), 0, st, x, k, ldx, g, q, s); if (e != cudaSuccess) return e; }
     set_last_kernel("quant_act_long_kernel");
   }
   return cudaGetLastError();

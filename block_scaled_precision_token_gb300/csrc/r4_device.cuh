@@ -134,6 +134,12 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
       : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) from global memory into L2 (no smem).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -281,6 +287,18 @@ __host__ __device__ constexpr uint32_t idesc_f8f6f4_e4m3(int n) {
          (static_cast<uint32_t>(128 >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Kernels are launched with programmatic stream serialization: the next
+// kernel in the stream may start while this one runs. Each kernel reads
+// data that does not depend on earlier kernels (weights) before pdl_wait(),
+// and touches everything else (activations, scales, outputs, workspace) only
+// after it. pdl_wait() returns once the preceding grid has completed and its
+// memory is visible; without a programmatic predecessor it returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- misc
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -292,10 +310,36 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
   return *reinterpret_cast<uint16_t *>(&h);
 }
 
-__device__ __forceinline__ float ld_cg_f32(const float *p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
+// Split-K epilogue of the last-arriving CTA: sum `splits` fp32 partial tiles
+// (each [BT tokens][128 n], n contiguous) in split order -- deterministic --
+// and store bf16(scale[t] * sum) (scale == nullptr: 1) into C[t0 + t][n0 + n]
+// for t < tmax, n0 + n < N. The loads are independent L2 reads (.cg: the
+// partials were written by other SMs), four n per thread.
+template <int BT>
+__device__ __forceinline__ void reduce_partials_store(const float *base, int splits, int tmax, int n0, int N,
+                                                      const float *scale, int t0, uint16_t *c, int ldc, int tid,
+                                                      int nthreads) {
+  constexpr size_t kTile = 128 * BT;
+  for (int idx = tid; idx < tmax * 32; idx += nthreads) {
+    const int tl = idx >> 5, n4 = (idx & 31) * 4;
+    const float *src = base + tl * 128 + n4;
+    float4 acc = __ldcg(reinterpret_cast<const float4 *>(src));
+#pragma unroll 4
+    for (int s2 = 1; s2 < splits; ++s2) {
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + s2 * kTile));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const float sc = scale ? __ldg(scale + t0 + tl) : 1.f;
+    const int n = n0 + n4;
+    uint16_t *dst = c + static_cast<size_t>(t0 + tl) * ldc + n;
+    const float vals[4] = {acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (n + j < N) dst[j] = f32_to_bf16_rn(vals[j]);
+  }
 }
 
 }  // namespace r4

@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "../../include/r4q.h"
 
 namespace r4 {
@@ -28,8 +30,27 @@ struct Options {
   int w4a8_splits = 0;      // 0 = automatic
   int w4a8_token_tile = 0;  // 0 = automatic
   int fp8_splits = 0;       // 0 = automatic
+  int pdl = 1;              // launch with programmatic stream serialization
 };
 Options &options();
+
+// Launch `kernel` on `st`; with options().pdl the launch allows programmatic
+// dependent launch (the kernel may start before its predecessor in the
+// stream finishes; it orders its dependent accesses with griddepcontrol.wait).
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = options().pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ------------------------------------------------------------------ plans
 // One output tile = 128 weight rows (n) x BT tokens (t). A work unit is a

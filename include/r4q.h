@@ -23,6 +23,15 @@
  *  - A device-side wait that runs out (a TMA or tensor-core completion that
  *    never arrives) makes the kernel stop early and set a device error word;
  *    r4_device_error() reads and clears it.
+ *  - The per-token path (quantization and the three GEMMs) is launched with
+ *    programmatic dependent launch: a kernel may start while its predecessor
+ *    in the stream is still running, and reads its WEIGHT operand before
+ *    waiting for that predecessor (activations, scales, outputs and the
+ *    workspace are touched only after it completed). Weights must therefore
+ *    not be written by the immediately preceding kernel unless that kernel
+ *    completes normally (every kernel outside this library does; within it,
+ *    only the prepack and weight-quantizer calls write weights, and they are
+ *    launched without programmatic dependence). r4_set_option(4, 0) turns it off.
  */
 #ifndef R4Q_H
 #define R4Q_H
@@ -193,7 +202,8 @@ int r4_gemm_bf16_nt_skinny(const uint16_t *x, const uint16_t *w, int64_t M, int6
  * r4_set_option -- benchmarking overrides of the host-side schedule choice
  * (process-wide, not thread-safe). key 1: force the W4A8 split-K factor
  * (0 = automatic); key 2: force the W4A8 token tile (0 = automatic, else
- * 16/32/64/128/256); key 3: force the block-FP8 split-K factor.
+ * 16/32/64/128/256); key 3: force the block-FP8 split-K factor; key 4:
+ * programmatic dependent launch on (1, default) or off (0).
  */
 int r4_set_option(int key, int64_t value);
 

@@ -142,6 +142,8 @@ def test_end_to_end_with_gpu_quant(r4q):
     q, s = Q.quant_act(x.float().numpy())
     c64, _ = G.gemm_w4a8(q, s, p, sc)
     assert_gemm_matches(c, c64, "end-to-end")
-    # the pages' own accuracy measure against the unquantized product
+    # the pages' own accuracy measure against the product with unquantized
+    # activations: radiance_mxfp4.py reports 0.0265 for W4A8 (fp8 activation
+    # rounding included), against 0.1119 for the W4A4 path
     ref = x.float().numpy().astype(np.float64) @ Q.dequant_mxfp4(p, sc, K).T
-    assert G.rel_frobenius(bf16_to_np(c), ref) < 0.02
+    assert G.rel_frobenius(bf16_to_np(c), ref) < 0.05
