@@ -51,6 +51,7 @@ _SIGS = {
     "r4_gemm_w4a8_mxfp4": ([_P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
     "r4_gemm_blockfp8": ([_P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
     "r4_gemm_bf16_nt_skinny": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
+    "r4_gemm_w4a8_mxfp4_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P, _I64, _P], _I),
 }
 
 
@@ -186,6 +187,14 @@ def r4_gemm_w4a8_mxfp4(q, s, packed, M, N, K, c, ldc, workspace=None, stream=Non
     wp, wb = _ws(workspace)
     _check(lib().r4_gemm_w4a8_mxfp4(_ptr(q), _ptr(s), _ptr(packed), M, N, K, _ptr(c), ldc, wp, wb, _stream(stream)),
            "r4_gemm_w4a8_mxfp4")
+
+
+def r4_gemm_w4a8_mxfp4_noalloc(q, s, packed, M, N, K, c, ldc, stream=None):
+    """W4A8 GEMM without a caller workspace (split-K scratch is the library's
+    static device buffer); for callers that cannot allocate device memory."""
+    _need(q, torch.uint8, "q"); _need(s, torch.float32, "s"); _need(c, torch.bfloat16, "c")
+    _check(lib().r4_gemm_w4a8_mxfp4_noalloc(_ptr(q), _ptr(s), _ptr(packed), M, N, K, _ptr(c), ldc, _stream(stream)),
+           "r4_gemm_w4a8_mxfp4_noalloc")
 
 
 def r4_gemm_blockfp8(q, As, packed, M, N, K, c, ldc, workspace=None, stream=None):

@@ -199,6 +199,29 @@ int r4_gemm_bf16_nt_skinny(const uint16_t *x, const uint16_t *w, int64_t M, int6
                            size_t workspace_bytes, r4_stream_t stream);
 
 /*
+ * r4_gemm_w4a8_mxfp4_noalloc -- r4_gemm_w4a8_mxfp4 for callers that cannot
+ * allocate device memory. (No counterpart on the pages: it is a convenience of
+ * this library.) Code that runs during CUDA-graph capture may not call
+ * cudaMalloc, and inference-runtime plugin or custom-op interfaces often hand
+ * a kernel only its input/output pointers and a stream; neither can supply
+ * the split-K workspace. This variant takes the same arguments and returns
+ * the same result minus the workspace: its split-K counters and partials live
+ * in a library-owned static device buffer of 16 MiB, which every GPU that
+ * loads the library holds until the process exits. It allocates nothing.
+ *  - The first call on a device looks up that buffer's device address (with
+ *    the device current) and caches it: make that first call before any
+ *    stream capture.
+ *  - Each call clears the buffer's counters on `stream` before the GEMM.
+ *  - All calls share the buffer: calls whose kernels can overlap on the GPU
+ *    (other streams, other host threads) race on it and must be serialized by
+ *    the caller.
+ *  - A shape whose split-K schedule needs more than 16 MiB returns
+ *    R4_ERR_WORKSPACE without launching anything.
+ */
+int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *packed, int64_t M, int64_t N,
+                               int64_t K, uint16_t *c, int64_t ldc, r4_stream_t stream);
+
+/*
  * r4_set_option -- benchmarking overrides of the host-side schedule choice
  * (process-wide, not thread-safe). key 1: force the W4A8 split-K factor
  * (0 = automatic); key 2: force the W4A8 token tile (0 = automatic, else
