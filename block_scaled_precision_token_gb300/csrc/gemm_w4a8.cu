@@ -20,11 +20,15 @@
 //    activation tile is a 2-D e4m3 box; both in the 128-byte swizzle. The
 //    512-byte scale atom of the tile is a plain bulk copy, then tcgen05.cp
 //    places it in tensor memory (one 4-column slot per pipeline stage).
-//  * Roles: warp 0 issues TMA, warp 1 allocates tensor memory and issues MMAs
-//    (one thread), warps 2..5 drain the accumulator (tcgen05.ld), scale by
-//    s[m], round to bf16 and store. A multi-stage smem ring decouples TMA from
-//    MMA; double-buffered accumulators (BT <= 128) let the epilogue of one
-//    unit overlap the MMAs of the next.
+//  * Roles: TMA producer warps (1 for prefill tiles, 4 for decode tiles),
+//    MMA-issuing warps (as many; one thread each, each with its own
+//    tensor-memory accumulator -- see Cfg for why decode needs several), and
+//    4 epilogue warps that sum the accumulators (tcgen05.ld), scale by s[m],
+//    round to bf16 and stage [32 tokens x 128 n] chunks in smem that leave
+//    through TMA tensor stores (ragged edges clipped by the hardware; plain
+//    stores when C's row stride is not 16-byte aligned). A multi-stage smem
+//    ring decouples TMA from MMA; double-buffered accumulators let the
+//    epilogue of one unit overlap the MMAs of the next.
 //  * Split-K when the output has too few tiles to fill 152 SMs: fp32 partials
 //    go to the caller's workspace and the last CTA to arrive at a tile (one
 //    atomic counter per tile) sums them in split order -- deterministic -- and
@@ -42,7 +46,16 @@
 namespace r4 {
 namespace w4a8 {
 
-constexpr int kThreads = 192;
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 constexpr int kBK = 128;
 constexpr uint32_t kWSmem = 128 * 128;  // expanded e2m1 tile: 128 rows x 128 one-byte slots
 // The 16U4_ALIGN16B tile load completes the mbarrier transaction with the
@@ -52,13 +65,14 @@ constexpr uint32_t kWTxBytes = 8192;
 constexpr uint32_t kSfBytes = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfaCol = 256;       // 4 columns per stage, up to 16 stages
-constexpr uint32_t kSfbCol = 320;       // 16 columns of constant 127
+constexpr uint32_t kSfbCol = 320;       // 16 columns of constant 127 per MMA warp (up to 4)
 constexpr int kMaxStages = 16;
 
 struct Params {
   int M, N, KB;
   int t_tiles, splits, kb_per_split, units;
   int ldc;
+  int tma_store;         // 1: bf16 output tiles leave through smem + TMA tensor stores
   const float *s;
   const uint8_t *sf;     // scale atoms of the prepacked weight
   uint16_t *c;
@@ -67,58 +81,79 @@ struct Params {
   int *err;
 };
 
+// Decode tiles (BT <= 64) are bound by instruction issue, not by HBM or the
+// tensor core (measured on GB300): issuing one TMA operation occupies the
+// issuing thread for a few hundred cycles, and an M=128, N<=64, K=32 MMA
+// occupies its issuing thread for ~53 cycles whatever N is, plus the per-stage
+// scale copy, commit and barrier handshake. So decode tiles run kIss TMA
+// producer warps and kIss MMA-issuing warps: slot g (one 128-K block) belongs
+// to producer g % kIss and MMA warp g % kIss, lives in ring stage g % kStages,
+// and is accumulated into MMA warp (g % kIss)'s own tensor-memory accumulator;
+// the epilogue sums the kIss partial accumulators.
 template <int BT>
 struct Cfg {
+  static constexpr int kIss = BT <= 64 ? 4 : 1;
+  static constexpr int kNumAcc = (kIss * 2 * BT <= 256) ? 2 : 1;
+  static constexpr int kThreads = 32 * (2 * kIss + 4);   // kIss producers, kIss MMA issuers, 4 epilogue
+  static constexpr int kEpiWarp0 = 2 * kIss;
   static constexpr uint32_t kXSmem = BT * 128;
   static constexpr uint32_t kStageBytes = ((kWSmem + kXSmem + kSfBytes + 1023) / 1024) * 1024;
-  static constexpr int kStagesRaw = static_cast<int>((224u * 1024u) / kStageBytes);
-  static constexpr int kStages = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
-  static constexpr int kNumAcc = BT <= 128 ? 2 : 1;
+  static constexpr int kOutChunk = BT < 32 ? BT : 32;                // tokens per output chunk
+  static constexpr uint32_t kOutBytes = 2u * kOutChunk * 128u * 2u;  // two bf16 [chunk][128] buffers
+  static constexpr int kStagesRaw = static_cast<int>((208u * 1024u) / kStageBytes);
+  static constexpr int kStagesCap = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
+  static constexpr int kStages = (kStagesCap / kIss) * kIss;        // every issuer owns fixed stages
   static constexpr uint32_t kTxBytes = kWTxBytes + kXSmem + kSfBytes;
   static constexpr uint32_t kMiscBytes = 1024;
-  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kMiscBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kMiscBytes + kOutBytes + 1024;  // + align slack
+  static_assert(kIss * kNumAcc * BT <= 256, "accumulators overlap the scale columns");
+  static_assert(kStages >= kIss && kStages % kIss == 0, "stage count");
 };
 
-__device__ __forceinline__ void decode_unit(const Params &p, int u, int &nt, int &tt, int &sp) {
+__device__ __forceinline__ void decode_unit(const Params &p, int u, int &nt, int &tt, int &sp, int &kb0, int &kb1) {
   const int tile = u / p.splits;
   sp = u - tile * p.splits;
   nt = tile / p.t_tiles;
   tt = tile - nt * p.t_tiles;
+  kb0 = sp * p.kb_per_split;
+  kb1 = min(p.KB, kb0 + p.kb_per_split);
 }
 
 template <int BT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
     w4a8_mxf8f6f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                         const Params p) {
+                         const __grid_constant__ CUtensorMap tm_c, const Params p) {
   using C = Cfg<BT>;
+  constexpr int ISS = C::kIss;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *misc = smem + C::kStages * C::kStageBytes;
   uint8_t *sfb_const = misc;                                         // 512 B of 0x7F
-  uint64_t *full_bar = reinterpret_cast<uint64_t *>(misc + 512);     // [8]
+  uint64_t *full_bar = reinterpret_cast<uint64_t *>(misc + 512);     // [16]
   uint64_t *empty_bar = full_bar + kMaxStages;                       // [16]
   uint64_t *accf_bar = empty_bar + kMaxStages;                       // [2]
   uint64_t *acce_bar = accf_bar + 2;                                 // [2]
-  uint64_t *drain_bar = acce_bar + 2;                                // [1]
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain_bar + 1);
+  uint64_t *drain_bar = acce_bar + 2;                                // [4], one per MMA warp
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain_bar + 4);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *is_last = abort_flag + 1;
   volatile int *epi_abort = abort_flag + 2;   // set and read by epilogue threads only
+  uint16_t *staging = reinterpret_cast<uint16_t *>(misc + C::kMiscBytes);   // [2][kOutChunk][128] bf16
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  for (int i = threadIdx.x; i < 128; i += kThreads) reinterpret_cast<uint32_t *>(sfb_const)[i] = 0x7F7F7F7Fu;
+  for (int i = threadIdx.x; i < 128; i += C::kThreads) reinterpret_cast<uint32_t *>(sfb_const)[i] = 0x7F7F7F7Fu;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&accf_bar[a], 1);
-      mbar_init(&acce_bar[a], 4);
+      mbar_init(&accf_bar[a], ISS);   // one arrival per MMA warp per unit
+      mbar_init(&acce_bar[a], 4);     // one per epilogue warp
     }
-    mbar_init(drain_bar, 1);
+    for (int w = 0; w < 4; ++w) mbar_init(&drain_bar[w], 1);
     *abort_flag = 0;
     *is_last = 0;
     *epi_abort = 0;
@@ -129,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_x);
     pdl_launch_dependents();   // let the next kernel in the stream start its own prologue
   }
-  if (warp == 1) {
+  if (warp == ISS) {           // first MMA warp owns the tensor-memory allocation
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -139,138 +174,175 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp < ISS) {
+    // ------------------------------------------------------------ TMA producers (warps 0..ISS-1)
+    // Slot sequence: every unit's k-blocks, padded to a multiple of ISS. A
+    // padding slot carries no data: its full barrier gets a plain arrival.
+    const int pw = warp;
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_phase = 0;
       bool ok = true;
-      // Weights do not depend on the preceding kernel: fill the ring with
-      // the first kStages weight tiles (+ scale atoms) before waiting for
-      // it, so under programmatic dependent launch the weight stream starts
-      // while the previous kernel is still running.
-      int pre = 0;
-      for (int u = blockIdx.x; u < p.units && pre < C::kStages; u += gridDim.x) {
-        int nt, tt, sp;
-        decode_unit(p, u, nt, tt, sp);
-        const int kb0 = sp * p.kb_per_split;
-        const int kb1 = min(p.KB, kb0 + p.kb_per_split);
-        for (int kb = kb0; kb < kb1 && pre < C::kStages; ++kb, ++pre) {
-          uint8_t *st = smem + pre * C::kStageBytes;
-          mbar_arrive_expect_tx(&full_bar[pre], C::kTxBytes);
-          tma_load_3d(st, &tm_w, &full_bar[pre], 0, 0, nt * p.KB + kb, pol_w);
-          bulk_load(st + kWSmem + C::kXSmem, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
-                    &full_bar[pre], pol_w);
+      // Weights do not depend on the preceding kernel: fill this producer's
+      // stages with weight tiles (+ scale atoms) before waiting for it, so
+      // under programmatic dependent launch the weight stream starts while
+      // the previous kernel is still running.
+      {
+        int g = 0;
+        for (int u = blockIdx.x; u < p.units && g < C::kStages; u += gridDim.x) {
+          int nt, tt, sp, kb0, kb1;
+          decode_unit(p, u, nt, tt, sp, kb0, kb1);
+          const int nkb = kb1 - kb0;
+          const int nslots = (nkb + ISS - 1) / ISS * ISS;
+          for (int i = pw; i < nslots && g + i < C::kStages; i += ISS) {
+            const int s_ = g + i;
+            if (i < nkb) {
+              uint8_t *st = smem + s_ * C::kStageBytes;
+              const int kb = kb0 + i;
+              mbar_arrive_expect_tx(&full_bar[s_], C::kTxBytes);
+              tma_load_3d(st, &tm_w, &full_bar[s_], 0, 0, nt * p.KB + kb, pol_w);
+              bulk_load(st + kWSmem + C::kXSmem, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
+                        &full_bar[s_], pol_w);
+            } else {
+              mbar_arrive(&full_bar[s_]);
+            }
+          }
+          g += nslots;
         }
       }
       pdl_wait();   // activations come from the preceding kernel
-      int it = 0;
+      int stage = pw;
+      uint32_t phase = 0;
+      int gbase = 0;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        int nt, tt, sp;
-        decode_unit(p, u, nt, tt, sp);
-        const int kb0 = sp * p.kb_per_split;
-        const int kb1 = min(p.KB, kb0 + p.kb_per_split);
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        int nt, tt, sp, kb0, kb1;
+        decode_unit(p, u, nt, tt, sp, kb0, kb1);
+        const int nkb = kb1 - kb0;
+        const int nslots = (nkb + ISS - 1) / ISS * ISS;
+        for (int i = pw; i < nslots; i += ISS) {
           uint8_t *st = smem + stage * C::kStageBytes;
-          if (it >= pre) {
+          const int kb = kb0 + i;
+          if (gbase + i >= C::kStages) {   // not pre-issued
             if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
-            tma_load_3d(st, &tm_w, &full_bar[stage], 0, 0, nt * p.KB + kb, pol_w);
-            bulk_load(st + kWSmem + C::kXSmem, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
-                      &full_bar[stage], pol_w);
+            if (i < nkb) {
+              mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
+              tma_load_3d(st, &tm_w, &full_bar[stage], 0, 0, nt * p.KB + kb, pol_w);
+              bulk_load(st + kWSmem + C::kXSmem, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
+                        &full_bar[stage], pol_w);
+            } else {
+              mbar_arrive(&full_bar[stage]);
+            }
           }
-          tma_load_2d(st + kWSmem, &tm_x, &full_bar[stage], kb * kBK, tt * BT, pol_x);
+          if (i < nkb) tma_load_2d(st + kWSmem, &tm_x, &full_bar[stage], kb * kBK, tt * BT, pol_x);
+          // Record the newest phase of every stage, padding slots included: a
+          // parity wait cannot tell phase k from k + 2, and a stage only
+          // advances after its earlier phases completed.
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == C::kStages) {
-            stage = 0;
+          stage += ISS;
+          if (stage >= C::kStages) {
+            stage -= C::kStages;
             phase ^= 1u;
           }
         }
+        gbase += nslots;
       }
       // Never leave a copy in flight: wait (bounded, even after an abort) for
-      // the last load issued into every stage.
-      for (int s = 0; s < C::kStages; ++s)
-        if (issued_mask & (1u << s)) {
+      // the last load issued into each of this producer's stages.
+      for (int s_ = 0; s_ < C::kStages; ++s_)
+        if (issued_mask & (1u << s_)) {
           volatile int dummy = 0;
-          mbar_wait(&full_bar[s], (issued_phase >> s) & 1u, &dummy, p.err, DEV_ERR_WAIT_DRAIN);
+          mbar_wait(&full_bar[s_], (issued_phase >> s_) & 1u, &dummy, p.err, DEV_ERR_WAIT_DRAIN);
         }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp < 2 * ISS) {
+    // ------------------------------------------------------------ MMA issuers (warps ISS..2*ISS-1)
+    const int mw = warp - ISS;
     if (lane == 0) {
+      const uint32_t sfb = tmem + kSfbCol + 16u * static_cast<uint32_t>(mw);
       const uint64_t sfb_desc = sdesc_sf_32x16(smem_u32(sfb_const));
 #pragma unroll
-      for (int j = 0; j < 4; ++j) tc_cp_32x128b_warpx4(tmem + kSfbCol + 4 * j, sfb_desc);
-      int stage = 0;
+      for (int j = 0; j < 4; ++j) tc_cp_32x128b_warpx4(sfb + 4 * j, sfb_desc);
+      int stage = mw;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        int nt, tt, sp;
-        decode_unit(p, u, nt, tt, sp);
-        const int kb0 = sp * p.kb_per_split;
-        const int kb1 = min(p.KB, kb0 + p.kb_per_split);
+        int nt, tt, sp, kb0, kb1;
+        decode_unit(p, u, nt, tt, sp, kb0, kb1);
+        const int nkb = kb1 - kb0;
+        const int nslots = (nkb + ISS - 1) / ISS * ISS;
         if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_ACC_EMPTY)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BT);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>((mw * C::kNumAcc + acc) * BT);
+        bool first = true;
+        for (int i = mw; i < nslots; i += ISS) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.err, DEV_ERR_WAIT_FULL)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          uint8_t *st = smem + stage * C::kStageBytes;
-          const uint32_t sfa = tmem + kSfaCol + 4u * static_cast<uint32_t>(stage);
-          tc_cp_32x128b_warpx4(sfa, sdesc_sf_32x16(smem_u32(st + kWSmem + C::kXSmem)));
-          const uint32_t a_base = smem_u32(st);
-          const uint32_t b_base = smem_u32(st + kWSmem);
+          if (i < nkb) {
+            tc_fence_after();
+            uint8_t *st = smem + stage * C::kStageBytes;
+            const uint32_t sfa = tmem + kSfaCol + 4u * static_cast<uint32_t>(stage);
+            tc_cp_32x128b_warpx4(sfa, sdesc_sf_32x16(smem_u32(st + kWSmem + C::kXSmem)));
+            const uint32_t a_base = smem_u32(st);
+            const uint32_t b_base = smem_u32(st + kWSmem);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128_kmajor(a_base + 32u * kk);
-            const uint64_t bd = sdesc_sw128_kmajor(b_base + 32u * kk);
-            const uint32_t idesc = idesc_mxf8f6f4_e2m1_e4m3(BT, kk, 0);
-            tc_mma_mxf8f6f4(d_tmem, ad, bd, idesc, sfa | (static_cast<uint32_t>(kk) << 30), tmem + kSfbCol,
-                            (kb > kb0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc_sw128_kmajor(a_base + 32u * kk);
+              const uint64_t bd = sdesc_sw128_kmajor(b_base + 32u * kk);
+              const uint32_t idesc = idesc_mxf8f6f4_e2m1_e4m3(BT, kk, 0);
+              tc_mma_mxf8f6f4(d_tmem, ad, bd, idesc, sfa | (static_cast<uint32_t>(kk) << 30), sfb,
+                              (!first || kk > 0) ? 1u : 0u);
+            }
+            first = false;
+            tc_commit(&empty_bar[stage]);
+          } else {
+            mbar_arrive(&empty_bar[stage]);   // padding slot: nothing read it
           }
-          tc_commit(&empty_bar[stage]);
-          if (++stage == C::kStages) {
-            stage = 0;
+          stage += ISS;
+          if (stage >= C::kStages) {
+            stage -= C::kStages;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(&accf_bar[acc]);
+        if (first)
+          mbar_arrive(&accf_bar[acc]);   // this warp owned no k-block of the unit
+        else
+          tc_commit(&accf_bar[acc]);
         if (++acc == C::kNumAcc) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // All MMAs this thread issued must be complete before tensor memory is freed.
-      tc_commit(drain_bar);
+      tc_commit(&drain_bar[mw]);
       volatile int dummy = 0;
-      mbar_wait(drain_bar, 0, &dummy, p.err, DEV_ERR_WAIT_DRAIN);
+      mbar_wait(&drain_bar[mw], 0, &dummy, p.err, DEV_ERR_WAIT_DRAIN);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------------ epilogue (4 warps)
     pdl_wait();                     // s, C and the workspace belong to the kernel stream order
     const int q = warp & 3;         // tensor-memory lane quarter this warp may access
-    const int ew = warp - 2;
+    const int ew = warp - C::kEpiWarp0;
     int acc = 0;
     uint32_t acc_phase = 0;
     constexpr int CH = BT < 32 ? BT : 32;
+    const bool leader = (ew == 0 && lane == 0);
+    uint32_t out_chunk = 0;   // running count of staged output chunks (selects the buffer)
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-      int nt, tt, sp;
-      decode_unit(p, u, nt, tt, sp);
+      int nt, tt, sp, kb0, kb1;
+      decode_unit(p, u, nt, tt, sp, kb0, kb1);
+      const int ncontrib = min(ISS, kb1 - kb0);   // MMA warps that accumulated something
       // The decision to stop must be the same in all 128 epilogue threads
       // (they meet at named barriers below): a failed wait is published
       // before the barrier and read after it.
@@ -281,34 +353,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = nt * 128 + q * 32 + lane;
       const int t0 = tt * BT;
       const int tile = nt * p.t_tiles + tt;
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BT);
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
       float *part = (p.splits > 1) ? p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (128 * BT) : nullptr;
 #pragma unroll 1
       for (int c0 = 0; c0 < BT; c0 += CH) {
         uint32_t r[32];
-        if constexpr (CH == 32) {
-          tc_ld_32x32b_x32(taddr + c0, r);
-        } else {
-          tc_ld_32x32b_x16(taddr + c0, r);
+        float v[32];
+#pragma unroll 1
+        for (int w = 0; w < ncontrib; ++w) {
+          const uint32_t taddr = lane_base + static_cast<uint32_t>((w * C::kNumAcc + acc) * BT + c0);
+          if constexpr (CH == 32) {
+            tc_ld_32x32b_x32(taddr, r);
+          } else {
+            tc_ld_32x32b_x16(taddr, r);
+          }
+          tc_wait_ld();
+#pragma unroll
+          for (int j = 0; j < CH; ++j) v[j] = (w == 0) ? __uint_as_float(r[j]) : v[j] + __uint_as_float(r[j]);
         }
-        tc_wait_ld();
         if (c0 + CH >= BT) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce_bar[acc]);
         }
-        if (p.splits == 1) {
+        if (p.splits == 1 && p.tma_store) {
+          // Stage [CH tokens][128 n] bf16 in smem, then one TMA tensor store;
+          // the store clips rows >= M and columns >= N.
+          uint16_t *stg = staging + (out_chunk & 1u) * (CH * 128);
+          if (leader) bulk_wait_read1();   // the store issued two chunks ago has read this buffer
+          named_bar_sync(1, 128);
+#pragma unroll
+          for (int j = 0; j < CH; ++j) {
+            const int t = t0 + c0 + j;
+            const float sc = (t < p.M) ? __ldg(p.s + t) : 0.f;
+            stg[j * 128 + q * 32 + lane] = f32_to_bf16_rn(v[j] * sc);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (leader) {
+            tma_store_2d(&tm_c, stg, nt * 128, t0 + c0);
+            bulk_commit();
+          }
+          ++out_chunk;
+        } else if (p.splits == 1) {
           if (n < p.N) {
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
               const int t = t0 + c0 + j;
-              if (t < p.M)
-                p.c[static_cast<size_t>(t) * p.ldc + n] = f32_to_bf16_rn(__uint_as_float(r[j]) * __ldg(p.s + t));
+              if (t < p.M) p.c[static_cast<size_t>(t) * p.ldc + n] = f32_to_bf16_rn(v[j] * __ldg(p.s + t));
             }
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < CH; ++j) part[(c0 + j) * 128 + q * 32 + lane] = __uint_as_float(r[j]);
+          for (int j = 0; j < CH; ++j) part[(c0 + j) * 128 + q * 32 + lane] = v[j];
         }
       }
       if (p.splits > 1) {
@@ -333,11 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    if (leader) bulk_wait_all();   // output stores complete before the CTA's smem goes away
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == ISS) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -348,7 +446,7 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
               int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st) {
   using C = Cfg<BT>;
   const int64_t NT = ceil_div(N, 128);
-  CUtensorMap tm_w, tm_x;
+  CUtensorMap tm_w, tm_x, tm_c;
   {
     const uint64_t dims[3] = {128, 128, static_cast<uint64_t>(NT * pl.KB)};
     const uint64_t strides[2] = {64, 8192};
@@ -365,6 +463,16 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return R4_ERR_CUDA;
   }
+  // Output through TMA tensor stores when C's base and row stride are 16-byte aligned.
+  int use_tma_store = 0;
+  if ((reinterpret_cast<uintptr_t>(c) % 16) == 0 && (ldc * 2) % 16 == 0) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(ldc) * 2};
+    const uint32_t box[2] = {128, static_cast<uint32_t>(C::kOutChunk)};
+    use_tma_store = encode_tiled(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims, strides, box,
+                                 CU_TENSOR_MAP_SWIZZLE_NONE) == CUDA_SUCCESS;
+  }
+  if (!use_tma_store) tm_c = tm_x;   // not read by the kernel in that case
   Params p;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
@@ -374,6 +482,7 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
   p.kb_per_split = pl.kb_per_split;
   p.units = pl.units;
   p.ldc = static_cast<int>(ldc);
+  p.tma_store = use_tma_store;
   p.s = s;
   p.sf = packed + mx_packed_codes_bytes(N, K);
   p.c = c;
@@ -382,7 +491,7 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
   p.err = device_error_word();
   auto kern = w4a8_mxf8f6f4_kernel<BT>;
   if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::kSmemBytes) != cudaSuccess) return R4_ERR_CUDA;
-  if (launch_pdl(kern, dim3(pl.grid), dim3(kThreads), C::kSmemBytes, st, tm_w, tm_x, p) != cudaSuccess)
+  if (launch_pdl(kern, dim3(pl.grid), dim3(C::kThreads), C::kSmemBytes, st, tm_w, tm_x, tm_c, p) != cudaSuccess)
     return R4_ERR_CUDA;
   set_last_kernel(BT == 16    ? "w4a8_mxf8f6f4_kernel<16>"
                   : BT == 32  ? "w4a8_mxf8f6f4_kernel<32>"

@@ -9,6 +9,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #ifndef R4_WAIT_TIMEOUT_NS
