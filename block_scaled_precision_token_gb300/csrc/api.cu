@@ -142,6 +142,8 @@ int r4_set_option(int key, int64_t value) {
       return R4_OK;
     case 3: options().fp8_splits = static_cast<int>(value); return R4_OK;
     case 4: options().pdl = value ? 1 : 0; return R4_OK;
+    case 5: options().l2_prefetch = value ? 1 : 0; return R4_OK;
+    case 6: options().cluster_split = value ? 1 : 0; return R4_OK;
     default: return R4_ERR_INVALID_ARG;
   }
 }

@@ -25,14 +25,21 @@
 //    tensor-memory accumulator -- see Cfg for why decode needs several), and
 //    4 epilogue warps that sum the accumulators (tcgen05.ld), scale by s[m],
 //    round to bf16 and stage [32 tokens x 128 n] chunks in smem that leave
-//    through TMA tensor stores (ragged edges clipped by the hardware; plain
-//    stores when C's row stride is not 16-byte aligned). A multi-stage smem
+//    through TMA tensor stores (ragged token edges clipped by the hardware;
+//    plain stores when C's base, row stride or row length is not a 16-byte
+//    multiple). A multi-stage smem
 //    ring decouples TMA from MMA; double-buffered accumulators let the
 //    epilogue of one unit overlap the MMAs of the next.
-//  * Split-K when the output has too few tiles to fill 152 SMs: fp32 partials
-//    go to the caller's workspace and the last CTA to arrive at a tile (one
-//    atomic counter per tile) sums them in split order -- deterministic -- and
-//    resets the counter. No CTA ever waits for another.
+//  * Split-K when the output has too few tiles to fill 152 SMs, two ways:
+//    - decode tiles of 32/64 tokens: the splits of a tile are the CTAs of one
+//      thread-block cluster; each writes its fp32 partial [32 tokens][128 n]
+//      into its own shared memory, and every CTA then sums its 1/splits share
+//      of the n range over all the cluster's partials (distributed shared
+//      memory, rank order: deterministic) and stores it. mbarrier arrivals
+//      across the cluster sequence the exchange, with bounded waits;
+//    - otherwise fp32 partials go to the caller's workspace and the last CTA
+//      to arrive at a tile (one atomic counter per tile) sums them in split
+//      order -- deterministic -- and resets the counter.
 //  * Every mbarrier wait is bounded (see r4_device.cuh).
 
 #include <cuda_bf16.h>
@@ -73,6 +80,9 @@ struct Params {
   int t_tiles, splits, kb_per_split, units;
   int ldc;
   int tma_store;         // 1: bf16 output tiles leave through smem + TMA tensor stores
+  int l2_prefetch;       // 1: producer 0 prefetches each unit's weight range into L2, one unit ahead
+  int cluster;           // 1: the `splits` CTAs of a cluster split K and exchange partials in DSMEM
+  const uint8_t *w;      // packed weight codes [NT][KB][128][64]
   const float *s;
   const uint8_t *sf;     // scale atoms of the prepacked weight
   uint16_t *c;
@@ -119,6 +129,17 @@ __device__ __forceinline__ void decode_unit(const Params &p, int u, int &nt, int
   kb1 = min(p.KB, kb0 + p.kb_per_split);
 }
 
+// Bulk L2 prefetch of unit u's weight codes and scale atoms (both contiguous).
+__device__ __forceinline__ void prefetch_unit_l2(const Params &p, int u) {
+  if (u >= p.units) return;
+  int nt, tt, sp, kb0, kb1;
+  decode_unit(p, u, nt, tt, sp, kb0, kb1);
+  const size_t blk = static_cast<size_t>(nt) * p.KB + kb0;
+  const uint32_t nkb = static_cast<uint32_t>(kb1 - kb0);
+  bulk_prefetch_l2(p.w + blk * 8192, nkb * 8192u);
+  bulk_prefetch_l2(p.sf + blk * kSfBytes, nkb * kSfBytes);
+}
+
 template <int BT>
 __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
     w4a8_mxf8f6f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
@@ -134,7 +155,9 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
   uint64_t *accf_bar = empty_bar + kMaxStages;                       // [2]
   uint64_t *acce_bar = accf_bar + 2;                                 // [2]
   uint64_t *drain_bar = acce_bar + 2;                                // [4], one per MMA warp
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain_bar + 4);
+  uint64_t *red_full = drain_bar + 4;    // cluster split-K: all partials of a chunk written
+  uint64_t *red_empty = red_full + 1;    // cluster split-K: all CTAs have read this CTA's partial
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(red_empty + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *is_last = abort_flag + 1;
   volatile int *epi_abort = abort_flag + 2;   // set and read by epilogue threads only
@@ -154,6 +177,8 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       mbar_init(&acce_bar[a], 4);     // one per epilogue warp
     }
     for (int w = 0; w < 4; ++w) mbar_init(&drain_bar[w], 1);
+    mbar_init(red_full, p.splits);    // one arrival per CTA of the cluster
+    mbar_init(red_empty, p.splits);
     *abort_flag = 0;
     *is_last = 0;
     *epi_abort = 0;
@@ -173,6 +198,8 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Every CTA of the cluster has initialised its barriers before any remote arrival.
+  if (p.cluster) cluster_sync_all();
 
   if (warp < ISS) {
     // ------------------------------------------------------------ TMA producers (warps 0..ISS-1)
@@ -188,6 +215,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       // stages with weight tiles (+ scale atoms) before waiting for it, so
       // under programmatic dependent launch the weight stream starts while
       // the previous kernel is still running.
+      if (p.l2_prefetch && pw == 0) prefetch_unit_l2(p, blockIdx.x);
       {
         int g = 0;
         for (int u = blockIdx.x; u < p.units && g < C::kStages; u += gridDim.x) {
@@ -220,6 +248,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
         decode_unit(p, u, nt, tt, sp, kb0, kb1);
         const int nkb = kb1 - kb0;
         const int nslots = (nkb + ISS - 1) / ISS * ISS;
+        if (p.l2_prefetch && pw == 0) prefetch_unit_l2(p, u + gridDim.x);
         for (int i = pw; i < nslots; i += ISS) {
           uint8_t *st = smem + stage * C::kStageBytes;
           const int kb = kb0 + i;
@@ -339,6 +368,8 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
     constexpr int CH = BT < 32 ? BT : 32;
     const bool leader = (ew == 0 && lane == 0);
     uint32_t out_chunk = 0;   // running count of staged output chunks (selects the buffer)
+    uint32_t xchg = 0;        // running count of cluster split-K exchanges
+    bool stop = false;
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
       int nt, tt, sp, kb0, kb1;
       decode_unit(p, u, nt, tt, sp, kb0, kb1);
@@ -354,7 +385,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       const int t0 = tt * BT;
       const int tile = nt * p.t_tiles + tt;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      float *part = (p.splits > 1) ? p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (128 * BT) : nullptr;
+      float *part = (p.splits > 1 && !p.cluster) ? p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (128 * BT) : nullptr;
 #pragma unroll 1
       for (int c0 = 0; c0 < BT; c0 += CH) {
         uint32_t r[32];
@@ -403,12 +434,69 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
               if (t < p.M) p.c[static_cast<size_t>(t) * p.ldc + n] = f32_to_bf16_rn(v[j] * __ldg(p.s + t));
             }
           }
+        } else if (p.cluster) {
+          // Split-K inside the cluster: this CTA's partial chunk goes to its
+          // staging buffer as fp32 [CH][128]; then every CTA sums its 1/splits
+          // share of the 128 n (in groups of 4) over all CTAs' partials, in
+          // rank order (deterministic), and stores bf16(s[t] * sum).
+          float *red = reinterpret_cast<float *>(staging);
+          if (xchg > 0 && leader &&
+              !mbar_wait_cluster(red_empty, (xchg - 1u) & 1u, abort_flag, p.err, DEV_ERR_WAIT_PEER))
+            *epi_abort = 1;
+          named_bar_sync(1, 128);
+          if (*epi_abort) {
+            stop = true;
+            break;
+          }
+#pragma unroll
+          for (int j = 0; j < CH; ++j) red[j * 128 + q * 32 + lane] = v[j];
+          named_bar_sync(1, 128);
+          if (leader) {
+            fence_acq_rel_cluster();
+            for (int pr = 0; pr < p.splits; ++pr) mbar_arrive_remote(mapa_shared(smem_u32(red_full), pr));
+            if (!mbar_wait_cluster(red_full, xchg & 1u, abort_flag, p.err, DEV_ERR_WAIT_PEER)) *epi_abort = 1;
+          }
+          named_bar_sync(1, 128);
+          if (*epi_abort) {
+            stop = true;
+            break;
+          }
+          const int rank = static_cast<int>(cluster_ctarank());
+          const int qlo = rank * 32 / p.splits, nq = (rank + 1) * 32 / p.splits - qlo;
+          const uint32_t red_base = smem_u32(red);
+          for (int idx = ew * 32 + lane; idx < CH * nq; idx += 128) {
+            const int j = idx / nq, qd = qlo + (idx - j * nq);
+            const uint32_t off = red_base + static_cast<uint32_t>((j * 128 + qd * 4) * 4);
+            float4 a4 = ld_dsmem_f32x4(mapa_shared(off, 0));
+            for (int pr = 1; pr < p.splits; ++pr) {
+              const float4 b4 = ld_dsmem_f32x4(mapa_shared(off, static_cast<uint32_t>(pr)));
+              a4.x += b4.x;
+              a4.y += b4.y;
+              a4.z += b4.z;
+              a4.w += b4.w;
+            }
+            const int t = t0 + c0 + j;
+            if (t < p.M) {
+              const float sc = __ldg(p.s + t);
+              const int n0 = nt * 128 + qd * 4;
+              uint16_t *dst = p.c + static_cast<size_t>(t) * p.ldc + n0;
+              const float o[4] = {a4.x * sc, a4.y * sc, a4.z * sc, a4.w * sc};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (n0 + e < p.N) dst[e] = f32_to_bf16_rn(o[e]);
+            }
+          }
+          named_bar_sync(1, 128);
+          if (leader)
+            for (int pr = 0; pr < p.splits; ++pr) mbar_arrive_remote(mapa_shared(smem_u32(red_empty), pr));
+          ++xchg;
         } else {
 #pragma unroll
           for (int j = 0; j < CH; ++j) part[(c0 + j) * 128 + q * 32 + lane] = v[j];
         }
       }
-      if (p.splits > 1) {
+      if (stop) break;
+      if (p.splits > 1 && !p.cluster) {
         __threadfence();
         named_bar_sync(1, 128);
         if (ew == 0 && lane == 0) {
@@ -439,6 +527,9 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // No CTA leaves while another may still read its shared memory or arrive
+  // on its barriers. Every role's waits are bounded, so all threads get here.
+  if (p.cluster) cluster_sync_all();
 }
 
 template <int BT>
@@ -463,9 +554,11 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return R4_ERR_CUDA;
   }
-  // Output through TMA tensor stores when C's base and row stride are 16-byte aligned.
+  // Output through TMA tensor stores when C's base, row stride and row length
+  // are 16-byte multiples. (Measured on GB300: a tensor store whose row ends
+  // inside a 16-byte granule writes the whole granule, past column N.)
   int use_tma_store = 0;
-  if ((reinterpret_cast<uintptr_t>(c) % 16) == 0 && (ldc * 2) % 16 == 0) {
+  if ((reinterpret_cast<uintptr_t>(c) % 16) == 0 && (ldc * 2) % 16 == 0 && (N * 2) % 16 == 0) {
     const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
     const uint64_t strides[1] = {static_cast<uint64_t>(ldc) * 2};
     const uint32_t box[2] = {128, static_cast<uint32_t>(C::kOutChunk)};
@@ -483,6 +576,9 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
   p.units = pl.units;
   p.ldc = static_cast<int>(ldc);
   p.tma_store = use_tma_store;
+  p.l2_prefetch = options().l2_prefetch;
+  p.cluster = pl.cluster;
+  p.w = packed;
   p.s = s;
   p.sf = packed + mx_packed_codes_bytes(N, K);
   p.c = c;
@@ -491,8 +587,11 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
   p.err = device_error_word();
   auto kern = w4a8_mxf8f6f4_kernel<BT>;
   if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::kSmemBytes) != cudaSuccess) return R4_ERR_CUDA;
-  if (launch_pdl(kern, dim3(pl.grid), dim3(C::kThreads), C::kSmemBytes, st, tm_w, tm_x, tm_c, p) != cudaSuccess)
-    return R4_ERR_CUDA;
+  const cudaError_t le =
+      pl.cluster ? launch_pdl_cluster(kern, dim3(pl.grid), dim3(C::kThreads), C::kSmemBytes, st, pl.splits, tm_w, tm_x,
+                                      tm_c, p)
+                 : launch_pdl(kern, dim3(pl.grid), dim3(C::kThreads), C::kSmemBytes, st, tm_w, tm_x, tm_c, p);
+  if (le != cudaSuccess) return R4_ERR_CUDA;
   set_last_kernel(BT == 16    ? "w4a8_mxf8f6f4_kernel<16>"
                   : BT == 32  ? "w4a8_mxf8f6f4_kernel<32>"
                   : BT == 64  ? "w4a8_mxf8f6f4_kernel<64>"
@@ -501,12 +600,57 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
   return cudaGetLastError() == cudaSuccess ? R4_OK : R4_ERR_CUDA;
 }
 
+// Co-resident clusters of `s` CTAs (2..8) the BT kernel can have on this
+// device (0: none / unsupported). Cached after the first query.
+template <int BT>
+int max_clusters_bt(int s) {
+  using C = Cfg<BT>;
+  static int cache[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};   // 0 unknown, -1 none
+  if (s < 2 || s > 8) return 0;
+  if (cache[s] != 0) return cache[s] > 0 ? cache[s] : 0;
+  auto kern = w4a8_mxf8f6f4_kernel<BT>;
+  int n = 0;
+  if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::kSmemBytes) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(s * 16));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(s);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();   // a failed query leaves no sticky error
+  cache[s] = n > 0 ? n : -1;
+  return n > 0 ? n : 0;
+}
+
+int max_clusters(int bt, int s) {
+  switch (bt) {
+    case 16: return max_clusters_bt<16>(s);
+    case 32: return max_clusters_bt<32>(s);
+    case 64: return max_clusters_bt<64>(s);
+    default: return 0;
+  }
+}
+
 }  // namespace w4a8
 
 // Token tile and split-K choice. A small wave model: every SM streams its
-// unit's weight bytes at an equal share of HBM bandwidth or runs its MMAs at
-// the per-SM FP8 rate, whichever is slower; split-K adds its partial traffic
-// and the serial final reduction of the last-arriving CTA.
+// unit's weight bytes at an equal share of HBM bandwidth (capped by what one
+// CTA keeps in flight) or runs its MMAs at the per-SM FP8 rate, whichever is
+// slower. Split-K either exchanges partials inside a thread-block cluster of
+// `splits` CTAs (decode tiles, 2..8 splits: a fixed cost per unit, no
+// workspace) or writes them to the workspace, where the last-arriving CTA
+// sums them at the few tens of GB/s one CTA's plain loads reach. The
+// constants were fitted to a GB300 sweep of split factors on the decode and
+// prefill shapes. Prefill tiles (BT >= 128) are never split once the tile
+// count is a quarter of the SM count: there the partial tiles cost more than
+// the idle SMs.
 GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
   GemmPlan pl;
   int bt = options().w4a8_token_tile;
@@ -516,37 +660,67 @@ GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
   pl.t_tiles = static_cast<int>(ceil_div(M, bt));
   pl.KB = static_cast<int>(ceil_div(K, 128));
   const int64_t tiles = static_cast<int64_t>(pl.n_tiles) * pl.t_tiles;
-  // per-SM streaming rate is capped (bytes in flight / latency), not hbm/active
-  const double hbm = 6.5e12, sm_bw = 60e9, sm_flops = 4.5e15 / 152.0, sm_l2 = 150e9;
+  const double hbm = 6.0e12, sm_bw = 70e9, sm_flops = 4.5e15 / 152.0, red_bw = 20e9;
   const double kb_bytes = 128.0 * 128 * 0.5 + 512 + 128.0 * bt;      // weight + scales + activations
   const double kb_flops = 2.0 * 128 * bt * 128;
-  int best_s = 1;
-  double best_t = 1e30;
+  const double part_bytes = 128.0 * bt * 4;
+  const double xchg_s = 2.5e-6 * ((bt + 31) / 32);                   // one cluster exchange per 32 tokens
   const int forced = options().w4a8_splits;
-  for (int s = 1; s <= std::min(pl.KB, 64); ++s) {
+  const int max_s = (bt >= 128 && tiles * 4 >= sms && !forced) ? 1 : std::min(pl.KB, 64);
+  int best_s = 1, best_cl = 0;
+  int64_t best_grid = std::min<int64_t>(tiles, sms);
+  double best_t = 1e30;
+  // A forced factor is rounded to the nearest schedule without an empty split.
+  const int forced_s =
+      forced > 0 ? static_cast<int>(ceil_div(pl.KB, ceil_div(pl.KB, std::min(forced, pl.KB)))) : 0;
+  for (int s = 1; s <= max_s; ++s) {
+    if (forced_s && s != forced_s) continue;
     const int kbps = static_cast<int>(ceil_div(pl.KB, s));
     if (static_cast<int64_t>(s - 1) * kbps >= pl.KB) continue;   // would leave an empty split
     const int64_t units = tiles * s;
-    const int64_t active = std::min<int64_t>(units, sms);
-    const double waves = std::ceil(static_cast<double>(units) / sms);
-    const double t_unit = std::max(kbps * kb_bytes / std::min(hbm / active, sm_bw), kbps * kb_flops / sm_flops);
-    double t = waves * t_unit;
-    if (s > 1) {
-      const double pbytes = static_cast<double>(units) * 128 * bt * 4;
-      t += 2 * pbytes / hbm + s * 128.0 * bt * 4 / sm_l2;
+    // Decode tiles split only while all units fit in one wave (measured: a
+    // second wave of split units always loses to fewer splits).
+    if (!forced_s && s > 1 && bt <= 64 && units > sms) continue;
+    // The cluster exchange beats the workspace path from 32 tokens up
+    // (measured); at 16 tokens the partial tiles are small enough that the
+    // last-arriving CTA sums them faster than a cluster round trip.
+    const int ncl = (options().cluster_split && bt >= 32 && bt <= 64 && s >= 2 && s <= 6)
+                        ? w4a8::max_clusters(bt, s)
+                        : 0;
+    double t;
+    int64_t grid;
+    if (ncl > 0) {
+      const int64_t nclust = std::min<int64_t>(tiles, ncl);
+      const int64_t active = nclust * s;
+      const double waves = std::ceil(static_cast<double>(tiles) / nclust);
+      const double t_unit =
+          std::max(kbps * kb_bytes / std::min(hbm / active, sm_bw), kbps * kb_flops / sm_flops);
+      t = waves * t_unit + xchg_s + 0.5e-6 * s;
+      grid = active;
+    } else {
+      const int64_t active = std::min<int64_t>(units, sms);
+      const double waves = std::ceil(static_cast<double>(units) / sms);
+      const double t_unit =
+          std::max(kbps * kb_bytes / std::min(hbm / active, sm_bw), kbps * kb_flops / sm_flops);
+      t = waves * t_unit;
+      if (s > 1) t += (waves + s) * part_bytes / red_bw;
+      grid = active;
     }
-    if (forced ? (s == forced) : (t < best_t * 0.97)) {
+    if (t < best_t) {
       best_t = t;
       best_s = s;
+      best_cl = ncl > 0;
+      best_grid = grid;
     }
   }
-  if (forced && forced <= pl.KB) best_s = forced;
   pl.splits = best_s;
   pl.kb_per_split = static_cast<int>(ceil_div(pl.KB, best_s));
   pl.splits = static_cast<int>(ceil_div(pl.KB, pl.kb_per_split));  // no empty split
+  if (pl.splits != best_s) best_cl = 0;                              // (cannot happen: empty splits skipped)
   pl.units = static_cast<int>(tiles * pl.splits);
-  pl.grid = std::min(pl.units, sms);
-  if (pl.splits > 1) {
+  pl.cluster = best_cl;
+  pl.grid = static_cast<int>(best_grid);
+  if (pl.splits > 1 && !pl.cluster) {
     pl.counters_bytes = round_up(static_cast<size_t>(tiles) * 4, 256);
     pl.ws_bytes = pl.counters_bytes + static_cast<size_t>(pl.units) * 128 * bt * 4;
   }

@@ -14,6 +14,10 @@
 
 #ifndef R4_WAIT_TIMEOUT_NS
 #define R4_WAIT_TIMEOUT_NS 2000000000ull  // 2 s of global time
+// Upper bound on how long one mbarrier try_wait may suspend the thread (it
+// resumes as soon as the phase completes): a waiting warp then issues no
+// instructions instead of spinning against the warps doing the work.
+#define R4_SUSPEND_HINT_NS 100000u
 #endif
 
 namespace r4 {
@@ -25,7 +29,8 @@ enum : int {
   DEV_ERR_WAIT_EMPTY = 2,    // producer gave up waiting for a free stage
   DEV_ERR_WAIT_ACC_FULL = 3, // epilogue gave up waiting for the accumulator
   DEV_ERR_WAIT_ACC_EMPTY = 4,// MMA issuer gave up waiting for the epilogue
-  DEV_ERR_WAIT_DRAIN = 5     // final drain of in-flight work gave up
+  DEV_ERR_WAIT_DRAIN = 5,    // final drain of in-flight work gave up
+  DEV_ERR_WAIT_PEER = 6      // split-K exchange gave up waiting for another CTA of the cluster
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -73,10 +78,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(R4_SUSPEND_HINT_NS)
       : "memory");
   return ok != 0;
 }
@@ -102,6 +107,87 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 }
 
 // ---------------------------------------------------------------- TMA
+
+// ---------------------------------------------------------------- thread-block clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (address from
+// mapa_shared); release at cluster scope orders this thread's earlier
+// writes (and what it synchronised with) before the arrival.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(R4_SUSPEND_HINT_NS)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait with cluster-scope acquire (the phase was completed by
+// arrivals from other CTAs of the cluster); same contract as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort, int *err,
+                                                  int code) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > R4_WAIT_TIMEOUT_NS) {
+        *abort = 1;
+        atomicCAS(err, 0, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// Full cluster barrier, executed by every thread of every CTA of the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Warp-wide bounded wait: lane 0 polls the barrier (an mbarrier poll by all
+// 32 lanes is 32 shared-memory barrier operations), the warp then syncs and
+// every lane gets lane 0's result. The warp barrier orders the lanes'
+// following accesses after lane 0's acquire.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *err,
+                                          int code) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, err, code);
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -304,6 +390,28 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier over `nthreads` threads that also ORs a per-thread flag: every
+// participant gets the same result (used to agree on stopping).
+__device__ __forceinline__ bool named_bar_any(int id, int nthreads, bool flag) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"(flag ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
+}
+
+// Two fp32 fused multiply-adds in one instruction: (d0, d1) += (a0, a1) * (b0, b1),
+// each rounded once (IEEE fma).
+__device__ __forceinline__ void fma_f32x2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%0, %1};\n\tfma.rn.f32x2 rc, ra, rb, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {

@@ -31,6 +31,8 @@ struct Options {
   int w4a8_token_tile = 0;  // 0 = automatic
   int fp8_splits = 0;       // 0 = automatic
   int pdl = 1;              // launch with programmatic stream serialization
+  int l2_prefetch = 0;      // W4A8: bulk L2 prefetch of each unit's weight range, one unit ahead
+  int cluster_split = 1;    // W4A8 decode tiles: split-K across a thread-block cluster when possible
 };
 Options &options();
 
@@ -52,6 +54,27 @@ cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStre
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// launch_pdl with a 1-D thread-block cluster of `cluster_x` CTAs.
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl_cluster(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster_x,
+                               Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = options().pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ------------------------------------------------------------------ plans
 // One output tile = 128 weight rows (n) x BT tokens (t). A work unit is a
 // tile and a contiguous range of 128-K blocks (its split).
@@ -61,6 +84,7 @@ struct GemmPlan {
   int KB = 0;            // number of 128-K blocks (K padded to 128)
   int splits = 1, kb_per_split = 0;
   int units = 0, grid = 0;
+  int cluster = 0;       // 1: split-K across a cluster of `splits` CTAs (partials in DSMEM, no workspace)
   size_t counters_bytes = 0;  // arrival counters (one int per tile), 256-B rounded
   size_t ws_bytes = 0;        // total workspace (0 when splits == 1)
 };

@@ -93,3 +93,20 @@ def test_end_to_end_group_quant(r4q):
     q, As = Q.quant_act(x.float().numpy(), group=128)
     c64, _ = G.gemm_blockfp8(q, As, wq, Ws)
     assert_gemm_matches(c, c64, "end-to-end")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 384, 1024), (13, 51200, 2048), (16, 256, 640), (17, 1024, 4096),
+                                   (33, 768, 1152), (100, 2048, 1024), (129, 384, 512), (300, 8192, 1024)])
+def test_token_tiles_ragged(r4q, M, N, K):
+    """Every token tile (16/32/64/128) with a ragged last tile; the larger
+    cases give each CTA several units, so the K-block slots wrap the scale
+    ring and the tensor-memory accumulator buffers many times."""
+    q = random_e4m3_codes((M, K), seed=M)
+    As = np.random.default_rng(M + 1).uniform(1e-3, 1e-2, (M, K // 128)).astype(np.float32)
+    w = random_e4m3_codes((N, K), seed=M + 2)
+    Ws = np.random.default_rng(M + 3).uniform(1e-4, 1e-3, (N // 128, K // 128)).astype(np.float32)
+    c = _run(r4q, q, As, w, Ws, N, K)
+    rows = None if N <= 2048 else synth.sample_indices(N, 384, M).numpy()
+    c64, _ = G.gemm_blockfp8(q, As, w, Ws, rows=rows)
+    got = c if rows is None else c[:, torch.from_numpy(rows).cuda()]
+    assert_gemm_matches(got, c64, f"M={M} N={N} K={K}")

@@ -19,6 +19,7 @@ def r4q():
     yield m
     m.r4_set_option(1, 0)
     m.r4_set_option(2, 0)
+    m.r4_set_option(6, 1)
 
 
 def _run(r4q, q_np, s_np, packed_np, scale_np, N, K, ldc=None):
@@ -100,6 +101,32 @@ def test_forced_tiles_and_splits(r4q, bt, splits):
     c64, _ = G.gemm_w4a8(q, s, p, sc)
     assert_gemm_matches(c, c64, f"bt={bt} splits={splits}")
     assert torch.equal(c, c2), "not deterministic across calls"
+
+
+@pytest.mark.parametrize("cluster", [0, 1])
+@pytest.mark.parametrize("M,N,K,splits", [(37, 300, 416, 4), (13, 640, 1792, 7), (40, 38400, 1024, 4),
+                                          (64, 2048, 5120, 5), (6, 5120, 17408, 8)])
+def test_split_k_paths(r4q, cluster, M, N, K, splits):
+    """Split-K through the cluster's distributed shared memory (option 6 on)
+    and through the workspace (off): ragged N with a guard band, 7 splits
+    (uneven n shares per CTA), more tiles than co-resident clusters (several
+    exchanges per CTA), full decode shapes. Deterministic across calls."""
+    q, s, p, sc = _dense_inputs(M, N, K, synth.CFG_DECODE)
+    ldc = N + 24
+    r4q.r4_set_option(1, splits)
+    r4q.r4_set_option(6, cluster)
+    try:
+        c, full = _run(r4q, q, s, p, sc, N, K, ldc=ldc)
+        c2, _ = _run(r4q, q, s, p, sc, N, K)
+    finally:
+        r4q.r4_set_option(1, 0)
+        r4q.r4_set_option(6, 1)
+    rows = None if N <= 2048 else synth.sample_indices(N, 384, M).numpy()
+    c64, _ = G.gemm_w4a8(q, s, p, sc, rows=rows)
+    got = c if rows is None else c[:, torch.from_numpy(rows).cuda()]
+    assert_gemm_matches(got, c64, f"M={M} N={N} K={K} splits={splits} cluster={cluster}")
+    assert torch.equal(c, c2), "not deterministic across calls"
+    assert np.all(full.float().cpu().numpy()[:, N:] == 7.0), "kernel wrote outside columns [0, N)"
 
 
 def _sampled_full_size(r4q, M, N, K, seed, nsample=384):

@@ -26,6 +26,7 @@ def r4q():
     m = require_gpu()
     yield m
     m.r4_set_option(1, 0)
+    m.r4_set_option(6, 1)
 
 
 def test_noalloc_matches_workspace_entry_point_twice(r4q):
@@ -37,7 +38,8 @@ def test_noalloc_matches_workspace_entry_point_twice(r4q):
     q = torch.from_numpy(q_np).cuda()
     s = torch.from_numpy(s_np).cuda()
     pk = r4q.prepack_mxfp4(torch.from_numpy(p).cuda(), torch.from_numpy(sc).cuda(), N, K)
-    r4q.r4_set_option(1, 4)                       # force split-K so the scratch is used
+    r4q.r4_set_option(1, 4)                       # force split-K through the workspace
+    r4q.r4_set_option(6, 0)                       # (not the cluster exchange) so the scratch is used
     try:
         assert r4q.r4_gemm_workspace_bytes(r4q.R4_OP_W4A8_MXFP4, M, N, K) > 0
         ref = r4q.gemm_w4a8(q, s, pk, N, K)       # existing entry point, caller workspace
@@ -49,6 +51,7 @@ def test_noalloc_matches_workspace_entry_point_twice(r4q):
         check_device_error(r4q)
     finally:
         r4q.r4_set_option(1, 0)
+        r4q.r4_set_option(6, 1)
     c64, _ = G.gemm_w4a8(q_np, s_np, p, sc)
     ref64 = bf16_to_np(ref)
     for c in outs:
