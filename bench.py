@@ -379,6 +379,27 @@ def run_sections(r4q, synth, device, sweep, l2_bytes, peaks):
         qt[f"M{M}_K{K}"] = {"us": round(ms * 1e3, 2), "GBps": round((3 * M * K + 4 * M) / ms / 1e6, 1)}
         del g
     out["quant_per_token"] = qt
+    # tiny W4A8 linear (quant + GEMM per call, as a decode step issues it)
+    M, N, K = synth.TINY["M"], synth.TINY["N"], synth.TINY["K"]
+    w = synth.weights_fp32(N, K, synth.CFG_TINY).to(device)
+    p_, sc_ = r4q.quantize_mxfp4_weight(w)
+    pk = r4q.prepack_mxfp4(p_, sc_, N, K)
+    x = synth.activations(M, K, synth.CFG_TINY).to(device)
+    q = torch.empty((M, K), dtype=torch.uint8, device=device)
+    s = torch.empty((M,), dtype=torch.float32, device=device)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    ws = r4q.workspace(r4q.R4_OP_W4A8_MXFP4, M, N, K, device)
+    R = 50
+
+    def fn():
+        for _ in range(R):
+            r4q.r4_quant_fp8_per_token(x, M, K, K, K, q, s)
+            r4q.r4_gemm_w4a8_mxfp4(q, s, pk, M, N, K, c, N, ws)
+
+    g = capture(fn)
+    ms = time_graph(g, 10) / R
+    out["tiny_w4a8"] = {f"M{M}_N{N}_K{K}": {"us_quant_plus_gemm": round(ms * 1e3, 2)}}
+    del g
     return out
 
 

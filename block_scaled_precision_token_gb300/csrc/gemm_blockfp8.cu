@@ -560,7 +560,8 @@ int launch_bt(const uint8_t *q, const float *As, const uint8_t *packed, int64_t 
 // block-FP8 per-K-block bytes (16 KiB of e4m3 weights).
 GemmPlan plan_blockfp8(int64_t M, int64_t N, int64_t K, int sms) {
   GemmPlan pl;
-  const int bt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  int bt = options().fp8_token_tile;
+  if (bt == 0) bt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
   pl.BT = bt;
   pl.n_tiles = static_cast<int>(N / 128);
   pl.t_tiles = static_cast<int>(ceil_div(M, bt));

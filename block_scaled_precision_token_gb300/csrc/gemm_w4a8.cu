@@ -80,7 +80,7 @@ struct Params {
   int t_tiles, splits, kb_per_split, units;
   int ldc;
   int tma_store;         // 1: bf16 output tiles leave through smem + TMA tensor stores
-  int l2_prefetch;       // 1: producer 0 prefetches each unit's weight range into L2, one unit ahead
+  int l2_prefetch;       // 1: producer 0 prefetches the CTA's whole weight range into L2 at start
   int cluster;           // 1: the `splits` CTAs of a cluster split K and exchange partials in DSMEM
   const uint8_t *w;      // packed weight codes [NT][KB][128][64]
   const float *s;
@@ -215,7 +215,11 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       // stages with weight tiles (+ scale atoms) before waiting for it, so
       // under programmatic dependent launch the weight stream starts while
       // the previous kernel is still running.
-      if (p.l2_prefetch && pw == 0) prefetch_unit_l2(p, blockIdx.x);
+      // Optionally ask L2 for this CTA's whole weight range up front: the
+      // stream then runs at HBM rate while this kernel waits for its
+      // predecessor, not only for the ring's depth.
+      if (p.l2_prefetch && pw == 0)
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) prefetch_unit_l2(p, u);
       {
         int g = 0;
         for (int u = blockIdx.x; u < p.units && g < C::kStages; u += gridDim.x) {
@@ -248,7 +252,6 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
         decode_unit(p, u, nt, tt, sp, kb0, kb1);
         const int nkb = kb1 - kb0;
         const int nslots = (nkb + ISS - 1) / ISS * ISS;
-        if (p.l2_prefetch && pw == 0) prefetch_unit_l2(p, u + gridDim.x);
         for (int i = pw; i < nslots; i += ISS) {
           uint8_t *st = smem + stage * C::kStageBytes;
           const int kb = kb0 + i;
@@ -634,6 +637,8 @@ int max_clusters(int bt, int s) {
     case 16: return max_clusters_bt<16>(s);
     case 32: return max_clusters_bt<32>(s);
     case 64: return max_clusters_bt<64>(s);
+    case 128: return max_clusters_bt<128>(s);
+    case 256: return max_clusters_bt<256>(s);
     default: return 0;
   }
 }
@@ -664,9 +669,13 @@ GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
   const double kb_bytes = 128.0 * 128 * 0.5 + 512 + 128.0 * bt;      // weight + scales + activations
   const double kb_flops = 2.0 * 128 * bt * 128;
   const double part_bytes = 128.0 * bt * 4;
-  const double xchg_s = 2.5e-6 * ((bt + 31) / 32);                   // one cluster exchange per 32 tokens
+  const double xchg_s = (bt <= 64 ? 2.5e-6 : 1.0e-6) * ((bt + 31) / 32);   // one cluster exchange per 32 tokens
   const int forced = options().w4a8_splits;
-  const int max_s = (bt >= 128 && tiles * 4 >= sms && !forced) ? 1 : std::min(pl.KB, 64);
+  // Prefill tiles (BT >= 128) split through the workspace only while the
+  // tile count is under a quarter of the SM count, and through a cluster
+  // only while one wave of clusters covers every tile.
+  const bool prefill_ws_ok = tiles * 4 < sms;
+  const int max_s = std::min(pl.KB, 64);
   int best_s = 1, best_cl = 0;
   int64_t best_grid = std::min<int64_t>(tiles, sms);
   double best_t = 1e30;
@@ -684,9 +693,13 @@ GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
     // The cluster exchange beats the workspace path from 32 tokens up
     // (measured); at 16 tokens the partial tiles are small enough that the
     // last-arriving CTA sums them faster than a cluster round trip.
-    const int ncl = (options().cluster_split && bt >= 32 && bt <= 64 && s >= 2 && s <= 6)
-                        ? w4a8::max_clusters(bt, s)
-                        : 0;
+    // Prefill tiles take the cluster path only when forced: each 32-token
+    // chunk costs a cluster round trip, and at 256 tokens the eight round
+    // trips ate the gain (measured: M=256, 5120x17408, 3 splits 49.9 us vs
+    // 49.8 us unsplit).
+    const bool cl_ok = bt <= 64 || forced_s;
+    const int ncl = (options().cluster_split && cl_ok && bt >= 32 && s >= 2 && s <= 6) ? w4a8::max_clusters(bt, s) : 0;
+    if (bt >= 128 && !forced_s && s > 1 && !prefill_ws_ok) continue;
     double t;
     int64_t grid;
     if (ncl > 0) {

@@ -227,10 +227,12 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * (0 = automatic); key 2: force the W4A8 token tile (0 = automatic, else
  * 16/32/64/128/256); key 3: force the block-FP8 split-K factor; key 4:
  * programmatic dependent launch on (1, default) or off (0); key 5: W4A8
- * bulk L2 prefetch of each unit's weight range one unit ahead (1) or not (0);
+ * bulk L2 prefetch of each CTA's whole weight range at kernel start (1) or
+ * not (0);
  * key 6: W4A8 decode split-K across a thread-block cluster with the partial
  * sums exchanged in distributed shared memory (1, default) or through the
- * caller's workspace (0).
+ * caller's workspace (0); key 7: force the block-FP8 token tile (0 =
+ * automatic, else 16/32/64/128).
  */
 int r4_set_option(int key, int64_t value);
 

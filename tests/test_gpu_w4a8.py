@@ -105,7 +105,7 @@ def test_forced_tiles_and_splits(r4q, bt, splits):
 
 @pytest.mark.parametrize("cluster", [0, 1])
 @pytest.mark.parametrize("M,N,K,splits", [(37, 300, 416, 4), (13, 640, 1792, 7), (40, 38400, 1024, 4),
-                                          (64, 2048, 5120, 5), (6, 5120, 17408, 8)])
+                                          (64, 2048, 5120, 5), (6, 5120, 17408, 8), (300, 640, 2048, 3)])
 def test_split_k_paths(r4q, cluster, M, N, K, splits):
     """Split-K through the cluster's distributed shared memory (option 6 on)
     and through the workspace (off): ragged N with a guard band, 7 splits
