@@ -13,10 +13,11 @@
 //    fp32 accumulator in tensor memory. Slot g uses accumulator buffer
 //    g % kNumBuf; with 512 columns there are 4 (BT = 128) to 16 buffers, so
 //    the MMAs run several K blocks ahead of the promotion epilogue;
-//  * a scale warp streams As[t0.., kb] and Ws[nt, kb] into a ring of shared
-//    memory slots with 4-byte cp.async copies (their landing tracked by an
-//    mbarrier, so no warp waits on global-load latency per K block), turns
-//    them into the per-column products As * Ws, and publishes each slot;
+//  * a scale warp turns As[t0.., kb] and Ws[nt, kb] into the per-token
+//    products As * Ws of each K block and publishes them in a ring of shared
+//    memory slots. With K/128 a multiple of 4 the scales arrive with the
+//    pipeline stage (a TMA box of As and a 16-byte copy of Ws); otherwise the
+//    warp loads As in coalesced row chunks, one chunk ahead in registers;
 //  * 4 x kH epilogue warps (one per tensor-memory lane quarter and column
 //    group of 32 tokens) load the block result and fold it into fp32
 //    registers: acc[t] += (As[t,kb] * Ws[nt,kb]) * D_kb[n,t], two columns per
