@@ -18,6 +18,9 @@ Sources (page title, then the section on it):
     activations with one scale per token per 128 K).
   * radiance_gemm.py -- module docstring (skinny bf16 NT GEMM C = x W^T with
     fp32 accumulation).
+  * radiance_arnq.py -- module docstring, ``ar_add_rms_quant``,
+    ``silu_mul_quant`` and the ``_SiluMulQuant`` docstring (fused residual-add
+    + RMS norm + quant and SiluAndMul + quant producers).
 
 Modules:
   formats -- value tables and round-to-nearest-even encoders for e4m3, e2m1,
@@ -25,6 +28,8 @@ Modules:
   quant   -- activation quantization (per token, per 128-K group) and the
              weight quantizers used only to manufacture test inputs.
   gemm    -- the three GEMM definitions.
+  fused   -- the fused quantization producers (add + RMS norm + quant,
+             SiluAndMul + quant).
 """
 
-from . import formats, quant, gemm  # noqa: F401
+from . import formats, quant, gemm, fused  # noqa: F401
