@@ -379,6 +379,41 @@ def run_sections(r4q, synth, device, sweep, l2_bytes, peaks):
         qt[f"M{M}_K{K}"] = {"us": round(ms * 1e3, 2), "GBps": round((3 * M * K + 4 * M) / ms / 1e6, 1)}
         del g
     out["quant_per_token"] = qt
+    # fused quantization producers (one launch each; HBM-bound row kernels)
+    fq = {}
+    for (M, K) in [(8, 5120), (64, 5120), (2048, 5120), (8192, 5120)]:
+        y = synth.activations(M, K, synth.CFG_PREFILL).to(device)
+        res = synth.activations(M, K, synth.CFG_DECODE).to(device)
+        wn = (synth.activations(1, K, synth.CFG_TINY)[0] * 0.1).to(torch.bfloat16).to(device)
+        q = torch.empty((M, K), dtype=torch.uint8, device=device)
+        s = torch.empty((M,), dtype=torch.float32, device=device)
+        ro = torch.empty_like(res)
+        R = 20
+
+        def fn():
+            for _ in range(R):
+                r4q.r4_add_rmsnorm_quant_fp8(y, res, wn, 1e-6, M, K, ro, q, s)
+
+        g = capture(fn)
+        ms = time_graph(g, 10) / R
+        fq[f"add_rmsnorm_quant_M{M}_K{K}"] = {"us": round(ms * 1e3, 2),
+                                              "GBps": round((7 * M * K + 2 * K + 4 * M) / ms / 1e6, 1)}
+        del g
+    for (M, N) in [(8, 17408), (64, 17408), (2048, 17408)]:
+        gu = synth.activations(M, 2 * N, synth.CFG_PREFILL).to(device)
+        q = torch.empty((M, N), dtype=torch.uint8, device=device)
+        s = torch.empty((M,), dtype=torch.float32, device=device)
+        R = 20
+
+        def fn():
+            for _ in range(R):
+                r4q.r4_silu_mul_quant_fp8(gu, M, N, q, s)
+
+        g = capture(fn)
+        ms = time_graph(g, 10) / R
+        fq[f"silu_mul_quant_M{M}_N{N}"] = {"us": round(ms * 1e3, 2), "GBps": round((5 * M * N + 4 * M) / ms / 1e6, 1)}
+        del g
+    out["fused_quant"] = fq
     # tiny W4A8 linear (quant + GEMM per call, as a decode step issues it)
     M, N, K = synth.TINY["M"], synth.TINY["N"], synth.TINY["K"]
     w = synth.weights_fp32(N, K, synth.CFG_TINY).to(device)
@@ -633,6 +668,18 @@ def run_one(spec):
         q, As = r4q.quant_fp8(synth.activations(M, K, synth.CFG_BLOCKFP8).to(dev), group=128)
         for _ in range(3):
             r4q.gemm_blockfp8(q, As, pk, N, K)
+    elif kind == "arq":
+        M, K = dims
+        y = synth.activations(M, K, synth.CFG_PREFILL).to(dev)
+        res = synth.activations(M, K, synth.CFG_DECODE).to(dev)
+        wn = (synth.activations(1, K, synth.CFG_TINY)[0] * 0.1).to(torch.bfloat16).to(dev)
+        for _ in range(3):
+            r4q.add_rmsnorm_quant(y, res, wn, 1e-6)
+    elif kind == "smq":
+        M, N = dims
+        gu = synth.activations(M, 2 * N, synth.CFG_PREFILL).to(dev)
+        for _ in range(3):
+            r4q.silu_mul_quant(gu)
     elif kind == "skinny":
         M, N, K = dims
         x = synth.activations(M, K, synth.CFG_SKINNY).to(dev)
@@ -657,7 +704,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--one", nargs="+", metavar="ARG",
-                    help="profiling driver: KIND M N K (KIND = w4a8 | fp8 | skinny) or quant M K; "
+                    help="profiling driver: KIND M N K (KIND = w4a8 | fp8 | skinny), quant M K, "
+                         "arq M K (add + RMS norm + quant) or smq M N (SiluAndMul + quant); "
                          "runs three launches of that one call and exits")
     args = ap.parse_args(argv)
     if args.one:

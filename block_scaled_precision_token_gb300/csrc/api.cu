@@ -186,6 +186,29 @@ int r4_quant_fp8_per_token(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
              : R4_ERR_CUDA;
 }
 
+int r4_add_rmsnorm_quant_fp8(const uint16_t *y, const uint16_t *residual, const uint16_t *weight, float eps,
+                             int64_t M, int64_t K, uint16_t *residual_out, uint8_t *q, float *s, r4_stream_t stream) {
+  if (!y || !residual || !weight || !residual_out || !q || !s) return R4_ERR_INVALID_ARG;
+  if (M < 1 || K < 8 || M > (1 << 30) || !(eps >= 0.f) || eps > 3.0e38f) return R4_ERR_INVALID_ARG;
+  if (K % 8 || K > 24576) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(y, 16) || !aligned(residual, 16) || !aligned(weight, 16) || !aligned(residual_out, 16) ||
+      !aligned(q, 8) || !aligned(s, 4))
+    return R4_ERR_MISALIGNED;
+  return launch_add_rmsnorm_quant(y, residual, weight, eps, M, K, residual_out, q, s,
+                                  reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? R4_OK
+             : R4_ERR_CUDA;
+}
+
+int r4_silu_mul_quant_fp8(const uint16_t *gu, int64_t M, int64_t N, uint8_t *q, float *s, r4_stream_t stream) {
+  if (!gu || !q || !s) return R4_ERR_INVALID_ARG;
+  if (M < 1 || N < 8 || M > (1 << 30)) return R4_ERR_INVALID_ARG;
+  if (N % 8 || N > 24576) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(gu, 16) || !aligned(q, 8) || !aligned(s, 4)) return R4_ERR_MISALIGNED;
+  return launch_silu_mul_quant(gu, M, N, q, s, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? R4_OK
+                                                                                                    : R4_ERR_CUDA;
+}
+
 int r4_quantize_mxfp4_weight(const float *w, int64_t N, int64_t K, uint8_t *packed, uint8_t *scale,
                              r4_stream_t stream) {
   if (!w || !packed || !scale || N < 1 || K < 32) return R4_ERR_INVALID_ARG;

@@ -1,0 +1,206 @@
+// fused_quant.cu -- per-token e4m3 quantization fused with the epilogue that
+// produces a W4A8 linear's input ("radiance_arnq.py": ar_add_rms_quant and
+// silu_mul_quant; the module docstring's single-rank epilogue).
+//
+//  * add + Gemma RMS norm + quant: r = bf16(y + residual) (the new residual,
+//    written out), h = bf16(r / sqrt(mean(r^2) + eps) * (1 + w)), then the
+//    per-token rule on h.
+//  * SiluAndMul + quant on [g | u]: h = bf16(bf16(silu(g)) * u), then the
+//    per-token rule.
+//
+// HBM-bound row kernels: one CTA per row holds the row in registers (16-byte
+// vectors, read once), reduces it twice (sum of squares, then amax) and
+// writes the codes -- one launch where the unfused chain takes two or three.
+// The row's arithmetic is fp32 with correctly rounded division and
+// reciprocal square root; expf is CUDA's.
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "quant_common.cuh"
+#include "r4_device.cuh"
+#include "r4_internal.h"
+
+namespace r4 {
+namespace {
+
+using namespace qc;
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint32_t bf16_rn_bits(float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  return static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&h));
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) { return bf16_rn_bits(lo) | (bf16_rn_bits(hi) << 16); }
+
+// Block-wide sum / max of one float per thread (fixed order: deterministic).
+__device__ __forceinline__ float block_sum(float a, float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+  const int nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  float t = red[0];
+  for (int w = 1; w < nw; ++w) t += red[w];
+  __syncthreads();   // red is reused by the next reduction
+  return t;
+}
+__device__ __forceinline__ float block_max(float a, float *red) {
+  a = warp_max(a);
+  const int nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  float t = red[0];
+  for (int w = 1; w < nw; ++w) t = fmaxf(t, red[w]);
+  return t;
+}
+
+// Scale and codes for one row held as bf16 vectors h[VPT]; writes s[row], q.
+template <int VPT>
+__device__ __forceinline__ void quant_row(const uint4 (&h)[VPT], int K, uint8_t *qr, float *s_row, float *red) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) a = fmaxf(a, absmax8(h[i]));   // padding vectors are zero
+  a = block_max(a, red);
+  const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
+  if (tid == 0) *s_row = sc;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int k = (i * nt + tid) * 8;
+    if (k < K) *reinterpret_cast<uint2 *>(qr + k) = quant8(h[i], sc);
+  }
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_kernel(const uint16_t *__restrict__ y,
+                                                                   const uint16_t *res, const uint16_t *__restrict__ w,
+                                                                   float eps, int K, uint16_t *ro,
+                                                                   uint8_t *__restrict__ q, float *__restrict__ s) {
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  pdl_wait();   // y and the residual come from the preceding kernels
+  __shared__ float red[kThreads / 32];
+  const int row = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+  const size_t base = static_cast<size_t>(row) * K;
+  uint4 r[VPT];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int k = (i * nt + tid) * 8;
+    if (k < K) {
+      // res may alias ro (in-place residual update): each vector is read
+      // before the same thread writes it.
+      const uint4 a = __ldg(reinterpret_cast<const uint4 *>(y + base + k));
+      const uint4 b = *reinterpret_cast<const uint4 *>(res + base + k);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      uint32_t rv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        rv[j] = pack2(bf16lo(av[j]) + bf16lo(bv[j]), bf16hi(av[j]) + bf16hi(bv[j]));
+        const float lo = bf16lo(rv[j]), hi = bf16hi(rv[j]);
+        ss = fmaf(lo, lo, ss);
+        ss = fmaf(hi, hi, ss);
+      }
+      r[i] = make_uint4(rv[0], rv[1], rv[2], rv[3]);
+      *reinterpret_cast<uint4 *>(ro + base + k) = r[i];
+    } else {
+      r[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  ss = block_sum(ss, red);
+  const float inv = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), eps));
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int k = (i * nt + tid) * 8;
+    if (k < K) {
+      const uint4 wv4 = __ldg(reinterpret_cast<const uint4 *>(w + k));
+      const uint32_t wv[4] = {wv4.x, wv4.y, wv4.z, wv4.w};
+      uint32_t rv[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        rv[j] = pack2(__fmul_rn(__fmul_rn(bf16lo(rv[j]), inv), 1.f + bf16lo(wv[j])),
+                      __fmul_rn(__fmul_rn(bf16hi(rv[j]), inv), 1.f + bf16hi(wv[j])));
+      r[i] = make_uint4(rv[0], rv[1], rv[2], rv[3]);
+    }
+  }
+  quant_row<VPT>(r, K, q + base, s + row, red);
+}
+
+__device__ __forceinline__ float silu_f32(float g) { return __fdiv_rn(g, 1.f + expf(-g)); }
+
+template <int VPT>
+__global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const uint16_t *__restrict__ gu, int N,
+                                                                uint8_t *__restrict__ q, float *__restrict__ s) {
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  pdl_wait();   // gu comes from the preceding kernel
+  __shared__ float red[kThreads / 32];
+  const int row = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+  const uint16_t *gr = gu + static_cast<size_t>(row) * 2 * N;
+  uint4 h[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int k = (i * nt + tid) * 8;
+    if (k < N) {
+      const uint4 g4 = __ldg(reinterpret_cast<const uint4 *>(gr + k));
+      const uint4 u4 = __ldg(reinterpret_cast<const uint4 *>(gr + N + k));
+      const uint32_t gv[4] = {g4.x, g4.y, g4.z, g4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
+      uint32_t hv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t av = pack2(silu_f32(bf16lo(gv[j])), silu_f32(bf16hi(gv[j])));
+        // bf16 x bf16 is exact in fp32: one rounding, to bf16
+        hv[j] = pack2(bf16lo(av) * bf16lo(uv[j]), bf16hi(av) * bf16hi(uv[j]));
+      }
+      h[i] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    } else {
+      h[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  quant_row<VPT>(h, N, q + static_cast<size_t>(row) * N, s + row, red);
+}
+
+int threads_for(int64_t K) {
+  const int64_t vecs = K / 8;
+  int t = static_cast<int>(vecs < kThreads ? ((vecs + 31) / 32) * 32 : kThreads);
+  return t < 32 ? 32 : t;
+}
+
+}  // namespace
+
+cudaError_t launch_add_rmsnorm_quant(const uint16_t *y, const uint16_t *res, const uint16_t *w, float eps, int64_t M,
+                                     int64_t K, uint16_t *ro, uint8_t *q, float *s, cudaStream_t st) {
+  const int t = threads_for(K);
+  const int64_t per = ceil_div(K / 8, t);
+  const dim3 grid(static_cast<unsigned>(M));
+  const int k = static_cast<int>(K);
+#define R4_ARQ(V)                                                                                     \
+  {                                                                                                   \
+    const cudaError_t e = launch_pdl(add_rmsnorm_quant_kernel<V>, grid, dim3(t), 0, st, y, res, w, eps, k, ro, q, s); \
+    if (e != cudaSuccess) return e;                                                                   \
+    set_last_kernel("add_rmsnorm_quant_kernel<" #V ">");                                              \
+  }
+  if (per <= 1) R4_ARQ(1) else if (per <= 2) R4_ARQ(2) else if (per <= 4) R4_ARQ(4) else if (per <= 9) R4_ARQ(9)
+  else R4_ARQ(12)
+#undef R4_ARQ
+  return cudaGetLastError();
+}
+
+cudaError_t launch_silu_mul_quant(const uint16_t *gu, int64_t M, int64_t N, uint8_t *q, float *s, cudaStream_t st) {
+  const int t = threads_for(N);
+  const int64_t per = ceil_div(N / 8, t);
+  const dim3 grid(static_cast<unsigned>(M));
+  const int n = static_cast<int>(N);
+#define R4_SMQ(V)                                                                                     \
+  {                                                                                                   \
+    const cudaError_t e = launch_pdl(silu_mul_quant_kernel<V>, grid, dim3(t), 0, st, gu, n, q, s);   \
+    if (e != cudaSuccess) return e;                                                                   \
+    set_last_kernel("silu_mul_quant_kernel<" #V ">");                                                 \
+  }
+  if (per <= 1) R4_SMQ(1) else if (per <= 2) R4_SMQ(2) else if (per <= 4) R4_SMQ(4) else if (per <= 9) R4_SMQ(9)
+  else R4_SMQ(12)
+#undef R4_SMQ
+  return cudaGetLastError();
+}
+
+}  // namespace r4

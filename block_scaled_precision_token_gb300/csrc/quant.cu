@@ -13,51 +13,14 @@
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
+#include "quant_common.cuh"
 #include "r4_device.cuh"
 #include "r4_internal.h"
 
 namespace r4 {
 namespace {
 
-constexpr float kFp8Max = 448.0f;
-constexpr float kMinScale = 1.0f / 229376.0f;  // 1 / (448 * 512)
-
-__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-
-__device__ __forceinline__ float absmax8(const uint4 &v) {
-  const uint32_t m = 0x7FFF7FFFu;
-  float a = fmaxf(bf16lo(v.x & m), bf16hi(v.x & m));
-  a = fmaxf(a, fmaxf(bf16lo(v.y & m), bf16hi(v.y & m)));
-  a = fmaxf(a, fmaxf(bf16lo(v.z & m), bf16hi(v.z & m)));
-  a = fmaxf(a, fmaxf(bf16lo(v.w & m), bf16hi(v.w & m)));
-  return a;
-}
-
-__device__ __forceinline__ uint32_t e4m3_of(float v) {
-  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
-
-// 8 bf16 -> 8 e4m3 codes (element i in byte i), each x/s correctly rounded.
-__device__ __forceinline__ uint2 quant8(const uint4 &v, float sc) {
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t b[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    b[2 * i] = e4m3_of(__fdiv_rn(bf16lo(w[i]), sc));
-    b[2 * i + 1] = e4m3_of(__fdiv_rn(bf16hi(w[i]), sc));
-  }
-  uint2 r;
-  r.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-  r.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
-  return r;
-}
-
-__device__ __forceinline__ float warp_max(float a) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  return a;
-}
+using namespace qc;
 
 // One CTA per row; VPT 16-byte vectors per thread stay in registers.
 template <int VPT>

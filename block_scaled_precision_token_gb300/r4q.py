@@ -52,6 +52,8 @@ _SIGS = {
     "r4_gemm_blockfp8": ([_P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
     "r4_gemm_bf16_nt_skinny": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
     "r4_gemm_w4a8_mxfp4_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P, _I64, _P], _I),
+    "r4_add_rmsnorm_quant_fp8": ([_P, _P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P, _P], _I),
+    "r4_silu_mul_quant_fp8": ([_P, _I64, _I64, _P, _P, _P], _I),
 }
 
 
@@ -211,6 +213,20 @@ def r4_gemm_bf16_nt_skinny(x, w, M, N, K, c, ldc, workspace=None, stream=None):
            "r4_gemm_bf16_nt_skinny")
 
 
+def r4_add_rmsnorm_quant_fp8(y, residual, weight, eps, M, K, residual_out, q, s, stream=None):
+    _need(y, torch.bfloat16, "y"); _need(residual, torch.bfloat16, "residual")
+    _need(weight, torch.bfloat16, "weight"); _need(residual_out, torch.bfloat16, "residual_out")
+    _need(q, torch.uint8, "q"); _need(s, torch.float32, "s")
+    _check(lib().r4_add_rmsnorm_quant_fp8(_ptr(y), _ptr(residual), _ptr(weight), float(eps), M, K,
+                                          _ptr(residual_out), _ptr(q), _ptr(s), _stream(stream)),
+           "r4_add_rmsnorm_quant_fp8")
+
+
+def r4_silu_mul_quant_fp8(gu, M, N, q, s, stream=None):
+    _need(gu, torch.bfloat16, "gu"); _need(q, torch.uint8, "q"); _need(s, torch.float32, "s")
+    _check(lib().r4_silu_mul_quant_fp8(_ptr(gu), M, N, _ptr(q), _ptr(s), _stream(stream)), "r4_silu_mul_quant_fp8")
+
+
 # --------------------------------------------------------------------------- helpers
 
 def quant_fp8(x, group=None, stream=None):
@@ -221,6 +237,29 @@ def quant_fp8(x, group=None, stream=None):
     q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     s = torch.empty((M,) if group is None else (M, K // g), dtype=torch.float32, device=x.device)
     r4_quant_fp8_per_token(x, M, K, x.stride(0), g, q, s, stream)
+    return q, s
+
+
+def add_rmsnorm_quant(y, residual, weight, eps, residual_out=None, stream=None):
+    """y, residual bf16 [M, K], weight bf16 [K] -> (q uint8 [M, K], s fp32 [M], residual_out bf16 [M, K]).
+    Pass residual_out=residual for the in-place residual update."""
+    M, K = y.shape
+    assert y.is_contiguous() and residual.is_contiguous() and weight.is_contiguous()
+    ro = torch.empty_like(residual) if residual_out is None else residual_out
+    q = torch.empty((M, K), dtype=torch.uint8, device=y.device)
+    s = torch.empty((M,), dtype=torch.float32, device=y.device)
+    r4_add_rmsnorm_quant_fp8(y, residual, weight, eps, M, K, ro, q, s, stream)
+    return q, s, ro
+
+
+def silu_mul_quant(gu, stream=None):
+    """gu bf16 [M, 2N] = [gate | up] -> (q uint8 [M, N], s fp32 [M])."""
+    M, N2 = gu.shape
+    assert gu.is_contiguous() and N2 % 2 == 0
+    N = N2 // 2
+    q = torch.empty((M, N), dtype=torch.uint8, device=gu.device)
+    s = torch.empty((M,), dtype=torch.float32, device=gu.device)
+    r4_silu_mul_quant_fp8(gu, M, N, q, s, stream)
     return q, s
 
 

@@ -89,6 +89,37 @@ int r4_quant_fp8_per_token(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                            int64_t group, uint8_t *q, float *s, r4_stream_t stream);
 
 /*
+ * r4_add_rmsnorm_quant_fp8 -- residual add + Gemma RMS norm + per-token e4m3
+ * quantization in one launch: the single-rank epilogue of
+ * "radiance_arnq.py" (module docstring; ar_add_rms_quant):
+ *   r[m,k]  = bf16(y[m,k] + residual[m,k])                    (fp32 add)
+ *   h[m,k]  = bf16(r[m,k] / sqrt(mean_k(r^2) + eps) * (1 + w[k]))
+ *   (q, s)  = the r4_quant_fp8_per_token rule on h (one scale per row)
+ * The norm is formed in fp32 (correctly rounded division and reciprocal
+ * square root); r is written to residual_out, which may be the residual
+ * buffer itself (in-place update).
+ *   y, residual, residual_out  bf16 [M, K] row-major (row stride K), 16-byte aligned.
+ *   weight                     bf16 [K], 16-byte aligned.
+ *   q  e4m3 [M, K] (8-byte aligned);  s  fp32 [M].
+ * Requirements: M >= 1, K % 8 == 0, 8 <= K <= 24576, eps finite and >= 0.
+ */
+int r4_add_rmsnorm_quant_fp8(const uint16_t *y, const uint16_t *residual, const uint16_t *weight,
+                             float eps, int64_t M, int64_t K, uint16_t *residual_out,
+                             uint8_t *q, float *s, r4_stream_t stream);
+
+/*
+ * r4_silu_mul_quant_fp8 -- SiluAndMul + per-token e4m3 quantization in one
+ * launch ("radiance_arnq.py", silu_mul_quant and the _SiluMulQuant
+ * docstring). For each row of gu = [g | u] (N columns each):
+ *   a = bf16(g / (1 + exp(-g))),  h = bf16(a * u),  (q, s) = per-token rule on h.
+ *   gu  bf16 [M, 2N] row-major, 16-byte aligned;  q  e4m3 [M, N] (8-byte aligned);
+ *   s   fp32 [M].
+ * Requirements: M >= 1, N % 8 == 0, 8 <= N <= 24576.
+ */
+int r4_silu_mul_quant_fp8(const uint16_t *gu, int64_t M, int64_t N, uint8_t *q, float *s,
+                          r4_stream_t stream);
+
+/*
  * r4_quantize_mxfp4_weight -- OCP MX FP4 quantization of a float32 weight
  * (a load-time utility, not on the per-token path): per 32-element block of a
  * row, X = floor(log2(amax)) - 2 (all-zero block: X = 0), scale code X + 127
