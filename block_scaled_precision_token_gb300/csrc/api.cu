@@ -101,23 +101,6 @@ CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank
 
 using namespace r4;
 
-namespace r4 {
-int gemm_w4a8_planned(const uint8_t *q, const float *s, const void *packed, int64_t M, int64_t N, int64_t K,
-                      uint16_t *c, int64_t ldc, void *workspace, size_t workspace_bytes, const GemmPlan &pl,
-                      r4_stream_t stream) {
-  if (!q || !s || !packed || !c) return R4_ERR_INVALID_ARG;
-  if (M < 1 || N < 1 || K < 1 || ldc < N || M > (1 << 30) || N > (1 << 30)) return R4_ERR_INVALID_ARG;
-  if (K % 32 || K < 128) return R4_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(q, 16) || !aligned(packed, 256) || !aligned(s, 4) || !aligned(c, 2)) return R4_ERR_MISALIGNED;
-  if (pl.ws_bytes > 0) {
-    if (!workspace || workspace_bytes < pl.ws_bytes) return R4_ERR_WORKSPACE;
-    if (!aligned(workspace, 256)) return R4_ERR_MISALIGNED;
-  }
-  if (device_error_word() == nullptr) return R4_ERR_CUDA;
-  return launch_gemm_w4a8(q, s, static_cast<const uint8_t *>(packed), M, N, K, c, ldc,
-                          pl.ws_bytes ? workspace : nullptr, pl, reinterpret_cast<cudaStream_t>(stream));
-}
-}  // namespace r4
 
 extern "C" {
 
@@ -162,10 +145,6 @@ int r4_set_option(int key, int64_t value) {
     case 4: options().pdl = value ? 1 : 0; return R4_OK;
     case 5: options().l2_prefetch = value ? 1 : 0; return R4_OK;
     case 6: options().cluster_split = value ? 1 : 0; return R4_OK;
-    case 8:
-      if (value < 0 || value > 2) return R4_ERR_INVALID_ARG;
-      options().streamk = static_cast<int>(value);
-      return R4_OK;
     case 7:
       if (value != 0 && value != 16 && value != 32 && value != 64 && value != 128) return R4_ERR_INVALID_ARG;
       options().fp8_token_tile = static_cast<int>(value);
@@ -277,12 +256,19 @@ size_t r4_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
 
 int r4_gemm_w4a8_mxfp4(const uint8_t *q, const float *s, const void *packed, int64_t M, int64_t N, int64_t K,
                        uint16_t *c, int64_t ldc, void *workspace, size_t workspace_bytes, r4_stream_t stream) {
-  if (M < 1 || N < 1 || K < 1 || M > (1 << 30) || N > (1 << 30)) return R4_ERR_INVALID_ARG;
+  if (!q || !s || !packed || !c) return R4_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldc < N || M > (1 << 30) || N > (1 << 30)) return R4_ERR_INVALID_ARG;
   if (K % 32 || K < 128) return R4_ERR_UNSUPPORTED_SHAPE;
-  return r4::gemm_w4a8_planned(q, s, packed, M, N, K, c, ldc, workspace, workspace_bytes,
-                               r4::plan_w4a8(M, N, K, r4::device_sm_count()), stream);
+  if (!aligned(q, 16) || !aligned(packed, 256) || !aligned(s, 4) || !aligned(c, 2)) return R4_ERR_MISALIGNED;
+  const GemmPlan pl = plan_w4a8(M, N, K, device_sm_count());
+  if (pl.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < pl.ws_bytes) return R4_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return R4_ERR_MISALIGNED;
+  }
+  if (device_error_word() == nullptr) return R4_ERR_CUDA;
+  return launch_gemm_w4a8(q, s, static_cast<const uint8_t *>(packed), M, N, K, c, ldc,
+                          pl.ws_bytes ? workspace : nullptr, pl, reinterpret_cast<cudaStream_t>(stream));
 }
-
 
 int r4_gemm_blockfp8(const uint8_t *q, const float *As, const void *packed, int64_t M, int64_t N, int64_t K,
                      uint16_t *c, int64_t ldc, void *workspace, size_t workspace_bytes, r4_stream_t stream) {

@@ -28,16 +28,22 @@ namespace skinny {
 
 constexpr int kThreads = 128;
 constexpr int kRows = 16;
-constexpr int kIter = 512;              // K staged per iteration
+constexpr int kIter = 256;              // K staged per iteration
 constexpr int kStride = kIter + 8;      // padded row, in bf16 elements
-constexpr int kMaxM = 64;
 constexpr int kMaxKS = 8;
 
-constexpr size_t kSmemW = kRows * kStride * 2;
-constexpr size_t kSmemX = kMaxM * kStride * 2;
-constexpr size_t kSmemRed = 4 * kRows * kMaxM * 4;
-constexpr size_t kSmemCluster = kMaxKS * kRows * kMaxM * 4;
-constexpr size_t kSmemBytes = kSmemW + kSmemX + kSmemRed + kSmemCluster;
+// Shared memory sized for the token groups actually present: at 1 CTA per
+// SM a cluster of 8 fits only 15 times on GB300 (measured: the 16th of a
+// 256-row weight's clusters ran as a second wave); small CTAs pack 2-7 per SM.
+template <int NG2>
+struct Smem {
+  static constexpr int kMpad = 16 * NG2;
+  static constexpr size_t kW = kRows * kStride * 2;
+  static constexpr size_t kX = kMpad * kStride * 2;
+  static constexpr size_t kRed = 4 * kRows * kMpad * 4;
+  static constexpr size_t kCluster = kMaxKS * kRows * kMpad * 4;
+  static constexpr size_t kBytes = kW + kX + kRed + kCluster;
+};
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -78,12 +84,13 @@ template <int NG2>  // token groups of 16 (Mpad = 16 * NG2)
 __global__ void __launch_bounds__(kThreads, 1)
     skinny_bf16_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w, int M, int N, int K,
                        int chunks_per_cta, uint16_t *__restrict__ c, int ldc) {
-  constexpr int kMpad = 16 * NG2;
+  using S = Smem<NG2>;
+  constexpr int kMpad = S::kMpad;
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t *sW = reinterpret_cast<uint16_t *>(smem);
-  uint16_t *sX = reinterpret_cast<uint16_t *>(smem + kSmemW);
-  float *sRed = reinterpret_cast<float *>(smem + kSmemW + kSmemX);             // [4][16][kMaxM]
-  float *sCl = reinterpret_cast<float *>(smem + kSmemW + kSmemX + kSmemRed);   // [KS][16][kMaxM]
+  uint16_t *sX = reinterpret_cast<uint16_t *>(smem + S::kW);
+  float *sRed = reinterpret_cast<float *>(smem + S::kW + S::kX);              // [4][16][kMpad]
+  float *sCl = reinterpret_cast<float *>(smem + S::kW + S::kX + S::kRed);     // [KS][16][kMpad]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
@@ -141,31 +148,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // warp partials -> shared memory (D fragment: rows lane/4 and lane/4 + 8,
   // token columns 8g + 2(lane%4) + {0,1})
-  float *red = sRed + warp * kRows * kMaxM;
+  float *red = sRed + warp * kRows * kMpad;
 #pragma unroll
   for (int g = 0; g < 2 * NG2; ++g) {
     const int r = lane >> 2, t = 8 * g + 2 * (lane & 3);
-    red[r * kMaxM + t] = acc[g][0];
-    red[r * kMaxM + t + 1] = acc[g][1];
-    red[(r + 8) * kMaxM + t] = acc[g][2];
-    red[(r + 8) * kMaxM + t + 1] = acc[g][3];
+    red[r * kMpad + t] = acc[g][0];
+    red[r * kMpad + t + 1] = acc[g][1];
+    red[(r + 8) * kMpad + t] = acc[g][2];
+    red[(r + 8) * kMpad + t + 1] = acc[g][3];
   }
   __syncthreads();
 
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  const uint32_t dst_base = map_rank(smem_addr(sCl + rank * kRows * kMaxM), 0);
+  const uint32_t dst_base = map_rank(smem_addr(sCl + rank * kRows * kMpad), 0);
   for (int i = tid; i < kRows * kMpad; i += kThreads) {
     const int r = i % kRows, t = i / kRows;
-    const float v = sRed[r * kMaxM + t] + sRed[kRows * kMaxM + r * kMaxM + t] +
-                    sRed[2 * kRows * kMaxM + r * kMaxM + t] + sRed[3 * kRows * kMaxM + r * kMaxM + t];
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst_base + 4u * (r * kMaxM + t)), "f"(v) : "memory");
+    const float v = sRed[r * kMpad + t] + sRed[kRows * kMpad + r * kMpad + t] +
+                    sRed[2 * kRows * kMpad + r * kMpad + t] + sRed[3 * kRows * kMpad + r * kMpad + t];
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst_base + 4u * (r * kMpad + t)), "f"(v) : "memory");
   }
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
   if (rank == 0) {
     for (int i = tid; i < kRows * kMpad; i += kThreads) {
       const int r = i % kRows, t = i / kRows;
       float v = 0.f;
-      for (int s = 0; s < KS; ++s) v += sCl[s * kRows * kMaxM + r * kMaxM + t];
+      for (int s = 0; s < KS; ++s) v += sCl[s * kRows * kMpad + r * kMpad + t];
       if (t < M && n0 + r < N) {
         __nv_bfloat16 h = __float2bfloat16_rn(v);
         c[static_cast<size_t>(t) * ldc + n0 + r] = *reinterpret_cast<uint16_t *>(&h);
@@ -181,6 +188,7 @@ cudaError_t launch_ng(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N
   const int ks = chunks < kMaxKS ? chunks : kMaxKS;
   const int cpc = (chunks + ks - 1) / ks;
   auto kern = skinny_bf16_kernel<NG2>;
+  constexpr size_t kSmemBytes = Smem<NG2>::kBytes;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

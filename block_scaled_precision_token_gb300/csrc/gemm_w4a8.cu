@@ -82,8 +82,6 @@ struct Params {
   int tma_store;         // 1: bf16 output tiles leave through smem + TMA tensor stores
   int l2_prefetch;       // 1: producer 0 prefetches the CTA's whole weight range into L2 at start
   int cluster;           // 1: the `splits` CTAs of a cluster split K and exchange partials in DSMEM
-  int streamk;           // 1: every CTA takes an equal share of all tiles' K blocks (stream-K, forced only)
-  int work;              // tiles * KB (stream-K)
   const uint8_t *w;      // packed weight codes [NT][KB][128][64]
   const float *s;
   const uint8_t *sf;     // scale atoms of the prepacked weight
@@ -122,96 +120,24 @@ struct Cfg {
   static_assert(kStages >= kIss && kStages % kIss == 0, "stage count");
 };
 
-// One piece of a CTA's work: output tile (nt, tt) and its K blocks
-// [kb0, kb1). slot < 0: the piece is the whole tile (stored directly);
-// otherwise its fp32 partial goes to workspace slot `slot`, and the last of
-// the tile's `contrib` pieces to arrive sums them.
-struct Piece {
-  int nt, tt, kb0, kb1;
-  int slot, contrib;
-  int c_first;           // stream-K: first contributing CTA of the tile
-};
-
-// Stream-K: CTA c owns global K blocks [bnd(c), bnd(c + 1)) of the
-// sequence tile-major, K block minor.
-__device__ __forceinline__ int sk_bnd(const Params &p, int c) {
-  return static_cast<int>(static_cast<int64_t>(c) * p.work / gridDim.x);
-}
-// The CTA owning global K block x: the largest c with sk_bnd(c) <= x.
-__device__ __forceinline__ int sk_owner(const Params &p, int x) {
-  return static_cast<int>((static_cast<int64_t>(x + 1) * gridDim.x - 1) / p.work);
+__device__ __forceinline__ void decode_unit(const Params &p, int u, int &nt, int &tt, int &sp, int &kb0, int &kb1) {
+  const int tile = u / p.splits;
+  sp = u - tile * p.splits;
+  nt = tile / p.t_tiles;
+  tt = tile - nt * p.t_tiles;
+  kb0 = sp * p.kb_per_split;
+  kb1 = min(p.KB, kb0 + p.kb_per_split);
 }
 
-// The i-th piece of this CTA's work, in processing order; false past the end.
-__device__ __forceinline__ bool get_piece(const Params &p, int i, Piece &pc) {
-  int tile;
-  if (p.streamk) {
-    const int a = sk_bnd(p, blockIdx.x), b = sk_bnd(p, blockIdx.x + 1);
-    tile = a / p.KB + i;
-    if (a >= b || tile > (b - 1) / p.KB) return false;
-    const int t0 = tile * p.KB;
-    pc.kb0 = max(a, t0) - t0;
-    pc.kb1 = min(b, t0 + p.KB) - t0;
-    pc.c_first = sk_owner(p, t0);
-    pc.contrib = sk_owner(p, t0 + p.KB - 1) - pc.c_first + 1;
-    pc.slot = pc.contrib > 1 ? 2 * static_cast<int>(blockIdx.x) + (i == 0 ? 0 : 1) : -1;
-  } else {
-    const int u = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-    if (u >= p.units) return false;
-    tile = u / p.splits;
-    const int sp = u - tile * p.splits;
-    pc.kb0 = sp * p.kb_per_split;
-    pc.kb1 = min(p.KB, pc.kb0 + p.kb_per_split);
-    pc.contrib = p.splits;
-    pc.c_first = 0;
-    pc.slot = p.splits > 1 ? u : -1;   // slots of one tile are contiguous
-  }
-  pc.nt = tile / p.t_tiles;
-  pc.tt = tile - pc.nt * p.t_tiles;
-  return true;
-}
-
-// Bulk L2 prefetch of a piece's weight codes and scale atoms (both contiguous).
-__device__ __forceinline__ void prefetch_piece_l2(const Params &p, const Piece &pc) {
-  const size_t blk = static_cast<size_t>(pc.nt) * p.KB + pc.kb0;
-  const uint32_t nkb = static_cast<uint32_t>(pc.kb1 - pc.kb0);
+// Bulk L2 prefetch of unit u's weight codes and scale atoms (both contiguous).
+__device__ __forceinline__ void prefetch_unit_l2(const Params &p, int u) {
+  if (u >= p.units) return;
+  int nt, tt, sp, kb0, kb1;
+  decode_unit(p, u, nt, tt, sp, kb0, kb1);
+  const size_t blk = static_cast<size_t>(nt) * p.KB + kb0;
+  const uint32_t nkb = static_cast<uint32_t>(kb1 - kb0);
   bulk_prefetch_l2(p.w + blk * 8192, nkb * 8192u);
   bulk_prefetch_l2(p.sf + blk * kSfBytes, nkb * kSfBytes);
-}
-
-// Last-arriving CTA of a split tile: sum its pieces' fp32 partials in K
-// order (deterministic) and store bf16(s[t] * sum) for t < M, n < N. Loads
-// are independent L2 reads (.cg: other SMs wrote them), four n per thread.
-template <int BT>
-__device__ __forceinline__ void reduce_pieces_store(const Params &p, const Piece &pc, int tid, int nthreads) {
-  constexpr size_t kTile = 128 * BT;
-  const int tile = pc.nt * p.t_tiles + pc.tt;
-  const int t0 = pc.tt * BT, tmax = min(BT, p.M - t0), n0 = pc.nt * 128;
-  for (int idx = tid; idx < tmax * 32; idx += nthreads) {
-    const int tl = idx >> 5, n4 = (idx & 31) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < pc.contrib; ++j) {
-      int slot;
-      if (p.streamk) {
-        const int c = pc.c_first + j;
-        slot = 2 * c + ((sk_bnd(p, c) / p.KB == tile) ? 0 : 1);
-      } else {
-        slot = tile * p.splits + j;
-      }
-      const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.partials + slot * kTile + tl * 128 + n4));
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    const float sc = __ldg(p.s + t0 + tl);
-    const int n = n0 + n4;
-    uint16_t *dst = p.c + static_cast<size_t>(t0 + tl) * p.ldc + n;
-    const float vals[4] = {acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc};
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (n + e < p.N) dst[e] = f32_to_bf16_rn(vals[e]);
-  }
 }
 
 template <int BT>
@@ -292,15 +218,13 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       // Optionally ask L2 for this CTA's whole weight range up front: the
       // stream then runs at HBM rate while this kernel waits for its
       // predecessor, not only for the ring's depth.
-      if (p.l2_prefetch && pw == 0) {
-        Piece pc;
-        for (int pi = 0; get_piece(p, pi, pc); ++pi) prefetch_piece_l2(p, pc);
-      }
+      if (p.l2_prefetch && pw == 0)
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) prefetch_unit_l2(p, u);
       {
         int g = 0;
-        Piece pc;
-        for (int pi = 0; g < C::kStages && get_piece(p, pi, pc); ++pi) {
-          const int nt = pc.nt, kb0 = pc.kb0, kb1 = pc.kb1;
+        for (int u = blockIdx.x; u < p.units && g < C::kStages; u += gridDim.x) {
+          int nt, tt, sp, kb0, kb1;
+          decode_unit(p, u, nt, tt, sp, kb0, kb1);
           const int nkb = kb1 - kb0;
           const int nslots = (nkb + ISS - 1) / ISS * ISS;
           for (int i = pw; i < nslots && g + i < C::kStages; i += ISS) {
@@ -323,9 +247,9 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       int stage = pw;
       uint32_t phase = 0;
       int gbase = 0;
-      Piece pc;
-      for (int pi = 0; ok && get_piece(p, pi, pc); ++pi) {
-        const int nt = pc.nt, tt = pc.tt, kb0 = pc.kb0, kb1 = pc.kb1;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        int nt, tt, sp, kb0, kb1;
+        decode_unit(p, u, nt, tt, sp, kb0, kb1);
         const int nkb = kb1 - kb0;
         const int nslots = (nkb + ISS - 1) / ISS * ISS;
         for (int i = pw; i < nslots; i += ISS) {
@@ -381,9 +305,9 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      Piece pc;
-      for (int pi = 0; ok && get_piece(p, pi, pc); ++pi) {
-        const int kb0 = pc.kb0, kb1 = pc.kb1;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        int nt, tt, sp, kb0, kb1;
+        decode_unit(p, u, nt, tt, sp, kb0, kb1);
         const int nkb = kb1 - kb0;
         const int nslots = (nkb + ISS - 1) / ISS * ISS;
         if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_ACC_EMPTY)) break;
@@ -449,9 +373,9 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
     uint32_t out_chunk = 0;   // running count of staged output chunks (selects the buffer)
     uint32_t xchg = 0;        // running count of cluster split-K exchanges
     bool stop = false;
-    Piece pc;
-    for (int pi = 0; get_piece(p, pi, pc); ++pi) {
-      const int nt = pc.nt, tt = pc.tt, kb0 = pc.kb0, kb1 = pc.kb1;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      int nt, tt, sp, kb0, kb1;
+      decode_unit(p, u, nt, tt, sp, kb0, kb1);
       const int ncontrib = min(ISS, kb1 - kb0);   // MMA warps that accumulated something
       // The decision to stop must be the same in all 128 epilogue threads
       // (they meet at named barriers below): a failed wait is published
@@ -464,7 +388,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       const int t0 = tt * BT;
       const int tile = nt * p.t_tiles + tt;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      float *part = (pc.slot >= 0 && !p.cluster) ? p.partials + static_cast<size_t>(pc.slot) * (128 * BT) : nullptr;
+      float *part = (p.splits > 1 && !p.cluster) ? p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (128 * BT) : nullptr;
 #pragma unroll 1
       for (int c0 = 0; c0 < BT; c0 += CH) {
         uint32_t r[32];
@@ -486,7 +410,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce_bar[acc]);
         }
-        if (pc.slot < 0 && p.tma_store) {
+        if (p.splits == 1 && p.tma_store) {
           // Stage [CH tokens][128 n] bf16 in smem, then one TMA tensor store;
           // the store clips rows >= M and columns >= N.
           uint16_t *stg = staging + (out_chunk & 1u) * (CH * 128);
@@ -505,7 +429,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
             bulk_commit();
           }
           ++out_chunk;
-        } else if (pc.slot < 0) {
+        } else if (p.splits == 1) {
           if (n < p.N) {
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
@@ -575,17 +499,19 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
         }
       }
       if (stop) break;
-      if (pc.slot >= 0 && !p.cluster) {
+      if (p.splits > 1 && !p.cluster) {
         __threadfence();
         named_bar_sync(1, 128);
         if (ew == 0 && lane == 0) {
           const int prev = atomicAdd(p.counters + tile, 1);
-          *is_last = (prev == pc.contrib - 1) ? 1 : 0;
+          *is_last = (prev == p.splits - 1) ? 1 : 0;
         }
         named_bar_sync(1, 128);
         if (*is_last) {
           __threadfence();
-          reduce_pieces_store<BT>(p, pc, ew * 32 + lane, 128);
+          const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (128 * BT);
+          reduce_partials_store<BT>(base, p.splits, min(BT, p.M - t0), nt * 128, p.N, p.s, t0, p.c, p.ldc,
+                                    ew * 32 + lane, 128);
           if (ew == 0 && lane == 0) p.counters[tile] = 0;
         }
         named_bar_sync(1, 128);
@@ -655,8 +581,6 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
   p.tma_store = use_tma_store;
   p.l2_prefetch = options().l2_prefetch;
   p.cluster = pl.cluster;
-  p.streamk = pl.streamk;
-  p.work = pl.n_tiles * pl.t_tiles * pl.KB;
   p.w = packed;
   p.s = s;
   p.sf = packed + mx_packed_codes_bytes(N, K);
@@ -732,7 +656,7 @@ int max_clusters(int bt, int s) {
 // prefill shapes. Prefill tiles (BT >= 128) are never split once the tile
 // count is a quarter of the SM count: there the partial tiles cost more than
 // the idle SMs.
-GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms, bool allow_streamk) {
+GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
   GemmPlan pl;
   int bt = options().w4a8_token_tile;
   if (bt == 0) bt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
@@ -800,26 +724,6 @@ GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms, bool allow_streamk)
       best_s = s;
       best_cl = ncl > 0;
       best_grid = grid;
-    }
-  }
-  // Stream-K (only when forced, option 8): every CTA takes an equal share of
-  // all tiles' K blocks; a tile cut between CTAs is summed by the last of
-  // them from the workspace (each CTA writes at most two partial tiles).
-  // Measured on GB300 it never wins here: the partial-tile round trip through
-  // L2 costs more than the balance gains (decode M=6, 34816x5120: 24.0 vs
-  // 19.9 us; M=6, 2048x5120: 18.9 vs 8.8 us; prefill M=256: 2-6x slower).
-  const int64_t work = tiles * pl.KB;
-  if (allow_streamk && options().streamk == 1 && work >= sms && work < (int64_t(1) << 31) / sms) {
-    const int64_t G = sms;
-    {
-      pl.streamk = 1;
-      pl.splits = 1;
-      pl.kb_per_split = pl.KB;
-      pl.units = static_cast<int>(tiles);
-      pl.grid = static_cast<int>(G);
-      pl.counters_bytes = round_up(static_cast<size_t>(tiles) * 4, 256);
-      pl.ws_bytes = pl.counters_bytes + static_cast<size_t>(2 * G) * 128 * bt * 4;
-      return pl;
     }
   }
   pl.splits = best_s;

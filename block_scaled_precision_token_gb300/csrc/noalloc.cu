@@ -57,10 +57,7 @@ extern "C" int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, cons
   if (!q || !s || !packed || !c) return R4_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1 || ldc < N || M > (1 << 30) || N > (1 << 30)) return R4_ERR_INVALID_ARG;
   if (K % 32 || K < 128) return R4_ERR_UNSUPPORTED_SHAPE;
-  GemmPlan pl = plan_w4a8(M, N, K, device_sm_count());
-  // A stream-K plan whose partials outgrow the scratch gives way to the
-  // best plan without it; beyond that the call is rejected.
-  if (pl.ws_bytes > kNoallocScratchBytes && pl.streamk) pl = plan_w4a8(M, N, K, device_sm_count(), false);
+  const GemmPlan pl = plan_w4a8(M, N, K, device_sm_count());
   if (pl.ws_bytes > kNoallocScratchBytes) return R4_ERR_WORKSPACE;   // beyond the static maximum
   void *ws = nullptr;
   if (pl.ws_bytes > 0) {
@@ -69,5 +66,5 @@ extern "C" int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, cons
     if (cudaMemsetAsync(ws, 0, pl.counters_bytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
       return R4_ERR_CUDA;
   }
-  return gemm_w4a8_planned(q, s, packed, M, N, K, c, ldc, ws, pl.ws_bytes, pl, stream);
+  return r4_gemm_w4a8_mxfp4(q, s, packed, M, N, K, c, ldc, ws, pl.ws_bytes, stream);
 }

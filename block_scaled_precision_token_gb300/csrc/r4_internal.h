@@ -34,7 +34,6 @@ struct Options {
   int pdl = 1;              // launch with programmatic stream serialization
   int l2_prefetch = 0;      // W4A8: bulk L2 prefetch of the CTA's whole weight range at kernel start
   int cluster_split = 1;    // W4A8 decode tiles: split-K across a thread-block cluster when possible
-  int streamk = 0;          // W4A8: 1 = stream-K schedule (measured slower; for experiments), else never
 };
 Options &options();
 
@@ -87,16 +86,11 @@ struct GemmPlan {
   int splits = 1, kb_per_split = 0;
   int units = 0, grid = 0;
   int cluster = 0;       // 1: split-K across a cluster of `splits` CTAs (partials in DSMEM, no workspace)
-  int streamk = 0;       // 1: stream-K (every CTA an equal share of all K blocks; workspace partials)
   size_t counters_bytes = 0;  // arrival counters (one int per tile), 256-B rounded
   size_t ws_bytes = 0;        // total workspace (0 when splits == 1)
 };
 
-GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms, bool allow_streamk = true);
-// r4_gemm_w4a8_mxfp4 with a given plan (argument checks included).
-int gemm_w4a8_planned(const uint8_t *q, const float *s, const void *packed, int64_t M, int64_t N, int64_t K,
-                      uint16_t *c, int64_t ldc, void *workspace, size_t workspace_bytes, const GemmPlan &pl,
-                      r4_stream_t stream);
+GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms);
 GemmPlan plan_blockfp8(int64_t M, int64_t N, int64_t K, int sms);
 
 // ------------------------------------------------------------------ prepack layout

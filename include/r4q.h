@@ -263,10 +263,7 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * key 6: W4A8 decode split-K across a thread-block cluster with the partial
  * sums exchanged in distributed shared memory (1, default) or through the
  * caller's workspace (0); key 7: force the block-FP8 token tile (0 =
- * automatic, else 16/32/64/128); key 8: W4A8 stream-K schedule (every CTA
- * takes an equal share of all tiles' K blocks, split tiles summed through
- * the workspace): 1 = on; 0 or 2 = off (default; measured slower on GB300
- * for every workload shape).
+ * automatic, else 16/32/64/128).
  */
 int r4_set_option(int key, int64_t value);
 

@@ -87,3 +87,29 @@ def test_blockfp8_weight_quant_bit_exact(r4q, N, K):
     check_device_error(r4q)
     assert np.array_equal(np_f32(s), s_ref)
     assert np.array_equal(np_u8(c), c_ref)
+
+
+def test_every_bf16_value_under_several_scales(r4q):
+    """Each row holds every finite bfloat16 value up to its own amax, so the
+    quotients x/s cover exact e4m3 ties (power-of-two scales) and land within
+    a few float32 ulps of every e4m3 rounding boundary (other scales): the
+    codes must still be those of the correctly rounded quotient."""
+    bits = np.arange(65536, dtype=np.uint32)
+    allv = (bits << 16).view(np.float32)
+    allv = allv[np.isfinite(allv)]
+    amaxes = [448.0, 1344.0, 0.01171875, 3.0517578e-05, 1.0078125, 57344.0, 1.0e-8]
+    K = 65536
+    rows = []
+    for a in amaxes:
+        a = float(torch.tensor(a).to(torch.bfloat16))
+        v = allv[np.abs(allv) <= a]
+        row = np.zeros(K, np.float32)
+        row[:v.size] = v
+        row[v.size] = a
+        rows.append(row)
+    x = torch.from_numpy(np.stack(rows)).to(torch.bfloat16)
+    q_ref, s_ref = Q.quant_act(x.float().numpy())
+    q, s = r4q.quant_fp8(x.cuda())
+    check_device_error(r4q)
+    assert np.array_equal(np_f32(s), s_ref)
+    assert np.array_equal(np_u8(q), q_ref)
