@@ -12,7 +12,7 @@
 // vectors, read once), reduces it twice (sum of squares, then amax) and
 // writes the codes -- one launch where the unfused chain takes two or three.
 // The norm is fp32 with correctly rounded division and reciprocal square
-// root; SiLU uses CUDA's expf; the codes are those of correctly rounded
+// root; SiLU uses CUDA's expf; the codes come from correctly rounded
 // quotients (quant_common.cuh).
 
 #include <cuda_bf16.h>
@@ -70,7 +70,7 @@ __device__ __forceinline__ void quant_row(const uint4 (&h)[VPT], int K, uint8_t 
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int k = (i * nt + tid) * 8;
-    if (k < K) *reinterpret_cast<uint2 *>(qr + k) = quant8(h[i], sc, __frcp_rn(sc));
+    if (k < K) *reinterpret_cast<uint2 *>(qr + k) = quant8(h[i], sc);
   }
 }
 
@@ -128,9 +128,9 @@ __global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_kernel(const uint1
   quant_row<VPT>(r, K, q + base, s + row, red);
 }
 
-// g * sigmoid(g) to a few float32 ulps (CUDA's expf, a correctly rounded
-// reciprocal); exp(-g) = inf gives -0 as the exact value does.
-__device__ __forceinline__ float silu_f32(float g) { return g * __frcp_rn(1.f + expf(-g)); }
+// g * sigmoid(g) to a few float32 ulps (CUDA's expf); exp(-g) = inf gives
+// -0 as the exact value does.
+__device__ __forceinline__ float silu_f32(float g) { return __fdiv_rn(g, 1.f + expf(-g)); }
 
 template <int VPT>
 __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const uint16_t *__restrict__ gu, int N,

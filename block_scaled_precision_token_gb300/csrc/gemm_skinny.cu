@@ -40,8 +40,11 @@ struct Smem {
   static constexpr int kMpad = 16 * NG2;
   static constexpr size_t kW = kRows * kStride * 2;
   static constexpr size_t kX = kMpad * kStride * 2;
-  static constexpr size_t kRed = 4 * kRows * kMpad * 4;
-  static constexpr size_t kCluster = kMaxKS * kRows * kMpad * 4;
+  // partial tiles [16 rows][kMpad tokens], rows kMpad + 1 floats apart: the
+  // reductions walk rows fastest, and an odd stride keeps them conflict-free
+  static constexpr int kRS = kMpad + 1;
+  static constexpr size_t kRed = 4 * kRows * kRS * 4;
+  static constexpr size_t kCluster = kMaxKS * kRows * kRS * 4;
   static constexpr size_t kBytes = kW + kX + kRed + kCluster;
 };
 
@@ -86,11 +89,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                        int chunks_per_cta, uint16_t *__restrict__ c, int ldc) {
   using S = Smem<NG2>;
   constexpr int kMpad = S::kMpad;
+  constexpr int kRS = S::kRS;
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t *sW = reinterpret_cast<uint16_t *>(smem);
   uint16_t *sX = reinterpret_cast<uint16_t *>(smem + S::kW);
-  float *sRed = reinterpret_cast<float *>(smem + S::kW + S::kX);              // [4][16][kMpad]
-  float *sCl = reinterpret_cast<float *>(smem + S::kW + S::kX + S::kRed);     // [KS][16][kMpad]
+  float *sRed = reinterpret_cast<float *>(smem + S::kW + S::kX);              // [4][16][kRS]
+  float *sCl = reinterpret_cast<float *>(smem + S::kW + S::kX + S::kRed);     // [KS][16][kRS]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
@@ -148,31 +152,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // warp partials -> shared memory (D fragment: rows lane/4 and lane/4 + 8,
   // token columns 8g + 2(lane%4) + {0,1})
-  float *red = sRed + warp * kRows * kMpad;
+  float *red = sRed + warp * kRows * kRS;
 #pragma unroll
   for (int g = 0; g < 2 * NG2; ++g) {
     const int r = lane >> 2, t = 8 * g + 2 * (lane & 3);
-    red[r * kMpad + t] = acc[g][0];
-    red[r * kMpad + t + 1] = acc[g][1];
-    red[(r + 8) * kMpad + t] = acc[g][2];
-    red[(r + 8) * kMpad + t + 1] = acc[g][3];
+    red[r * kRS + t] = acc[g][0];
+    red[r * kRS + t + 1] = acc[g][1];
+    red[(r + 8) * kRS + t] = acc[g][2];
+    red[(r + 8) * kRS + t + 1] = acc[g][3];
   }
   __syncthreads();
 
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  const uint32_t dst_base = map_rank(smem_addr(sCl + rank * kRows * kMpad), 0);
+  const uint32_t dst_base = map_rank(smem_addr(sCl + rank * kRows * kRS), 0);
   for (int i = tid; i < kRows * kMpad; i += kThreads) {
     const int r = i % kRows, t = i / kRows;
-    const float v = sRed[r * kMpad + t] + sRed[kRows * kMpad + r * kMpad + t] +
-                    sRed[2 * kRows * kMpad + r * kMpad + t] + sRed[3 * kRows * kMpad + r * kMpad + t];
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst_base + 4u * (r * kMpad + t)), "f"(v) : "memory");
+    const float v = sRed[r * kRS + t] + sRed[kRows * kRS + r * kRS + t] + sRed[2 * kRows * kRS + r * kRS + t] +
+                    sRed[3 * kRows * kRS + r * kRS + t];
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst_base + 4u * (r * kRS + t)), "f"(v) : "memory");
   }
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
   if (rank == 0) {
     for (int i = tid; i < kRows * kMpad; i += kThreads) {
       const int r = i % kRows, t = i / kRows;
       float v = 0.f;
-      for (int s = 0; s < KS; ++s) v += sCl[s * kRows * kMpad + r * kMpad + t];
+      for (int s = 0; s < KS; ++s) v += sCl[s * kRows * kRS + r * kRS + t];
       if (t < M && n0 + r < N) {
         __nv_bfloat16 h = __float2bfloat16_rn(v);
         c[static_cast<size_t>(t) * ldc + n0 + r] = *reinterpret_cast<uint16_t *>(&h);

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int k = (i * nt + tid) * 8;
-      if (k < K) *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc, __frcp_rn(sc));
+      if (k < K) *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc);
     }
   } else {
     // group of 128 = 16 lanes x 8 elements; nt is a multiple of 32
@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
       const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
       if (k < K) {
         if ((tid & 15) == 0) s[static_cast<size_t>(row) * groups + (k >> 7)] = sc;
-        *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc, __frcp_rn(sc));
+        *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc);
       }
     }
   }
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(256) quant_act_long_kernel(const uint16_t *__r
     const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
     if (tid == 0) s[row] = sc;
     for (int k = tid * 8; k < K; k += nt * 8)
-      *reinterpret_cast<uint2 *>(qr + k) = quant8(__ldg(reinterpret_cast<const uint4 *>(xr + k)), sc, __frcp_rn(sc));
+      *reinterpret_cast<uint2 *>(qr + k) = quant8(__ldg(reinterpret_cast<const uint4 *>(xr + k)), sc);
   } else {
     const int groups = K / 128;
     for (int base = 0; base < K; base += nt * 8) {
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(256) quant_act_long_kernel(const uint16_t *__r
       const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
       if (k < K) {
         if ((tid & 15) == 0) s[static_cast<size_t>(row) * groups + (k >> 7)] = sc;
-        *reinterpret_cast<uint2 *>(qr + k) = quant8(v, sc, __frcp_rn(sc));
+        *reinterpret_cast<uint2 *>(qr + k) = quant8(v, sc);
       }
     }
   }

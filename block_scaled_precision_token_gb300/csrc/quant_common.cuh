@@ -34,29 +34,14 @@ __device__ __forceinline__ uint32_t e4m3_of(float v) {
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
 
-// e4m3 code of the correctly rounded quotient x / s, given rs = RN(1/s).
-// y = RN(x * rs) is within 2.5 float32 ulps of RN(x / s) (two roundings of
-// 2^-24 each around the exact quotient, plus RN(x / s)'s half ulp), so when
-// y scaled down and up by 2^-20 (~8 ulps, each product rounded) converts to
-// one code, the monotone conversion gives RN(x / s) that code too. Only a y
-// within ~8 ulps of an e4m3 rounding boundary (about 1 in 60,000) takes the
-// correctly rounded division.
-__device__ __forceinline__ uint32_t e4m3_of_quotient(float x, float s, float rs) {
-  const float y = x * rs;
-  const uint32_t c = e4m3_of(y);
-  if (e4m3_of(y * 0.99999904632568359375f) == c && e4m3_of(y * 1.00000095367431640625f) == c) return c;
-  return e4m3_of(__fdiv_rn(x, s));
-}
-
-// 8 bf16 -> 8 e4m3 codes (element i in byte i) of the correctly rounded x/s;
-// rs = __frcp_rn(sc).
-__device__ __forceinline__ uint2 quant8(const uint4 &v, float sc, float rs) {
+// 8 bf16 -> 8 e4m3 codes (element i in byte i), each x/s correctly rounded.
+__device__ __forceinline__ uint2 quant8(const uint4 &v, float sc) {
   uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t b[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    b[2 * i] = e4m3_of_quotient(bf16lo(w[i]), sc, rs);
-    b[2 * i + 1] = e4m3_of_quotient(bf16hi(w[i]), sc, rs);
+    b[2 * i] = e4m3_of(__fdiv_rn(bf16lo(w[i]), sc));
+    b[2 * i + 1] = e4m3_of(__fdiv_rn(bf16hi(w[i]), sc));
   }
   uint2 r;
   r.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
