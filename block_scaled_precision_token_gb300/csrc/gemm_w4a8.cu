@@ -82,6 +82,7 @@ struct Params {
   int tma_store;         // 1: bf16 output tiles leave through smem + TMA tensor stores
   int l2_prefetch;       // 1: producer 0 prefetches the CTA's whole weight range into L2 at start
   int cluster;           // 1: the `splits` CTAs of a cluster split K and exchange partials in DSMEM
+  int xchg_stage;        // 1 (cluster, one unit per CTA): exchange the whole tile from the pipeline stages
   const uint8_t *w;      // packed weight codes [NT][KB][128][64]
   const float *s;
   const uint8_t *sf;     // scale atoms of the prepacked weight
@@ -438,21 +439,33 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
             }
           }
         } else if (p.cluster) {
-          // Split-K inside the cluster: this CTA's partial chunk goes to its
-          // staging buffer as fp32 [CH][128]; then every CTA sums its 1/splits
-          // share of the 128 n (in groups of 4) over all CTAs' partials, in
-          // rank order (deterministic), and stores bf16(s[t] * sum).
-          float *red = reinterpret_cast<float *>(staging);
-          if (xchg > 0 && leader &&
-              !mbar_wait_cluster(red_empty, (xchg - 1u) & 1u, abort_flag, p.err, DEV_ERR_WAIT_PEER))
-            *epi_abort = 1;
-          named_bar_sync(1, 128);
-          if (*epi_abort) {
-            stop = true;
-            break;
+          // Split-K inside the cluster: this CTA's partial goes to its own
+          // shared memory as fp32 [tokens][128]; then every CTA sums its
+          // 1/splits share of the 128 n (in groups of 4) over all CTAs'
+          // partials, in rank order (deterministic), and stores
+          // bf16(s[t] * sum). With one unit per CTA (p.xchg_stage) the whole
+          // tile goes into the drained pipeline stages -- every MMA of the
+          // unit has completed (its accumulator barrier) and no load follows --
+          // and one exchange round covers all BT tokens; otherwise the
+          // staging buffer carries one 32-token chunk per round.
+          const bool whole = p.xchg_stage != 0;
+          float *red = whole ? reinterpret_cast<float *>(smem) : reinterpret_cast<float *>(staging);
+          const int row0 = whole ? c0 : 0;        // this chunk's first token row in red
+          const int rows = whole ? BT : CH;       // token rows of one exchange round
+          const int tbase = whole ? t0 : t0 + c0;
+          if (!whole) {
+            if (xchg > 0 && leader &&
+                !mbar_wait_cluster(red_empty, (xchg - 1u) & 1u, abort_flag, p.err, DEV_ERR_WAIT_PEER))
+              *epi_abort = 1;
+            named_bar_sync(1, 128);
+            if (*epi_abort) {
+              stop = true;
+              break;
+            }
           }
 #pragma unroll
-          for (int j = 0; j < CH; ++j) red[j * 128 + q * 32 + lane] = v[j];
+          for (int j = 0; j < CH; ++j) red[(row0 + j) * 128 + q * 32 + lane] = v[j];
+          if (whole && c0 + CH < BT) continue;   // more chunks before the (single) round
           named_bar_sync(1, 128);
           if (leader) {
             fence_acq_rel_cluster();
@@ -467,7 +480,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
           const int rank = static_cast<int>(cluster_ctarank());
           const int qlo = rank * 32 / p.splits, nq = (rank + 1) * 32 / p.splits - qlo;
           const uint32_t red_base = smem_u32(red);
-          for (int idx = ew * 32 + lane; idx < CH * nq; idx += 128) {
+          for (int idx = ew * 32 + lane; idx < rows * nq; idx += 128) {
             const int j = idx / nq, qd = qlo + (idx - j * nq);
             const uint32_t off = red_base + static_cast<uint32_t>((j * 128 + qd * 4) * 4);
             float4 a4 = ld_dsmem_f32x4(mapa_shared(off, 0));
@@ -478,7 +491,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
               a4.z += b4.z;
               a4.w += b4.w;
             }
-            const int t = t0 + c0 + j;
+            const int t = tbase + j;
             if (t < p.M) {
               const float sc = __ldg(p.s + t);
               const int n0 = nt * 128 + qd * 4;
@@ -581,6 +594,7 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
   p.tma_store = use_tma_store;
   p.l2_prefetch = options().l2_prefetch;
   p.cluster = pl.cluster;
+  p.xchg_stage = (pl.cluster && pl.units <= pl.grid) ? 1 : 0;
   p.w = packed;
   p.s = s;
   p.sf = packed + mx_packed_codes_bytes(N, K);
@@ -693,13 +707,14 @@ GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
     // The cluster exchange beats the workspace path from 32 tokens up
     // (measured); at 16 tokens the partial tiles are small enough that the
     // last-arriving CTA sums them faster than a cluster round trip.
-    // Prefill tiles take the cluster path only when forced: each 32-token
-    // chunk costs a cluster round trip, and at 256 tokens the eight round
-    // trips ate the gain (measured: M=256, 5120x17408, 3 splits 49.9 us vs
-    // 49.8 us unsplit).
-    const bool cl_ok = bt <= 64 || forced_s;
-    const int ncl = (options().cluster_split && cl_ok && bt >= 32 && s >= 2 && s <= 6) ? w4a8::max_clusters(bt, s) : 0;
-    if (bt >= 128 && !forced_s && s > 1 && !prefill_ws_ok) continue;
+    // Prefill tiles take the cluster path when one wave of clusters covers
+    // every tile: each CTA then has one unit and exchanges its whole tile
+    // from the drained pipeline stages in one round (per-32-token rounds ate
+    // the gain at 256 tokens: M=256, 5120x17408, 3 splits 49.9 us vs 49.8 us
+    // unsplit).
+    int ncl = (options().cluster_split && bt >= 32 && s >= 2 && s <= 6) ? w4a8::max_clusters(bt, s) : 0;
+    if (bt >= 128 && !forced_s && tiles > ncl) ncl = 0;
+    if (bt >= 128 && !forced_s && s > 1 && ncl == 0 && !prefill_ws_ok) continue;
     double t;
     int64_t grid;
     if (ncl > 0) {
@@ -708,7 +723,8 @@ GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
       const double waves = std::ceil(static_cast<double>(tiles) / nclust);
       const double t_unit =
           std::max(kbps * kb_bytes / std::min(hbm / active, sm_bw), kbps * kb_flops / sm_flops);
-      t = waves * t_unit + xchg_s + 0.5e-6 * s;
+      const double xchg = waves == 1 ? 3.0e-6 : xchg_s;   // one whole-tile round, or a round per 32 tokens
+      t = waves * t_unit + xchg + 0.5e-6 * s;
       grid = active;
     } else {
       const int64_t active = std::min<int64_t>(units, sms);
