@@ -263,7 +263,9 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * key 6: W4A8 decode split-K across a thread-block cluster with the partial
  * sums exchanged in distributed shared memory (1, default) or through the
  * caller's workspace (0); key 7: force the block-FP8 token tile (0 =
- * automatic, else 16/32/64/128).
+ * automatic, else 16/32/64/128); key 9: block-FP8 activation scales carried
+ * by each pipeline stage (1, default, when K/128 is a multiple of 4) or
+ * loaded by the scale warp (0).
  */
 int r4_set_option(int key, int64_t value);
 
