@@ -311,8 +311,14 @@ def run_sections(r4q, synth, device, sweep, l2_bytes, peaks):
             g = capture(fn)
             ms = time_graph(g, 10) / R
             tf = 2.0 * M * N * K / ms / 1e9
-            pre[f"M{M}_N{N}_K{K}"] = {"us": round(ms * 1e3, 1), "TFLOPs": round(tf, 1),
-                                      "frac_fp8_peak": round(tf / fp8_peak, 3) if fp8_peak else None}
+            ent = {"us": round(ms * 1e3, 1), "TFLOPs": round(tf, 1),
+                   "frac_fp8_peak": round(tf / fp8_peak, 3) if fp8_peak else None}
+            if fp8_peak and peaks.get("hbm_gbs"):
+                # the applicable roofline: max(flops / tensor peak, bytes / HBM bandwidth)
+                t_bound = max(2.0 * M * N * K / (fp8_peak * 1e12), gemm_bytes(M, N, K) / (peaks["hbm_gbs"] * 1e9))
+                ent["roofline_us"] = round(t_bound * 1e6, 1)
+                ent["frac_roofline"] = round(t_bound * 1e3 / ms, 3)
+            pre[f"M{M}_N{N}_K{K}"] = ent
             del g, pool, x, q, s, c, ws
     out["prefill_w4a8"] = pre
     out["prefill_peak_TFLOPs"] = {"value": fp8_peak, "how": "measured bf16 cuBLAS burst x 2 (fp8/bf16 nominal ratio)"}

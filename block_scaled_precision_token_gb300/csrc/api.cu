@@ -146,6 +146,7 @@ int r4_set_option(int key, int64_t value) {
     case 5: options().l2_prefetch = value ? 1 : 0; return R4_OK;
     case 6: options().cluster_split = value ? 1 : 0; return R4_OK;
     case 9: options().fp8_stage_scales = value ? 1 : 0; return R4_OK;
+    case 10: options().inject_stall = value ? 1 : 0; return R4_OK;
     case 7:
       if (value != 0 && value != 16 && value != 32 && value != 64 && value != 128) return R4_ERR_INVALID_ARG;
       options().fp8_token_tile = static_cast<int>(value);

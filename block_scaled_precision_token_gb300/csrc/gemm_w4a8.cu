@@ -83,6 +83,7 @@ struct Params {
   int l2_prefetch;       // 1: producer 0 prefetches the CTA's whole weight range into L2 at start
   int cluster;           // 1: the `splits` CTAs of a cluster split K and exchange partials in DSMEM
   int xchg_stage;        // 1 (cluster, one unit per CTA): exchange the whole tile from the pipeline stages
+  int inject_stall;      // test of the bounded waits: CTA 0 withholds its first activation copy
   const uint8_t *w;      // packed weight codes [NT][KB][128][64]
   const float *s;
   const uint8_t *sf;     // scale atoms of the prepacked weight
@@ -270,7 +271,11 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
               mbar_arrive(&full_bar[stage]);
             }
           }
-          if (i < nkb) tma_load_2d(st + kWSmem, &tm_x, &full_bar[stage], kb * kBK, tt * BT, pol_x);
+          // (Failure-detection test: with inject_stall, CTA 0 never issues its
+          // first activation copy, so that stage's transaction never completes
+          // and the consumer's bounded wait must expire and report.)
+          const bool withhold = p.inject_stall && blockIdx.x == 0 && gbase + i == 0;
+          if (i < nkb && !withhold) tma_load_2d(st + kWSmem, &tm_x, &full_bar[stage], kb * kBK, tt * BT, pol_x);
           // Record the newest phase of every stage, padding slots included: a
           // parity wait cannot tell phase k from k + 2, and a stage only
           // advances after its earlier phases completed.
@@ -595,6 +600,7 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
   p.l2_prefetch = options().l2_prefetch;
   p.cluster = pl.cluster;
   p.xchg_stage = (pl.cluster && pl.units <= pl.grid) ? 1 : 0;
+  p.inject_stall = options().inject_stall;
   p.w = packed;
   p.s = s;
   p.sf = packed + mx_packed_codes_bytes(N, K);

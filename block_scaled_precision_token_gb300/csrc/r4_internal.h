@@ -32,6 +32,7 @@ struct Options {
   int fp8_splits = 0;       // 0 = automatic
   int fp8_token_tile = 0;   // 0 = automatic, else 16/32/64/128
   int fp8_stage_scales = 1; // block-FP8: activation scales ride with the pipeline stage when possible
+  int inject_stall = 0;     // tests only: the next W4A8 launches withhold one copy (bounded-wait test)
   int pdl = 1;              // launch with programmatic stream serialization
   int l2_prefetch = 0;      // W4A8: bulk L2 prefetch of the CTA's whole weight range at kernel start
   int cluster_split = 1;    // W4A8 decode tiles: split-K across a thread-block cluster when possible

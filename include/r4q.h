@@ -265,7 +265,11 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * caller's workspace (0); key 7: force the block-FP8 token tile (0 =
  * automatic, else 16/32/64/128); key 9: block-FP8 activation scales carried
  * by each pipeline stage (1, default, when K/128 is a multiple of 4) or
- * loaded by the scale warp (0).
+ * loaded by the scale warp (0); key 10 (tests of failure detection only):
+ * 1 makes the next W4A8 launches withhold one activation copy in their
+ * first CTA, so a pipeline wait never completes, expires after ~2 s and is
+ * reported by r4_device_error (the launch itself returns R4_OK, the output
+ * is unspecified and the context stays usable); 0 (default) turns it off.
  */
 int r4_set_option(int key, int64_t value);
 

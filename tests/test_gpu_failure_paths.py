@@ -1,0 +1,123 @@
+"""Failure detection and capture safety, on the GPU without a fault.
+
+* A pipeline wait that can never complete (a test option withholds one TMA
+  copy in the first CTA of a W4A8 launch) must expire after its ~2 s limit,
+  leave a device error word that r4_device_error reports, and leave the
+  context usable: the next launch is correct.
+* Every entry point must be capturable in a CUDA graph (the library never
+  allocates or synchronizes), and the graph's results must equal the eager
+  ones bit for bit."""
+
+import time
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_precision_token_gb300 import synth
+from oracle import gemm as G
+from oracle import quant as Q
+from tests.gpu_util import assert_gemm_matches, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+# device error codes of the waits that can expire first here: the MMA issuer
+# on the starved pipeline stage, or the epilogue on the accumulator it feeds
+WAIT_FULL, WAIT_ACC_FULL = 1, 3
+
+
+@pytest.fixture(scope="module")
+def r4q():
+    m = require_gpu()
+    yield m
+    m.r4_set_option(10, 0)
+
+
+def _w4a8_inputs(r4q, M, N, K):
+    x = synth.activations(M, K, synth.CFG_DECODE, outliers=True)
+    w = synth.weights_fp32(N, K, synth.CFG_DECODE)
+    p, sc = Q.quant_mxfp4_ocp(w.numpy())
+    q, s = Q.quant_act(x.float().numpy())
+    pk = r4q.prepack_mxfp4(torch.from_numpy(p).cuda(), torch.from_numpy(sc).cuda(), N, K)
+    return torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), pk, (q, s, p, sc)
+
+
+def test_bounded_wait_expires_and_reports(r4q):
+    M, N, K = 8, 512, 1024
+    q, s, pk, ref = _w4a8_inputs(r4q, M, N, K)
+    r4q.r4_device_error(clear=True)
+    r4q.r4_set_option(10, 1)
+    try:
+        t0 = time.time()
+        r4q.gemm_w4a8(q, s, pk, N, K)          # launch succeeds; a stage never fills
+        torch.cuda.synchronize()                # returns: every wait is bounded
+        elapsed = time.time() - t0
+    finally:
+        r4q.r4_set_option(10, 0)
+    code = r4q.r4_device_error(clear=True)
+    assert code in (WAIT_FULL, WAIT_ACC_FULL), f"device error word {code}"
+    assert 1.0 < elapsed < 30.0, f"the stalled launch took {elapsed:.1f} s"
+    # the context is intact: the same call now gives the oracle's result
+    c = r4q.gemm_w4a8(q, s, pk, N, K)
+    torch.cuda.synchronize()
+    assert r4q.r4_device_error(clear=True) == 0
+    c64, _ = G.gemm_w4a8(*ref)
+    assert_gemm_matches(c, c64, "after the stalled launch")
+
+
+def test_every_entry_point_captures_in_a_graph(r4q):
+    dev = torch.device("cuda")
+    M, K, N = 16, 2048, 1024
+    x = synth.activations(M, K, synth.CFG_DECODE, outliers=True).to(dev)
+    res = synth.activations(M, K, synth.CFG_TINY).to(dev)
+    nw = (synth.activations(1, K, synth.CFG_TINY)[0] * 0.1).to(torch.bfloat16).to(dev)
+    w = synth.weights_fp32(N, K, synth.CFG_DECODE).to(dev)
+    p, sc = r4q.quantize_mxfp4_weight(w)
+    pk = r4q.prepack_mxfp4(p, sc, N, K)
+    wq, Ws = r4q.quantize_blockfp8_weight(w)
+    pk8 = r4q.prepack_blockfp8(wq, Ws, N, K)
+    wb = synth.weights_bf16(256, K, synth.CFG_SKINNY).to(dev)
+    gu = synth.activations(M, 2 * K, synth.CFG_TINY).to(dev)
+    # outputs and workspaces allocated before capture
+    q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    s = torch.empty((M,), dtype=torch.float32, device=dev)
+    qg = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sg = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+    c1 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    c2 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    c3 = torch.empty((M, 256), dtype=torch.bfloat16, device=dev)
+    q2 = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    s2 = torch.empty((M,), dtype=torch.float32, device=dev)
+    ro = torch.empty_like(res)
+    q3 = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    s3 = torch.empty((M,), dtype=torch.float32, device=dev)
+    ws1 = r4q.workspace(r4q.R4_OP_W4A8_MXFP4, M, N, K, dev)
+    ws2 = r4q.workspace(r4q.R4_OP_BLOCKFP8, M, N, K, dev)
+
+    def step():
+        r4q.r4_quant_fp8_per_token(x, M, K, K, K, q, s)
+        r4q.r4_quant_fp8_per_token(x, M, K, K, 128, qg, sg)
+        r4q.r4_gemm_w4a8_mxfp4(q, s, pk, M, N, K, c1, N, ws1)
+        r4q.r4_gemm_blockfp8(qg, sg, pk8, M, N, K, c2, N, ws2)
+        r4q.r4_gemm_bf16_nt_skinny(x, wb, M, 256, K, c3, 256)
+        r4q.r4_add_rmsnorm_quant_fp8(x, res, nw, 1e-6, M, K, ro, q2, s2)
+        r4q.r4_silu_mul_quant_fp8(gu, M, K, q3, s3)
+
+    outs = (q, s, qg, sg, c1, c2, c3, q2, s2, ro, q3, s3)
+    step()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in outs]
+    for t in outs:
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    assert r4q.r4_device_error(clear=True) == 0
+    for a, b in zip(eager, outs):
+        assert torch.equal(a, b)
