@@ -48,6 +48,25 @@ int device_sm_count() {
   return g_sms[d];
 }
 
+int row_split(int64_t M, int64_t K, RowKind kind) {
+  if (options().row_split > 0) return options().row_split;
+  // Fitted on GB300 (graph-timed launches, M 1..256): a cluster costs about
+  // 0.4 us more to launch and synchronise, so a row is split only when its
+  // work is well above that (per-token quant K >= 10240, the norm producer
+  // K >= 5120, the SiLU producer N >= 3072), and into no more CTAs than
+  // still gain: up to one CTA per SM for the quantizer (half that for the
+  // norm producer, whose CTAs synchronise twice), four per SM for the
+  // SiLU producer, whose exponential and two divisions per element make it
+  // issue-bound. Each CTA keeps at least 1024 elements.
+  const int sms = device_sm_count();
+  const int64_t min_k = kind == RowKind::kQuant ? 10240 : kind == RowKind::kNorm ? 5120 : 3072;
+  const int64_t cap = kind == RowKind::kQuant ? sms : kind == RowKind::kNorm ? sms / 2 : 4 * sms;
+  if (K < min_k || (kind == RowKind::kSilu && M >= sms)) return 1;
+  int c = 1;
+  while (c < 8 && M * 2 * c <= cap && K >= 1024 * 2 * c) c *= 2;
+  return c;
+}
+
 int *device_error_word() {
   const int d = current_device();
   if (g_err_ptr[d] == nullptr) {
@@ -147,6 +166,10 @@ int r4_set_option(int key, int64_t value) {
     case 6: options().cluster_split = value ? 1 : 0; return R4_OK;
     case 9: options().fp8_stage_scales = value ? 1 : 0; return R4_OK;
     case 10: options().inject_stall = value ? 1 : 0; return R4_OK;
+    case 11:
+      if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return R4_ERR_INVALID_ARG;
+      options().row_split = static_cast<int>(value);
+      return R4_OK;
     case 7:
       if (value != 0 && value != 16 && value != 32 && value != 64 && value != 128) return R4_ERR_INVALID_ARG;
       options().fp8_token_tile = static_cast<int>(value);

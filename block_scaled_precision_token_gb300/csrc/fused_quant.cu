@@ -8,9 +8,11 @@
 //  * SiluAndMul + quant on [g | u]: h = bf16(bf16(silu(g)) * u), then the
 //    per-token rule.
 //
-// HBM-bound row kernels: one CTA per row holds the row in registers (16-byte
-// vectors, read once), reduces it twice (sum of squares, then amax) and
-// writes the codes -- one launch where the unfused chain takes two or three.
+// HBM-bound row kernels: the CTAs of a row hold it in registers (16-byte
+// vectors, read once), reduce it twice (sum of squares, then amax) and write
+// the codes -- one launch where the unfused chain takes two or three. A
+// short batch spreads each row over a thread-block cluster whose CTAs
+// combine their partial sums and maxima through distributed shared memory.
 // The norm is fp32 with correctly rounded division and reciprocal square
 // root; SiLU uses CUDA's expf; the codes come from correctly rounded
 // quotients (quant_common.cuh).
@@ -57,39 +59,50 @@ __device__ __forceinline__ float block_max(float a, float *red) {
   return t;
 }
 
-// Scale and codes for one row held as bf16 vectors h[VPT]; writes s[row], q.
+// Scale and codes for the columns [c0, c1) of one row, held as bf16 vectors
+// h[VPT]; the row's C CTAs (a cluster when C > 1) agree on its maximum.
+// Writes s[row] (CTA 0 of the row) and the codes. With C > 1 the kernel
+// must call cluster_wait() before it exits.
 template <int VPT>
-__device__ __forceinline__ void quant_row(const uint4 (&h)[VPT], int K, uint8_t *qr, float *s_row, float *red) {
+__device__ __forceinline__ void quant_row(const uint4 (&h)[VPT], int c0, int c1, int C, bool first, uint8_t *qr,
+                                          float *s_row, float *red, float *slot) {
   const int tid = threadIdx.x, nt = blockDim.x;
   float a = 0.f;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) a = fmaxf(a, absmax8(h[i]));   // padding vectors are zero
   a = block_max(a, red);
+  if (C > 1) {
+    a = cluster_combine<true>(a, slot, C);
+    cluster_arrive();
+  }
   const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
-  if (tid == 0) *s_row = sc;
+  if (first && tid == 0) *s_row = sc;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int k = (i * nt + tid) * 8;
-    if (k < K) *reinterpret_cast<uint2 *>(qr + k) = quant8(h[i], sc);
+    const int k = c0 + (i * nt + tid) * 8;
+    if (k < c1) *reinterpret_cast<uint2 *>(qr + k) = quant8(h[i], sc);
   }
 }
 
+// Row `blockIdx.x / C`, columns [part * cols, part * cols + cols) of it.
 template <int VPT>
 __global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_kernel(const uint16_t *__restrict__ y,
                                                                    const uint16_t *res, const uint16_t *__restrict__ w,
-                                                                   float eps, int K, uint16_t *ro,
+                                                                   float eps, int K, int cols, int C, uint16_t *ro,
                                                                    uint8_t *__restrict__ q, float *__restrict__ s) {
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait();   // y and the residual come from the preceding kernels
   __shared__ float red[kThreads / 32];
-  const int row = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+  __shared__ float slot[2];
+  const int row = blockIdx.x / C, part = blockIdx.x - row * C, tid = threadIdx.x, nt = blockDim.x;
+  const int c0 = part * cols, c1 = min(K, c0 + cols);
   const size_t base = static_cast<size_t>(row) * K;
   uint4 r[VPT];
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int k = (i * nt + tid) * 8;
-    if (k < K) {
+    const int k = c0 + (i * nt + tid) * 8;
+    if (k < c1) {
       // res may alias ro (in-place residual update): each vector is read
       // before the same thread writes it.
       const uint4 a = __ldg(reinterpret_cast<const uint4 *>(y + base + k));
@@ -110,11 +123,12 @@ __global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_kernel(const uint1
     }
   }
   ss = block_sum(ss, red);
+  if (C > 1) ss = cluster_combine<false>(ss, &slot[0], C);
   const float inv = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), eps));
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int k = (i * nt + tid) * 8;
-    if (k < K) {
+    const int k = c0 + (i * nt + tid) * 8;
+    if (k < c1) {
       const uint4 wv4 = __ldg(reinterpret_cast<const uint4 *>(w + k));
       const uint32_t wv[4] = {wv4.x, wv4.y, wv4.z, wv4.w};
       uint32_t rv[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
@@ -125,7 +139,8 @@ __global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_kernel(const uint1
       r[i] = make_uint4(rv[0], rv[1], rv[2], rv[3]);
     }
   }
-  quant_row<VPT>(r, K, q + base, s + row, red);
+  quant_row<VPT>(r, c0, c1, C, part == 0, q + base, s + row, red, &slot[1]);
+  if (C > 1) cluster_wait();
 }
 
 // g * sigmoid(g) to a few float32 ulps (CUDA's expf); exp(-g) = inf gives
@@ -133,18 +148,21 @@ __global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_kernel(const uint1
 __device__ __forceinline__ float silu_f32(float g) { return __fdiv_rn(g, 1.f + expf(-g)); }
 
 template <int VPT>
-__global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const uint16_t *__restrict__ gu, int N,
-                                                                uint8_t *__restrict__ q, float *__restrict__ s) {
+__global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const uint16_t *__restrict__ gu, int N, int cols,
+                                                                int C, uint8_t *__restrict__ q,
+                                                                float *__restrict__ s) {
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait();   // gu comes from the preceding kernel
   __shared__ float red[kThreads / 32];
-  const int row = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+  __shared__ float slot;
+  const int row = blockIdx.x / C, part = blockIdx.x - row * C, tid = threadIdx.x, nt = blockDim.x;
+  const int c0 = part * cols, c1 = min(N, c0 + cols);
   const uint16_t *gr = gu + static_cast<size_t>(row) * 2 * N;
   uint4 h[VPT];
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int k = (i * nt + tid) * 8;
-    if (k < N) {
+    const int k = c0 + (i * nt + tid) * 8;
+    if (k < c1) {
       const uint4 g4 = __ldg(reinterpret_cast<const uint4 *>(gr + k));
       const uint4 u4 = __ldg(reinterpret_cast<const uint4 *>(gr + N + k));
       const uint32_t gv[4] = {g4.x, g4.y, g4.z, g4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
@@ -160,7 +178,8 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const uint16_t
       h[i] = make_uint4(0, 0, 0, 0);
     }
   }
-  quant_row<VPT>(h, N, q + static_cast<size_t>(row) * N, s + row, red);
+  quant_row<VPT>(h, c0, c1, C, part == 0, q + static_cast<size_t>(row) * N, s + row, red, &slot);
+  if (C > 1) cluster_wait();
 }
 
 int threads_for(int64_t K) {
@@ -169,20 +188,40 @@ int threads_for(int64_t K) {
   return t < 32 ? 32 : t;
 }
 
+// Row split for a row of K columns: CTAs per row, columns per CTA, threads
+// and 16-byte vectors per thread.
+struct RowSplit {
+  int C, cols, threads;
+  int64_t per;
+};
+RowSplit split_row(int64_t M, int64_t K, RowKind kind) {
+  int C = row_split(M, K, kind);
+  if (M * C > (int64_t{1} << 30)) C = 1;
+  const int64_t cols = ceil_div(ceil_div(K, static_cast<int64_t>(C)), int64_t{8}) * 8;
+  const int t = threads_for(cols);
+  return {C, static_cast<int>(cols), t, ceil_div(cols / 8, static_cast<int64_t>(t))};
+}
+
 }  // namespace
 
+// Rows of up to 24576 columns fit in registers (VPT <= 12 at 256 threads),
+// so the split never has to fall back to a two-pass kernel.
 cudaError_t launch_add_rmsnorm_quant(const uint16_t *y, const uint16_t *res, const uint16_t *w, float eps, int64_t M,
                                      int64_t K, uint16_t *ro, uint8_t *q, float *s, cudaStream_t st) {
-  const int t = threads_for(K);
-  const int64_t per = ceil_div(K / 8, t);
-  const dim3 grid(static_cast<unsigned>(M));
+  const RowSplit rs = split_row(M, K, RowKind::kNorm);
+  const dim3 grid(static_cast<unsigned>(M * rs.C));
   const int k = static_cast<int>(K);
-#define R4_ARQ(V)                                                                                     \
-  {                                                                                                   \
-    const cudaError_t e = launch_pdl(add_rmsnorm_quant_kernel<V>, grid, dim3(t), 0, st, y, res, w, eps, k, ro, q, s); \
-    if (e != cudaSuccess) return e;                                                                   \
-    set_last_kernel("add_rmsnorm_quant_kernel<" #V ">");                                              \
+#define R4_ARQ(V)                                                                                            \
+  {                                                                                                          \
+    const cudaError_t e =                                                                                    \
+        rs.C > 1 ? launch_pdl_cluster(add_rmsnorm_quant_kernel<V>, grid, dim3(rs.threads), 0, st, rs.C, y, res, \
+                                      w, eps, k, rs.cols, rs.C, ro, q, s)                                      \
+                 : launch_pdl(add_rmsnorm_quant_kernel<V>, grid, dim3(rs.threads), 0, st, y, res, w, eps, k,    \
+                              rs.cols, rs.C, ro, q, s);                                                        \
+    if (e != cudaSuccess) return e;                                                                          \
+    set_last_kernel("add_rmsnorm_quant_kernel<" #V ">");                                                     \
   }
+  const int64_t per = rs.per;
   if (per <= 1) R4_ARQ(1) else if (per <= 2) R4_ARQ(2) else if (per <= 4) R4_ARQ(4) else if (per <= 9) R4_ARQ(9)
   else R4_ARQ(12)
 #undef R4_ARQ
@@ -190,16 +229,19 @@ cudaError_t launch_add_rmsnorm_quant(const uint16_t *y, const uint16_t *res, con
 }
 
 cudaError_t launch_silu_mul_quant(const uint16_t *gu, int64_t M, int64_t N, uint8_t *q, float *s, cudaStream_t st) {
-  const int t = threads_for(N);
-  const int64_t per = ceil_div(N / 8, t);
-  const dim3 grid(static_cast<unsigned>(M));
+  const RowSplit rs = split_row(M, N, RowKind::kSilu);
+  const dim3 grid(static_cast<unsigned>(M * rs.C));
   const int n = static_cast<int>(N);
-#define R4_SMQ(V)                                                                                     \
-  {                                                                                                   \
-    const cudaError_t e = launch_pdl(silu_mul_quant_kernel<V>, grid, dim3(t), 0, st, gu, n, q, s);   \
-    if (e != cudaSuccess) return e;                                                                   \
-    set_last_kernel("silu_mul_quant_kernel<" #V ">");                                                 \
+#define R4_SMQ(V)                                                                                            \
+  {                                                                                                          \
+    const cudaError_t e =                                                                                    \
+        rs.C > 1 ? launch_pdl_cluster(silu_mul_quant_kernel<V>, grid, dim3(rs.threads), 0, st, rs.C, gu, n,    \
+                                      rs.cols, rs.C, q, s)                                                     \
+                 : launch_pdl(silu_mul_quant_kernel<V>, grid, dim3(rs.threads), 0, st, gu, n, rs.cols, rs.C, q, s); \
+    if (e != cudaSuccess) return e;                                                                          \
+    set_last_kernel("silu_mul_quant_kernel<" #V ">");                                                        \
   }
+  const int64_t per = rs.per;
   if (per <= 1) R4_SMQ(1) else if (per <= 2) R4_SMQ(2) else if (per <= 4) R4_SMQ(4) else if (per <= 9) R4_SMQ(9)
   else R4_SMQ(12)
 #undef R4_SMQ

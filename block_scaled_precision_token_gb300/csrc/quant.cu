@@ -6,8 +6,10 @@
 // divisions are correctly rounded (__fdiv_rn) so the codes are bit-exact
 // against any other correctly rounded fp32 implementation.
 //
-// HBM-bound: 2 bytes read, 1 byte (+ scales) written per element. One CTA per
-// row keeps the whole row in registers (read once), with 16-byte vector loads.
+// HBM-bound: 2 bytes read, 1 byte (+ scales) written per element. The CTAs
+// of a row keep it in registers (read once), with 16-byte vector loads; a
+// short batch spreads each row over a thread-block cluster whose CTAs agree
+// on the row maximum through distributed shared memory.
 
 #include <cuda_bf16.h>
 #include <cuda_fp4.h>
@@ -22,14 +24,19 @@ namespace {
 
 using namespace qc;
 
-// One CTA per row; VPT 16-byte vectors per thread stay in registers.
+// C CTAs per row (C = 1, or a thread-block cluster of C when the row's scale
+// needs the whole row); CTA `part` owns columns [part * cols, part * cols +
+// cols) and keeps them in registers, VPT 16-byte vectors per thread.
 template <int VPT>
 __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restrict__ x, int K, int64_t ldx,
-                                                        int group, uint8_t *__restrict__ q,
+                                                        int group, int cols, int C, uint8_t *__restrict__ q,
                                                         float *__restrict__ s) {
   if (threadIdx.x == 0) pdl_launch_dependents();   // the next kernel may start its weight stream
   pdl_wait();                                       // x (and the q, s buffers) follow the stream order
-  const int row = blockIdx.x;
+  const int row = blockIdx.x / C;
+  const int part = blockIdx.x - row * C;
+  const int c0 = part * cols;
+  const int c1 = min(K, c0 + cols);
   const int tid = threadIdx.x;
   const int nt = blockDim.x;
   const uint16_t *xr = x + static_cast<size_t>(row) * ldx;
@@ -37,11 +44,12 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
   uint4 v[VPT];
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int k = (i * nt + tid) * 8;
-    v[i] = (k < K) ? __ldg(reinterpret_cast<const uint4 *>(xr + k)) : make_uint4(0, 0, 0, 0);
+    const int k = c0 + (i * nt + tid) * 8;
+    v[i] = (k < c1) ? __ldg(reinterpret_cast<const uint4 *>(xr + k)) : make_uint4(0, 0, 0, 0);
   }
   if (group == K) {
     __shared__ float red[8];
+    __shared__ float slot;
     float a = 0.f;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) a = fmaxf(a, absmax8(v[i]));
@@ -50,24 +58,29 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
     __syncthreads();
     a = red[0];
     for (int w = 1; w < (nt >> 5); ++w) a = fmaxf(a, red[w]);
+    if (C > 1) {
+      a = cluster_combine<true>(a, &slot, C);
+      cluster_arrive();
+    }
     const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
-    if (tid == 0) s[row] = sc;
+    if (part == 0 && tid == 0) s[row] = sc;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int k = (i * nt + tid) * 8;
-      if (k < K) *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc);
+      const int k = c0 + (i * nt + tid) * 8;
+      if (k < c1) *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc);
     }
+    if (C > 1) cluster_wait();   // peers may still read `slot` until they arrive
   } else {
-    // group of 128 = 16 lanes x 8 elements; nt is a multiple of 32
+    // group of 128 = 16 lanes x 8 elements; nt is a multiple of 32 and c0 of 128
     const int groups = K / 128;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int k = (i * nt + tid) * 8;
+      const int k = c0 + (i * nt + tid) * 8;
       float a = absmax8(v[i]);
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
       const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
-      if (k < K) {
+      if (k < c1) {
         if ((tid & 15) == 0) s[static_cast<size_t>(row) * groups + (k >> 7)] = sc;
         *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc);
       }
@@ -187,28 +200,39 @@ __global__ void __launch_bounds__(256) quant_blockfp8_weight_kernel(const float 
 
 cudaError_t launch_quant_act(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int64_t group, uint8_t *q,
                              float *s, cudaStream_t st) {
-  const int64_t vecs = K / 8;
+  const bool per_token = group == K;
+  int C = row_split(M, K, RowKind::kQuant);
+  if (M * C > (int64_t{1} << 30)) C = 1;
+  const int64_t align = per_token ? 8 : 128;
+  int64_t cols = ceil_div(ceil_div(K, static_cast<int64_t>(C)), align) * align;
+  int64_t vecs = cols / 8;
   int threads = static_cast<int>(vecs < 256 ? ((vecs + 31) / 32) * 32 : 256);
   if (threads < 32) threads = 32;
-  const int64_t per = ceil_div(vecs, threads);
-  const dim3 grid(static_cast<unsigned>(M));
-  const int g = static_cast<int>(group), k = static_cast<int>(K);
-  if (per <= 1) {
-    { const cudaError_t e = launch_pdl(quant_act_kernel<1>, grid, dim3(threads), 0, st, x, k, ldx, g, q, s); if (e != cudaSuccess) return e; }
-    set_last_kernel("quant_act_kernel<1>");
-  } else if (per <= 2) {
-    { const cudaError_t e = launch_pdl(quant_act_kernel<2>, grid, dim3(threads), 0, st, x, k, ldx, g, q, s); if (e != cudaSuccess) return e; }
-    set_last_kernel("quant_act_kernel<2>");
-  } else if (per <= 4) {
-    { const cudaError_t e = launch_pdl(quant_act_kernel<4>, grid, dim3(threads), 0, st, x, k, ldx, g, q, s); if (e != cudaSuccess) return e; }
-    set_last_kernel("quant_act_kernel<4>");
-  } else if (per <= 9) {
-    { const cudaError_t e = launch_pdl(quant_act_kernel<9>, grid, dim3(threads), 0, st, x, k, ldx, g, q, s); if (e != cudaSuccess) return e; }
-    set_last_kernel("quant_act_kernel<9>");
-  } else {
-    { const cudaError_t e = launch_pdl(quant_act_long_kernel, grid, dim3(threads), 0, st, x, k, ldx, g, q, s); if (e != cudaSuccess) return e; }
+  int64_t per = ceil_div(vecs, threads);
+  if (per > 9 && C > 1) {   // the row does not fit in registers even when split: two-pass kernel
+    C = 1;
+    cols = K;
+    threads = 256;
+    per = 10;
+  }
+  const dim3 grid(static_cast<unsigned>(M * C));
+  const int g = static_cast<int>(group), k = static_cast<int>(K), cl = static_cast<int>(cols);
+#define R4_QA(V)                                                                                             \
+  {                                                                                                          \
+    const cudaError_t e =                                                                                    \
+        (per_token && C > 1)                                                                                 \
+            ? launch_pdl_cluster(quant_act_kernel<V>, grid, dim3(threads), 0, st, C, x, k, ldx, g, cl, C, q, s) \
+            : launch_pdl(quant_act_kernel<V>, grid, dim3(threads), 0, st, x, k, ldx, g, cl, C, q, s);         \
+    if (e != cudaSuccess) return e;                                                                          \
+    set_last_kernel("quant_act_kernel<" #V ">");                                                             \
+  }
+  if (per <= 1) R4_QA(1) else if (per <= 2) R4_QA(2) else if (per <= 4) R4_QA(4) else if (per <= 9) R4_QA(9)
+  else {
+    const cudaError_t e = launch_pdl(quant_act_long_kernel, grid, dim3(threads), 0, st, x, k, ldx, g, q, s);
+    if (e != cudaSuccess) return e;
     set_last_kernel("quant_act_long_kernel");
   }
+#undef R4_QA
   return cudaGetLastError();
 }
 

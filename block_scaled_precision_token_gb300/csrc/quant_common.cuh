@@ -12,6 +12,8 @@
 
 #include <cstdint>
 
+#include "r4_device.cuh"
+
 namespace r4 {
 namespace qc {
 
@@ -53,6 +55,30 @@ __device__ __forceinline__ float warp_max(float a) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
   return a;
+}
+
+// A row split over the C CTAs (C <= 32) of a 1-D thread-block cluster:
+// combines the CTAs' block-reduced values t (sum, or max of non-negative
+// values), every thread of every CTA returning the same result. Each CTA
+// publishes t in its own shared word `slot`; after a cluster barrier lane i
+// of every warp reads CTA i's word and a butterfly shuffle combines the
+// lanes, so every CTA forms the same sum in the same order. Each combine
+// needs a slot of its own, and a CTA may not exit while a peer can still
+// read its slot: after the last combine the kernel calls cluster_arrive()
+// and, before it exits, cluster_wait().
+template <bool kMax>
+__device__ __forceinline__ float cluster_combine(float t, float *slot, int C) {
+  if (threadIdx.x == 0) *slot = t;
+  cluster_sync_all();
+  const int lane = threadIdx.x & 31;
+  float v = 0.f;
+  if (lane < C) v = ld_dsmem_f32(mapa_shared(smem_u32(slot), static_cast<uint32_t>(lane)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float u = __shfl_xor_sync(0xffffffffu, v, o);
+    v = kMax ? fmaxf(v, u) : v + u;
+  }
+  return v;
 }
 
 }  // namespace qc

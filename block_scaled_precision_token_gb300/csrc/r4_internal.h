@@ -36,8 +36,15 @@ struct Options {
   int pdl = 1;              // launch with programmatic stream serialization
   int l2_prefetch = 0;      // W4A8: bulk L2 prefetch of the CTA's whole weight range at kernel start
   int cluster_split = 1;    // W4A8 decode tiles: split-K across a thread-block cluster when possible
+  int row_split = 0;        // row-wise quantizers: CTAs per row (0 = automatic, else 1/2/4/8)
 };
 Options &options();
+
+// CTAs that share one row of a row-wise quantization kernel (1, 2, 4 or 8):
+// short batches spread each row over a thread-block cluster so that more
+// than M SMs take part.
+enum class RowKind { kQuant, kNorm, kSilu };   // per-token quant, add+RMS norm+quant, SiLU-and-mul+quant
+int row_split(int64_t M, int64_t K, RowKind kind);
 
 // Launch `kernel` on `st`; with options().pdl the launch allows programmatic
 // dependent launch (the kernel may start before its predecessor in the

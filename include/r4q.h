@@ -269,7 +269,11 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * 1 makes the next W4A8 launches withhold one activation copy in their
  * first CTA, so a pipeline wait never completes, expires after ~2 s and is
  * reported by r4_device_error (the launch itself returns R4_OK, the output
- * is unspecified and the context stays usable); 0 (default) turns it off.
+ * is unspecified and the context stays usable); 0 (default) turns it off;
+ * key 11: CTAs that share one row in the row-wise activation quantizers
+ * (per-token, group-128 and the two fused producers): 0 (default) chooses
+ * automatically (short batches spread each row over a cluster of up to 8
+ * CTAs), 1/2/4/8 force it; other values return R4_ERR_INVALID_ARG.
  */
 int r4_set_option(int key, int64_t value);
 

@@ -62,8 +62,8 @@ def _check_quant(q_gpu, s_gpu, h_lo, h_hi, what):
     c_lo, c_hi = _codes_of(h_lo, s), _codes_of(h_hi, s)
     ok = (q == c_lo) | (q == c_hi)
     assert ok.all(), f"{what}: {np.count_nonzero(~ok)} codes match neither candidate"
-    ambiguous = np.count_nonzero(h_lo != h_hi) / h_lo.size
-    assert ambiguous < 0.01, f"{what}: {ambiguous:.4f} of the elements are rounding-ambiguous"
+    ambiguous = np.count_nonzero(h_lo != h_hi)
+    assert ambiguous <= max(2, 0.01 * h_lo.size), f"{what}: {ambiguous} of {h_lo.size} elements are rounding-ambiguous"
 
 
 def _run_arq(r4q, y, res, w, eps, inplace=False):
@@ -134,6 +134,33 @@ def test_silu_mul_quant(r4q, M, N):
     qo, so, _, _ = U.silu_mul_quant(gu.float().numpy())
     assert np.mean(np_u8(q) == qo) > 0.999
     assert r4q.r4_last_kernel_name().startswith("silu_mul_quant_kernel")
+
+
+@pytest.mark.parametrize("C", [1, 2, 4, 8])
+@pytest.mark.parametrize("M,K", [(3, 5120), (2, 1000), (5, 8), (4, 17408)])
+def test_row_split(r4q, C, M, K):
+    """Rows spread over C CTAs of a cluster (partial sums of squares and
+    maxima combined across the cluster) give the same accepted results."""
+    y = _randn((M, K), M * 13 + K + C, 1.0)
+    res = _randn((M, K), M * 17 + K + C, 2.0)
+    w = _randn((K,), K + C, 0.1)
+    g = _randn((M, K), M * 19 + K + C, 3.0)
+    u = _randn((M, K), M * 23 + K + C, 1.0)
+    r4q.r4_set_option(11, C)
+    try:
+        q, s, ro = _run_arq(r4q, y, res, w, 1e-6)
+        q2, s2 = r4q.silu_mul_quant(torch.cat([g, u], dim=1).cuda())
+        check_device_error(r4q)
+    finally:
+        r4q.r4_set_option(11, 0)
+    r, h64 = U.add_rmsnorm(y.float().numpy(), res.float().numpy(), w.float().numpy(), 1e-6)
+    assert np.array_equal(bf16_to_np(ro), r)
+    h_lo, h_hi = _candidates(h64)
+    _check_quant(q, s, h_lo, h_hi, f"add_rmsnorm_quant C={C} M={M} K={K}")
+    g64, u64 = g.double().numpy(), u.double().numpy()
+    a_lo, a_hi = _candidates(g64 / (1.0 + np.exp(-g64)))
+    h1, h2 = F.bf16_round(a_lo * u64), F.bf16_round(a_hi * u64)
+    _check_quant(q2, s2, np.minimum(h1, h2), np.maximum(h1, h2), f"silu_mul_quant C={C} M={M} N={K}")
 
 
 def test_fused_quant_argument_checks(r4q):

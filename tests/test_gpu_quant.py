@@ -48,6 +48,38 @@ def test_group128_bit_exact(r4q, M, K):
     assert np.array_equal(np_u8(q), q_ref)
 
 
+@pytest.mark.parametrize("C", [1, 2, 4, 8])
+@pytest.mark.parametrize("M,K,ld,group", [
+    (6, 17408, 17408, None),     # decode row, even split
+    (3, 1000, 1000, None),       # ragged: the last CTA holds a partial slice
+    (5, 8, 8, None),             # one vector: all but the first CTA hold nothing
+    (4, 2048, 2056, None),       # row stride > K
+    (300, 5120, 5120, None),     # more rows than SMs
+    (7, 6144, 6144, 128),        # group-128 scales, slices of whole groups
+    (2, 384, 384, 128),
+])
+def test_row_split_bit_exact(r4q, C, M, K, ld, group):
+    """Each row spread over C CTAs (a thread-block cluster that agrees on the
+    per-token maximum): identical codes and scales to the oracle for every C."""
+    xb = _x(M, ld, synth.CFG_DECODE, True, seed=M * 1009 + K + C)
+    q_ref, s_ref = Q.quant_act(xb[:, :K].float().numpy(), **({} if group is None else {"group": group}))
+    r4q.r4_set_option(11, C)
+    try:
+        q, s = r4q.quant_fp8(xb.cuda()[:, :K], group=group)
+        check_device_error(r4q)
+    finally:
+        r4q.r4_set_option(11, 0)
+    assert np.array_equal(np_f32(s), s_ref)
+    assert np.array_equal(np_u8(q), q_ref)
+
+
+def test_row_split_option_checks(r4q):
+    with pytest.raises(r4q.R4Error):
+        r4q.r4_set_option(11, 3)
+    with pytest.raises(r4q.R4Error):
+        r4q.r4_set_option(11, 16)
+
+
 def test_special_rows_and_row_stride(r4q):
     M, K, ld = 6, 1024, 1040
     base = _x(M, ld, synth.CFG_DECODE, False, seed=77).float()
