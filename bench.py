@@ -370,7 +370,7 @@ def run_sections(r4q, synth, device, sweep, l2_bytes, peaks):
     out["skinny_bf16_graph"] = sk
     # quantization bandwidth
     qt = {}
-    for (M, K) in [(8192, 5120), (64, 5120), (2048, 6144)]:
+    for (M, K) in [(8192, 5120), (64, 5120), (6, 17408), (2048, 6144)]:
         x = synth.activations(M, K, synth.CFG_PREFILL).to(device)
         q = torch.empty((M, K), dtype=torch.uint8, device=device)
         s = torch.empty((M,), dtype=torch.float32, device=device)
