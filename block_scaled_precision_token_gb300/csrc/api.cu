@@ -190,6 +190,13 @@ int r4_quant_fp8_per_token(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
              : R4_ERR_CUDA;
 }
 
+int r4_check_quotients(unsigned long long *count, float *example, r4_stream_t stream) {
+  if (!count || !example) return R4_ERR_INVALID_ARG;
+  if (!aligned(count, 8) || !aligned(example, 4)) return R4_ERR_MISALIGNED;
+  return launch_check_quotients(count, example, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? R4_OK
+                                                                                                        : R4_ERR_CUDA;
+}
+
 int r4_add_rmsnorm_quant_fp8(const uint16_t *y, const uint16_t *residual, const uint16_t *weight, float eps,
                              int64_t M, int64_t K, uint16_t *residual_out, uint8_t *q, float *s, r4_stream_t stream) {
   if (!y || !residual || !weight || !residual_out || !q || !s) return R4_ERR_INVALID_ARG;

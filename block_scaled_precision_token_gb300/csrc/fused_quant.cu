@@ -14,8 +14,8 @@
 // short batch spreads each row over a thread-block cluster whose CTAs
 // combine their partial sums and maxima through distributed shared memory.
 // The norm is fp32 with correctly rounded division and reciprocal square
-// root; SiLU uses CUDA's expf; the codes come from correctly rounded
-// quotients (quant_common.cuh).
+// root; SiLU uses CUDA's expf and a fast quotient (a few ulps); the codes
+// come from correctly rounded quotients (quant_common.cuh).
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -76,11 +76,12 @@ __device__ __forceinline__ void quant_row(const uint4 (&h)[VPT], int c0, int c1,
     cluster_arrive();
   }
   const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
+  const float rc = __frcp_rn(sc);
   if (first && tid == 0) *s_row = sc;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int k = c0 + (i * nt + tid) * 8;
-    if (k < c1) *reinterpret_cast<uint2 *>(qr + k) = quant8(h[i], sc);
+    if (k < c1) *reinterpret_cast<uint2 *>(qr + k) = quant8(h[i], sc, rc);
   }
 }
 
@@ -143,9 +144,14 @@ __global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_kernel(const uint1
   if (C > 1) cluster_wait();
 }
 
-// g * sigmoid(g) to a few float32 ulps (CUDA's expf); exp(-g) = inf gives
+// g * sigmoid(g) to a few float32 ulps: CUDA's expf, then __fdividef (within
+// 2 ulps while the denominator is below 2^126); larger denominators
+// (g < -87.3) take the correctly rounded division, and exp(-g) = inf gives
 // -0 as the exact value does.
-__device__ __forceinline__ float silu_f32(float g) { return __fdiv_rn(g, 1.f + expf(-g)); }
+__device__ __forceinline__ float silu_f32(float g) {
+  const float t = 1.f + expf(-g);
+  return t < 0x1p126f ? __fdividef(g, t) : __fdiv_rn(g, t);
+}
 
 template <int VPT>
 __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const uint16_t *__restrict__ gu, int N, int cols,

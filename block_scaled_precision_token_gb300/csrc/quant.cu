@@ -3,8 +3,10 @@
 //
 // Activation rule ("radiance_mxfp4.py", _traced_quant and the comment above
 // it): s = max(amax/448, 1/(448*512)) in fp32, q = e4m3_rne_sat(x / s). Both
-// divisions are correctly rounded (__fdiv_rn) so the codes are bit-exact
-// against any other correctly rounded fp32 implementation.
+// divisions are correctly rounded (the scale by __fdiv_rn, the quotients by
+// div_by_scale, proved equal to __fdiv_rn on the quantizers' domain), so the
+// codes are bit-exact against any other correctly rounded fp32
+// implementation.
 //
 // HBM-bound: 2 bytes read, 1 byte (+ scales) written per element. The CTAs
 // of a row keep it in registers (read once), with 16-byte vector loads; a
@@ -63,11 +65,12 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
       cluster_arrive();
     }
     const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
+    const float rc = __frcp_rn(sc);
     if (part == 0 && tid == 0) s[row] = sc;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int k = c0 + (i * nt + tid) * 8;
-      if (k < c1) *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc);
+      if (k < c1) *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc, rc);
     }
     if (C > 1) cluster_wait();   // peers may still read `slot` until they arrive
   } else {
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
       const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
       if (k < c1) {
         if ((tid & 15) == 0) s[static_cast<size_t>(row) * groups + (k >> 7)] = sc;
-        *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc);
+        *reinterpret_cast<uint2 *>(qr + k) = quant8(v[i], sc, __frcp_rn(sc));
       }
     }
   }
@@ -109,9 +112,10 @@ __global__ void __launch_bounds__(256) quant_act_long_kernel(const uint16_t *__r
     a = red[0];
     for (int w = 1; w < (nt >> 5); ++w) a = fmaxf(a, red[w]);
     const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
+    const float rc = __frcp_rn(sc);
     if (tid == 0) s[row] = sc;
     for (int k = tid * 8; k < K; k += nt * 8)
-      *reinterpret_cast<uint2 *>(qr + k) = quant8(__ldg(reinterpret_cast<const uint4 *>(xr + k)), sc);
+      *reinterpret_cast<uint2 *>(qr + k) = quant8(__ldg(reinterpret_cast<const uint4 *>(xr + k)), sc, rc);
   } else {
     const int groups = K / 128;
     for (int base = 0; base < K; base += nt * 8) {
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(256) quant_act_long_kernel(const uint16_t *__r
       const float sc = fmaxf(__fdiv_rn(a, kFp8Max), kMinScale);
       if (k < K) {
         if ((tid & 15) == 0) s[static_cast<size_t>(row) * groups + (k >> 7)] = sc;
-        *reinterpret_cast<uint2 *>(qr + k) = quant8(v, sc);
+        *reinterpret_cast<uint2 *>(qr + k) = quant8(v, sc, __frcp_rn(sc));
       }
     }
   }
@@ -196,7 +200,54 @@ __global__ void __launch_bounds__(256) quant_blockfp8_weight_kernel(const float 
   }
 }
 
+// Self-check of div_by_scale on the quantizers' whole domain: block b takes
+// the bf16 amax with bit pattern b (0 .. 0x7F7F, every finite non-negative
+// value), forms the scale the per-token rule derives from it, and compares
+// div_by_scale with a correctly rounded division for every bf16 x with
+// |x| <= amax, both signs. count[0]: pairs whose e4m3 codes differ (the
+// first one's (x, s) lands in example[0..1]); count[2]: pairs whose fp32
+// quotients differ at all; count[3]: the largest |x/s| (fp32 bits) among
+// those. (Quotients of x within a few ulps of the fp32 normal range leave a
+// remainder that underflows; they are far below the smallest e4m3 code.)
+__global__ void __launch_bounds__(256) check_quotients_kernel(unsigned long long *count, float *example) {
+  const uint32_t vb = blockIdx.x;
+  const float sc = fmaxf(__fdiv_rn(__uint_as_float(vb << 16), kFp8Max), kMinScale);
+  const float rc = __frcp_rn(sc);
+  unsigned int bad_code = 0, bad_bits = 0, worst = 0;
+  for (uint32_t m = threadIdx.x; m <= vb; m += blockDim.x) {
+#pragma unroll
+    for (uint32_t sgn = 0; sgn < 2; ++sgn) {
+      const float x = __uint_as_float((m | (sgn << 15)) << 16);
+      const float exact = __fdiv_rn(x, sc), fast = div_by_scale(x, sc, rc);
+      if (__float_as_uint(exact) != __float_as_uint(fast)) {
+        ++bad_bits;
+        worst = max(worst, __float_as_uint(fabsf(exact)));
+        if (e4m3_of(exact) != e4m3_of(fast)) {
+          ++bad_code;
+          if (atomicAdd(count + 1, 1ull) == 0) {
+            example[0] = x;
+            example[1] = sc;
+          }
+        }
+      }
+    }
+  }
+  if (bad_code) atomicAdd(count, static_cast<unsigned long long>(bad_code));
+  if (bad_bits) {
+    atomicAdd(count + 2, static_cast<unsigned long long>(bad_bits));
+    atomicMax(count + 3, static_cast<unsigned long long>(worst));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_check_quotients(unsigned long long *count, float *example, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(count, 0, 4 * sizeof(unsigned long long), st);
+  if (e != cudaSuccess) return e;
+  check_quotients_kernel<<<0x7F80, 256, 0, st>>>(count, example);
+  set_last_kernel("check_quotients_kernel");
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant_act(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int64_t group, uint8_t *q,
                              float *s, cudaStream_t st) {

@@ -36,14 +36,31 @@ __device__ __forceinline__ uint32_t e4m3_of(float v) {
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
 
-// 8 bf16 -> 8 e4m3 codes (element i in byte i), each x/s correctly rounded.
-__device__ __forceinline__ uint2 quant8(const uint4 &v, float sc) {
+// x / s rounded once to fp32 -- the correctly rounded quotient -- from
+// rc = RN(1/s), by Markstein's correction step (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): q = RN(x rc); the remainder e = x - s q is exact in one
+// FMA; q' = RN(q + e rc). The sign is taken from x, so a quotient that
+// underflows to zero keeps the sign of the exact one. The quantizers only
+// divide a bf16 value x by a scale s = max(RN(amax/448), 1/(448*512)) with
+// |x| <= amax; on that whole domain (every bf16 x, every bf16 amax) the
+// result is bit-identical to a correctly rounded division, which
+// r4_check_quotients verifies on the device.
+__device__ __forceinline__ float div_by_scale(float x, float s, float rc) {
+  const float q = __fmul_rn(x, rc);
+  const float e = __fmaf_rn(-s, q, x);
+  return copysignf(__fmaf_rn(e, rc, q), x);
+}
+
+// 8 bf16 -> 8 e4m3 codes (element i in byte i), each x/s correctly rounded;
+// rc = __frcp_rn(sc).
+__device__ __forceinline__ uint2 quant8(const uint4 &v, float sc, float rc) {
   uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t b[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    b[2 * i] = e4m3_of(__fdiv_rn(bf16lo(w[i]), sc));
-    b[2 * i + 1] = e4m3_of(__fdiv_rn(bf16hi(w[i]), sc));
+    b[2 * i] = e4m3_of(div_by_scale(bf16lo(w[i]), sc, rc));
+    b[2 * i + 1] = e4m3_of(div_by_scale(bf16hi(w[i]), sc, rc));
   }
   uint2 r;
   r.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);

@@ -126,6 +126,7 @@ inline size_t fp8_packed_bytes(int64_t N, int64_t K) {
 cudaError_t launch_add_rmsnorm_quant(const uint16_t *y, const uint16_t *res, const uint16_t *w, float eps, int64_t M,
                                      int64_t K, uint16_t *ro, uint8_t *q, float *s, cudaStream_t st);
 cudaError_t launch_silu_mul_quant(const uint16_t *gu, int64_t M, int64_t N, uint8_t *q, float *s, cudaStream_t st);
+cudaError_t launch_check_quotients(unsigned long long *count, float *example, cudaStream_t st);
 cudaError_t launch_quant_act(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int64_t group, uint8_t *q,
                              float *s, cudaStream_t st);
 cudaError_t launch_quant_mxfp4_weight(const float *w, int64_t N, int64_t K, uint8_t *packed, uint8_t *scale,

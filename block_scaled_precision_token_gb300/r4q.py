@@ -54,6 +54,7 @@ _SIGS = {
     "r4_gemm_w4a8_mxfp4_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P, _I64, _P], _I),
     "r4_add_rmsnorm_quant_fp8": ([_P, _P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P, _P], _I),
     "r4_silu_mul_quant_fp8": ([_P, _I64, _I64, _P, _P, _P], _I),
+    "r4_check_quotients": ([_P, _P, _P], _I),
 }
 
 
@@ -220,6 +221,11 @@ def r4_add_rmsnorm_quant_fp8(y, residual, weight, eps, M, K, residual_out, q, s,
     _check(lib().r4_add_rmsnorm_quant_fp8(_ptr(y), _ptr(residual), _ptr(weight), float(eps), M, K,
                                           _ptr(residual_out), _ptr(q), _ptr(s), _stream(stream)),
            "r4_add_rmsnorm_quant_fp8")
+
+
+def r4_check_quotients(count, example, stream=None):
+    _need(count, torch.int64, "count"); _need(example, torch.float32, "example")
+    _check(lib().r4_check_quotients(_ptr(count), _ptr(example), _stream(stream)), "r4_check_quotients")
 
 
 def r4_silu_mul_quant_fp8(gu, M, N, q, s, stream=None):

@@ -89,6 +89,22 @@ int r4_quant_fp8_per_token(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                            int64_t group, uint8_t *q, float *s, r4_stream_t stream);
 
 /*
+ * r4_check_quotients -- device self-check of the quotient x / s that the
+ * activation quantizers compute (a reciprocal and one FMA correction instead
+ * of a full division): over every finite bf16 amax, the scale
+ * s = max(amax/448, 1/(448*512)) the rule derives from it, and every bf16 x
+ * with |x| <= amax (both signs), compares the quotient with a correctly
+ * rounded fp32 division.
+ *   count    device, 4 x uint64, zeroed by the call (stream-ordered), 8-byte
+ *            aligned: [0] = pairs whose e4m3 codes differ (must be 0);
+ *            [1] = internal; [2] = pairs whose fp32 quotients differ in any
+ *            bit; [3] = fp32 bit pattern of the largest |x/s| among those.
+ *   example  device, 2 x fp32: (x, s) of one pair with differing codes, if any.
+ * Asynchronous on `stream`; ~1.07e9 pairs, about a millisecond on GB300.
+ */
+int r4_check_quotients(unsigned long long *count, float *example, r4_stream_t stream);
+
+/*
  * r4_add_rmsnorm_quant_fp8 -- residual add + Gemma RMS norm + per-token e4m3
  * quantization in one launch: the single-rank epilogue of
  * "radiance_arnq.py" (module docstring; ar_add_rms_quant):

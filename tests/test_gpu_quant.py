@@ -80,6 +80,25 @@ def test_row_split_option_checks(r4q):
         r4q.r4_set_option(11, 16)
 
 
+def test_quotient_correctly_rounded_on_whole_domain(r4q):
+    """The quantizers divide by the scale with a reciprocal and one FMA
+    correction. For every finite bf16 amax, the scale the rule derives from
+    it, and every bf16 x with |x| <= amax (both signs), the quotient must equal
+    a correctly rounded fp32 division in its e4m3 code (~1.07e9 pairs). The
+    fp32 quotients themselves may differ only where the remainder underflows
+    (x within a few ulps of the fp32 normal range), far below the smallest
+    e4m3 code 2^-9."""
+    count = torch.zeros(4, dtype=torch.int64, device="cuda")
+    ex = torch.zeros(2, dtype=torch.float32, device="cuda")
+    r4q.r4_check_quotients(count, ex)
+    torch.cuda.synchronize()
+    check_device_error(r4q)
+    n_code, n_bits, worst_bits = (int(v) for v in count[[0, 2, 3]].cpu())
+    assert n_code == 0, f"{n_code} (x, s) pairs give other codes, e.g. x={ex[0].item()!r} s={ex[1].item()!r}"
+    worst = np.array([worst_bits], dtype=np.uint32).view(np.float32)[0]
+    assert worst < 2.0 ** -20, f"{n_bits} quotients differ, the largest {worst!r}"
+
+
 def test_special_rows_and_row_stride(r4q):
     M, K, ld = 6, 1024, 1040
     base = _x(M, ld, synth.CFG_DECODE, False, seed=77).float()
