@@ -67,6 +67,19 @@ int row_split(int64_t M, int64_t K, RowKind kind) {
   return c;
 }
 
+int row_threads(RowKind kind, int64_t M, int64_t vecs) {
+  if (options().row_threads > 0) return options().row_threads;
+  // Fitted on GB300 (graph-timed launches): for rows of up to 768 vectors
+  // of 8 (K <= 6144) a 128-thread block with more vectors per thread keeps
+  // more rows resident per SM -- per-token quant M=8192, K=5120: 30.9 ->
+  // 24.3 us; the norm producer gains only with many rows (M=8192: 67.6 ->
+  // 63.1 us; M=64: 3.8 -> 4.6 us, so it keeps 256 below 2 rows per SM); the
+  // SiLU producer is issue-bound and loses (M=2048: 72.5 -> 86.1 us).
+  if (vecs > 768 || kind == RowKind::kSilu) return 256;
+  if (kind == RowKind::kNorm && M < 2 * static_cast<int64_t>(device_sm_count())) return 256;
+  return 128;
+}
+
 int *device_error_word() {
   const int d = current_device();
   if (g_err_ptr[d] == nullptr) {
@@ -166,6 +179,10 @@ int r4_set_option(int key, int64_t value) {
     case 6: options().cluster_split = value ? 1 : 0; return R4_OK;
     case 9: options().fp8_stage_scales = value ? 1 : 0; return R4_OK;
     case 10: options().inject_stall = value ? 1 : 0; return R4_OK;
+    case 13:
+      if (value != 0 && value != 64 && value != 128 && value != 256) return R4_ERR_INVALID_ARG;
+      options().row_threads = static_cast<int>(value);
+      return R4_OK;
     case 11:
       if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return R4_ERR_INVALID_ARG;
       options().row_split = static_cast<int>(value);

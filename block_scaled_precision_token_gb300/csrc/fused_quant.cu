@@ -188,10 +188,14 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const uint16_t
   if (C > 1) cluster_wait();
 }
 
-int threads_for(int64_t K) {
+int threads_for(int64_t K, RowKind kind, int64_t M) {
   const int64_t vecs = K / 8;
-  int t = static_cast<int>(vecs < kThreads ? ((vecs + 31) / 32) * 32 : kThreads);
-  return t < 32 ? 32 : t;
+  const int cap = row_threads(kind, M, vecs);
+  int t = static_cast<int>(vecs < cap ? ((vecs + 31) / 32) * 32 : cap);
+  if (t < 32) t = 32;
+  if (ceil_div(vecs, static_cast<int64_t>(t)) > 12)   // at most 12 vectors per thread: widen a capped block
+    t = static_cast<int>(ceil_div(ceil_div(vecs, int64_t{12}), int64_t{32}) * 32);
+  return t;
 }
 
 // Row split for a row of K columns: CTAs per row, columns per CTA, threads
@@ -204,7 +208,7 @@ RowSplit split_row(int64_t M, int64_t K, RowKind kind) {
   int C = row_split(M, K, kind);
   if (M * C > (int64_t{1} << 30)) C = 1;
   const int64_t cols = ceil_div(ceil_div(K, static_cast<int64_t>(C)), int64_t{8}) * 8;
-  const int t = threads_for(cols);
+  const int t = threads_for(cols, kind, M);
   return {C, static_cast<int>(cols), t, ceil_div(cols / 8, static_cast<int64_t>(t))};
 }
 
@@ -228,8 +232,8 @@ cudaError_t launch_add_rmsnorm_quant(const uint16_t *y, const uint16_t *res, con
     set_last_kernel("add_rmsnorm_quant_kernel<" #V ">");                                                     \
   }
   const int64_t per = rs.per;
-  if (per <= 1) R4_ARQ(1) else if (per <= 2) R4_ARQ(2) else if (per <= 4) R4_ARQ(4) else if (per <= 9) R4_ARQ(9)
-  else R4_ARQ(12)
+  if (per <= 1) R4_ARQ(1) else if (per <= 2) R4_ARQ(2) else if (per <= 4) R4_ARQ(4) else if (per <= 6) R4_ARQ(6)
+  else if (per <= 9) R4_ARQ(9) else R4_ARQ(12)
 #undef R4_ARQ
   return cudaGetLastError();
 }
@@ -248,8 +252,8 @@ cudaError_t launch_silu_mul_quant(const uint16_t *gu, int64_t M, int64_t N, uint
     set_last_kernel("silu_mul_quant_kernel<" #V ">");                                                        \
   }
   const int64_t per = rs.per;
-  if (per <= 1) R4_SMQ(1) else if (per <= 2) R4_SMQ(2) else if (per <= 4) R4_SMQ(4) else if (per <= 9) R4_SMQ(9)
-  else R4_SMQ(12)
+  if (per <= 1) R4_SMQ(1) else if (per <= 2) R4_SMQ(2) else if (per <= 4) R4_SMQ(4) else if (per <= 6) R4_SMQ(6)
+  else if (per <= 9) R4_SMQ(9) else R4_SMQ(12)
 #undef R4_SMQ
   return cudaGetLastError();
 }

@@ -13,6 +13,8 @@
 // short batch spreads each row over a thread-block cluster whose CTAs agree
 // on the row maximum through distributed shared memory.
 
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
@@ -257,14 +259,19 @@ cudaError_t launch_quant_act(const uint16_t *x, int64_t M, int64_t K, int64_t ld
   const int64_t align = per_token ? 8 : 128;
   int64_t cols = ceil_div(ceil_div(K, static_cast<int64_t>(C)), align) * align;
   int64_t vecs = cols / 8;
-  int threads = static_cast<int>(vecs < 256 ? ((vecs + 31) / 32) * 32 : 256);
+  const int cap = row_threads(RowKind::kQuant, M, vecs);
+  int threads = static_cast<int>(vecs < cap ? ((vecs + 31) / 32) * 32 : cap);
   if (threads < 32) threads = 32;
   int64_t per = ceil_div(vecs, threads);
-  if (per > 9 && C > 1) {   // the row does not fit in registers even when split: two-pass kernel
+  if (per > 12 && threads < 256) {   // a capped block too small for the row: widen it first
+    threads = static_cast<int>(std::min<int64_t>(256, ceil_div(ceil_div(vecs, int64_t{12}), int64_t{32}) * 32));
+    per = ceil_div(vecs, threads);
+  }
+  if (per > 12 && C > 1) {   // the row does not fit in registers even when split: two-pass kernel
     C = 1;
     cols = K;
     threads = 256;
-    per = 10;
+    per = 13;
   }
   const dim3 grid(static_cast<unsigned>(M * C));
   const int g = static_cast<int>(group), k = static_cast<int>(K), cl = static_cast<int>(cols);
@@ -277,7 +284,8 @@ cudaError_t launch_quant_act(const uint16_t *x, int64_t M, int64_t K, int64_t ld
     if (e != cudaSuccess) return e;                                                                          \
     set_last_kernel("quant_act_kernel<" #V ">");                                                             \
   }
-  if (per <= 1) R4_QA(1) else if (per <= 2) R4_QA(2) else if (per <= 4) R4_QA(4) else if (per <= 9) R4_QA(9)
+  if (per <= 1) R4_QA(1) else if (per <= 2) R4_QA(2) else if (per <= 4) R4_QA(4) else if (per <= 6) R4_QA(6)
+  else if (per <= 9) R4_QA(9) else if (per <= 12) R4_QA(12)
   else {
     const cudaError_t e = launch_pdl(quant_act_long_kernel, grid, dim3(threads), 0, st, x, k, ldx, g, q, s);
     if (e != cudaSuccess) return e;

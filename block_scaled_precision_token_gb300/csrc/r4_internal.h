@@ -37,6 +37,7 @@ struct Options {
   int l2_prefetch = 0;      // W4A8: bulk L2 prefetch of the CTA's whole weight range at kernel start
   int cluster_split = 1;    // W4A8 decode tiles: split-K across a thread-block cluster when possible
   int row_split = 0;        // row-wise quantizers: CTAs per row (0 = automatic, else 1/2/4/8)
+  int row_threads = 0;      // row-wise quantizers: threads per CTA at most (0 = automatic, else 64/128/256)
 };
 Options &options();
 
@@ -45,6 +46,8 @@ Options &options();
 // than M SMs take part.
 enum class RowKind { kQuant, kNorm, kSilu };   // per-token quant, add+RMS norm+quant, SiLU-and-mul+quant
 int row_split(int64_t M, int64_t K, RowKind kind);
+// Threads per CTA at most for a row slice of `vecs` 16-byte vectors.
+int row_threads(RowKind kind, int64_t M, int64_t vecs);
 
 // Launch `kernel` on `st`; with options().pdl the launch allows programmatic
 // dependent launch (the kernel may start before its predecessor in the

@@ -289,7 +289,12 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * key 11: CTAs that share one row in the row-wise activation quantizers
  * (per-token, group-128 and the two fused producers): 0 (default) chooses
  * automatically (short batches spread each row over a cluster of up to 8
- * CTAs), 1/2/4/8 force it; other values return R4_ERR_INVALID_ARG.
+ * CTAs), 1/2/4/8 force it; other values return R4_ERR_INVALID_ARG;
+ * key 13: threads per CTA at most in the same quantizers: 0 (default)
+ * chooses (128 for slices of up to 6144 columns where that gains, else
+ * 256), 64/128/256 cap it (a row that would need more than 12 vectors of 8
+ * per thread widens the block again); other values return
+ * R4_ERR_INVALID_ARG.
  */
 int r4_set_option(int key, int64_t value);
 

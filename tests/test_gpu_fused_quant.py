@@ -163,6 +163,32 @@ def test_row_split(r4q, C, M, K):
     _check_quant(q2, s2, np.minimum(h1, h2), np.maximum(h1, h2), f"silu_mul_quant C={C} M={M} N={K}")
 
 
+@pytest.mark.parametrize("T", [64, 128])
+@pytest.mark.parametrize("M,K", [(300, 5120), (3, 24576), (4, 1000)])
+def test_block_size_cap(r4q, T, M, K):
+    """Option 13 caps the threads per CTA of both producers."""
+    y = _randn((M, K), M * 29 + K + T, 1.0)
+    res = _randn((M, K), M * 37 + K + T, 2.0)
+    w = _randn((K,), K + T, 0.1)
+    g = _randn((M, K), M * 41 + K + T, 3.0)
+    u = _randn((M, K), M * 43 + K + T, 1.0)
+    r4q.r4_set_option(13, T)
+    try:
+        q, s, ro = _run_arq(r4q, y, res, w, 1e-6)
+        q2, s2 = r4q.silu_mul_quant(torch.cat([g, u], dim=1).cuda())
+        check_device_error(r4q)
+    finally:
+        r4q.r4_set_option(13, 0)
+    r, h64 = U.add_rmsnorm(y.float().numpy(), res.float().numpy(), w.float().numpy(), 1e-6)
+    assert np.array_equal(bf16_to_np(ro), r)
+    h_lo, h_hi = _candidates(h64)
+    _check_quant(q, s, h_lo, h_hi, f"add_rmsnorm_quant T={T} M={M} K={K}")
+    g64, u64 = g.double().numpy(), u.double().numpy()
+    a_lo, a_hi = _candidates(g64 / (1.0 + np.exp(-g64)))
+    h1, h2 = F.bf16_round(a_lo * u64), F.bf16_round(a_hi * u64)
+    _check_quant(q2, s2, np.minimum(h1, h2), np.maximum(h1, h2), f"silu_mul_quant T={T} M={M} N={K}")
+
+
 def test_fused_quant_argument_checks(r4q):
     y = torch.zeros((2, 12), dtype=torch.bfloat16, device="cuda")
     w = torch.zeros((12,), dtype=torch.bfloat16, device="cuda")

@@ -73,11 +73,30 @@ def test_row_split_bit_exact(r4q, C, M, K, ld, group):
     assert np.array_equal(np_u8(q), q_ref)
 
 
+@pytest.mark.parametrize("T", [64, 128])
+@pytest.mark.parametrize("M,K,group", [(300, 5120, None), (7, 24576, None), (33, 6144, 128), (5, 1000, None)])
+def test_block_size_cap_bit_exact(r4q, T, M, K, group):
+    """Option 13 caps the threads per CTA (more vectors per thread; a row
+    too long for 12 vectors per thread widens the block again)."""
+    x = _x(M, K, synth.CFG_DECODE, True, seed=M * 31 + K + T)
+    q_ref, s_ref = Q.quant_act(x.float().numpy(), group=group)
+    r4q.r4_set_option(13, T)
+    try:
+        q, s = r4q.quant_fp8(x.cuda(), group=group)
+        check_device_error(r4q)
+    finally:
+        r4q.r4_set_option(13, 0)
+    assert np.array_equal(np_f32(s), s_ref)
+    assert np.array_equal(np_u8(q), q_ref)
+
+
 def test_row_split_option_checks(r4q):
     with pytest.raises(r4q.R4Error):
         r4q.r4_set_option(11, 3)
     with pytest.raises(r4q.R4Error):
         r4q.r4_set_option(11, 16)
+    with pytest.raises(r4q.R4Error):
+        r4q.r4_set_option(13, 96)
 
 
 def test_quotient_correctly_rounded_on_whole_domain(r4q):
