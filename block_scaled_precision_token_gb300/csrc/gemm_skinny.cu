@@ -14,10 +14,12 @@
 //    HBM-bound (about 2 flops per weight byte at M = 8), not tensor-bound, so
 //    the warp-level MMA is sufficient; tcgen05 setup (TMEM allocation,
 //    descriptor pipeline) would only add latency here.
-//  * reduction: 4 warps -> shared memory -> one CTA partial; the cluster's
-//    partials are written into rank 0's shared memory through distributed
-//    shared memory, and rank 0 sums them in rank order (deterministic), rounds
-//    to bf16 and stores. No global workspace, no atomics, no second kernel.
+//  * reduction: 4 warps -> shared memory -> one CTA partial in the CTA's own
+//    shared memory; after one cluster barrier every CTA sums a 1/KS share of
+//    the tile's outputs over the cluster's partials, read in rank order
+//    through distributed shared memory (deterministic), rounds to bf16 and
+//    stores (a reduce-scatter). No global workspace, no atomics, no second
+//    kernel.
 
 #include <cuda_bf16.h>
 
@@ -44,7 +46,7 @@ struct Smem {
   // reductions walk rows fastest, and an odd stride keeps them conflict-free
   static constexpr int kRS = kMpad + 1;
   static constexpr size_t kRed = 4 * kRows * kRS * 4;
-  static constexpr size_t kCluster = kMaxKS * kRows * kRS * 4;
+  static constexpr size_t kCluster = kRows * kRS * 4;   // this CTA's partial, read by the cluster
   static constexpr size_t kBytes = kW + kX + kRed + kCluster;
 };
 
@@ -94,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint16_t *sW = reinterpret_cast<uint16_t *>(smem);
   uint16_t *sX = reinterpret_cast<uint16_t *>(smem + S::kW);
   float *sRed = reinterpret_cast<float *>(smem + S::kW + S::kX);              // [4][16][kRS]
-  float *sCl = reinterpret_cast<float *>(smem + S::kW + S::kX + S::kRed);     // [KS][16][kRS]
+  float *sCl = reinterpret_cast<float *>(smem + S::kW + S::kX + S::kRed);     // [16][kRS]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
@@ -103,8 +105,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kbeg = static_cast<int>(rank) * chunks_per_cta * 256;
   const int kend = min(K, kbeg + chunks_per_cta * 256);
 
-  // Let the cluster's CTAs start; the matching wait precedes the DSMEM writes.
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   float acc[2 * NG2][4];
@@ -112,10 +112,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int g = 0; g < 2 * NG2; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
 
   for (int kk = kbeg; kk < kend; kk += kIter) {
-    const int klen = min(kIter, kend - kk);      // multiple of 256
-    const int cpr = klen / 8;                     // 16-byte chunks per row
+    const int klen = min(kIter, kend - kk);      // == kIter: K is a multiple of 256
+    constexpr int cpr = kIter / 8;                // 16-byte chunks per row
     for (int i = tid; i < kRows * cpr; i += kThreads) {
-      const int r = i / cpr, ch = i - r * cpr;
+      const int r = i / cpr, ch = i % cpr;
       uint16_t *dst = sW + r * kStride + ch * 8;
       if (n0 + r < N)
         cp_async16(dst, w + static_cast<size_t>(n0 + r) * K + kk + ch * 8);
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The weight is independent of the preceding kernel; x is not.
     if (kk == kbeg) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int i = tid; i < kMpad * cpr; i += kThreads) {
-      const int r = i / cpr, ch = i - r * cpr;
+      const int r = i / cpr, ch = i % cpr;
       uint16_t *dst = sX + r * kStride + ch * 8;
       if (r < M)
         cp_async16(dst, x + static_cast<size_t>(r) * K + kk + ch * 8);
@@ -163,26 +163,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  const uint32_t dst_base = map_rank(smem_addr(sCl + rank * kRows * kRS), 0);
+  // this CTA's partial (sum of the 4 warps) in its own shared memory
   for (int i = tid; i < kRows * kMpad; i += kThreads) {
     const int r = i % kRows, t = i / kRows;
-    const float v = sRed[r * kRS + t] + sRed[kRows * kRS + r * kRS + t] + sRed[2 * kRows * kRS + r * kRS + t] +
-                    sRed[3 * kRows * kRS + r * kRS + t];
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst_base + 4u * (r * kRS + t)), "f"(v) : "memory");
+    sCl[r * kRS + t] = sRed[r * kRS + t] + sRed[kRows * kRS + r * kRS + t] +
+                       sRed[2 * kRows * kRS + r * kRS + t] + sRed[3 * kRows * kRS + r * kRS + t];
   }
+  // Every CTA of the cluster has written its partial (release / acquire).
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-  if (rank == 0) {
-    for (int i = tid; i < kRows * kMpad; i += kThreads) {
-      const int r = i % kRows, t = i / kRows;
-      float v = 0.f;
-      for (int s = 0; s < KS; ++s) v += sCl[s * kRows * kRS + r * kRS + t];
-      if (t < M && n0 + r < N) {
-        __nv_bfloat16 h = __float2bfloat16_rn(v);
-        c[static_cast<size_t>(t) * ldc + n0 + r] = *reinterpret_cast<uint16_t *>(&h);
-      }
+  // Reduce-scatter: CTA `rank` owns outputs e in [rank * per, rank * per + per)
+  // of the tile's 16 x kMpad (e = token * 16 + row: 16 consecutive outputs
+  // are one token's 16 consecutive columns of c).
+  const int total = kRows * kMpad;
+  const int per = (total + KS - 1) / KS;
+  const uint32_t my_part = smem_addr(sCl);
+  for (int e = static_cast<int>(rank) * per + tid; e < min(total, static_cast<int>(rank + 1) * per); e += kThreads) {
+    const int r = e % kRows, t = e / kRows;
+    const uint32_t off = 4u * static_cast<uint32_t>(r * kRS + t);
+    float v = 0.f;
+    for (int q = 0; q < KS; ++q) {
+      float pq;
+      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(pq) : "r"(map_rank(my_part + off, q)) : "memory");
+      v += pq;
+    }
+    if (t < M && n0 + r < N) {
+      __nv_bfloat16 h = __float2bfloat16_rn(v);
+      c[static_cast<size_t>(t) * ldc + n0 + r] = *reinterpret_cast<uint16_t *>(&h);
     }
   }
+  // No CTA leaves while another may still read its partial.
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 template <int NG2>
