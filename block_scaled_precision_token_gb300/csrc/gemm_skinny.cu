@@ -37,17 +37,17 @@ constexpr int kMaxKS = 8;
 // Shared memory sized for the token groups actually present: at 1 CTA per
 // SM a cluster of 8 fits only 15 times on GB300 (measured: the 16th of a
 // 256-row weight's clusters ran as a second wave); small CTAs pack 2-7 per SM.
-template <int NG2>
+template <int NG2, int NB>   // NB staging buffers: 2 when a CTA walks several K chunks
 struct Smem {
   static constexpr int kMpad = 16 * NG2;
-  static constexpr size_t kW = kRows * kStride * 2;
+  static constexpr size_t kW = kRows * kStride * 2;    // one buffer
   static constexpr size_t kX = kMpad * kStride * 2;
   // partial tiles [16 rows][kMpad tokens], rows kMpad + 1 floats apart: the
   // reductions walk rows fastest, and an odd stride keeps them conflict-free
   static constexpr int kRS = kMpad + 1;
   static constexpr size_t kRed = 4 * kRows * kRS * 4;
   static constexpr size_t kCluster = kRows * kRS * 4;   // this CTA's partial, read by the cluster
-  static constexpr size_t kBytes = kW + kX + kRed + kCluster;
+  static constexpr size_t kBytes = NB * (kW + kX) + kRed + kCluster;
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -85,18 +85,19 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
-template <int NG2>  // token groups of 16 (Mpad = 16 * NG2)
+template <int NG2, int NB>  // token groups of 16 (Mpad = 16 * NG2); NB staging buffers
 __global__ void __launch_bounds__(kThreads, 1)
     skinny_bf16_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w, int M, int N, int K,
                        int chunks_per_cta, uint16_t *__restrict__ c, int ldc) {
-  using S = Smem<NG2>;
+  using S = Smem<NG2, NB>;
   constexpr int kMpad = S::kMpad;
   constexpr int kRS = S::kRS;
   extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t *sW = reinterpret_cast<uint16_t *>(smem);
-  uint16_t *sX = reinterpret_cast<uint16_t *>(smem + S::kW);
-  float *sRed = reinterpret_cast<float *>(smem + S::kW + S::kX);              // [4][16][kRS]
-  float *sCl = reinterpret_cast<float *>(smem + S::kW + S::kX + S::kRed);     // [16][kRS]
+  // NB staging buffers (double-buffered K loop when NB == 2), then the partial tiles
+  uint16_t *sW0 = reinterpret_cast<uint16_t *>(smem);
+  uint16_t *sX0 = reinterpret_cast<uint16_t *>(smem + S::kW);
+  float *sRed = reinterpret_cast<float *>(smem + NB * (S::kW + S::kX));              // [4][16][kRS]
+  float *sCl = reinterpret_cast<float *>(smem + NB * (S::kW + S::kX) + S::kRed);     // [16][kRS]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
@@ -107,13 +108,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  float acc[2 * NG2][4];
+  // Warp roles: NGW token-group slots x KP k-phases (4 warps). Warp w
+  // multiplies token group w % NGW over the k-steps of phase w / NGW, so with
+  // 64 tokens each warp owns one group over all of K and no two warps add
+  // into the same outputs.
+  constexpr int NGW = NG2 == 3 ? 4 : NG2;   // with 3 groups the 4th warp only stages and reduces
+  constexpr int KP = 4 / NGW;
+  const int g2w = warp % NGW, kp = warp / NGW;
+  float acc[2][4];
 #pragma unroll
-  for (int g = 0; g < 2 * NG2; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
+  for (int g = 0; g < 2; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
 
-  for (int kk = kbeg; kk < kend; kk += kIter) {
-    const int klen = min(kIter, kend - kk);      // == kIter: K is a multiple of 256
-    constexpr int cpr = kIter / 8;                // 16-byte chunks per row
+  // Stage chunk kk (kIter columns of the 16 weight rows and of the tokens)
+  // into buffer b: one cp.async group.
+  constexpr int cpr = kIter / 8;                // 16-byte chunks per row
+  auto stage = [&](int kk, int b) {
+    uint16_t *sW = sW0 + b * ((S::kW + S::kX) / 2);
+    uint16_t *sX = sX0 + b * ((S::kW + S::kX) / 2);
     for (int i = tid; i < kRows * cpr; i += kThreads) {
       const int r = i / cpr, ch = i % cpr;
       uint16_t *dst = sW + r * kStride + ch * 8;
@@ -132,42 +143,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
     }
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+
+  if (kbeg < kend) stage(kbeg, 0);
+  for (int kk = kbeg, it = 0; kk < kend; kk += kIter, ++it) {
+    const int klen = kIter;                       // K is a multiple of 256
+    // prefetch the next chunk into the other buffer, then wait for this one
+    if (NB == 2 && kk + kIter < kend) {
+      stage(kk + kIter, (it + 1) & 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
     __syncthreads();
+    const int cur = NB == 2 ? (it & 1) : 0;
+    const uint16_t *sW = sW0 + cur * ((S::kW + S::kX) / 2);
+    const uint16_t *sX = sX0 + cur * ((S::kW + S::kX) / 2);
     const int nsteps = klen / 16;
-    for (int ks = warp; ks < nsteps; ks += 4) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(smem_addr(sW + (lane & 15) * kStride + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
-#pragma unroll
-      for (int g2 = 0; g2 < NG2; ++g2) {
-        uint32_t b0, b1, b2, b3;
-        const int tok = g2 * 16 + (lane >> 4) * 8 + (lane & 7);
+    if (g2w < NG2) {
+      for (int ks = kp; ks < nsteps; ks += KP) {
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+        ldsm_x4(smem_addr(sW + (lane & 15) * kStride + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+        const int tok = g2w * 16 + (lane >> 4) * 8 + (lane & 7);
         ldsm_x4(smem_addr(sX + tok * kStride + ks * 16 + ((lane >> 3) & 1) * 8), b0, b1, b2, b3);
-        mma_bf16(acc[2 * g2], a0, a1, a2, a3, b0, b1);
-        mma_bf16(acc[2 * g2 + 1], a0, a1, a2, a3, b2, b3);
+        mma_bf16(acc[0], a0, a1, a2, a3, b0, b1);
+        mma_bf16(acc[1], a0, a1, a2, a3, b2, b3);
       }
     }
     __syncthreads();
+    if (NB == 1 && kk + kIter < kend) stage(kk + kIter, 0);   // single buffer: refill after use
   }
 
-  // warp partials -> shared memory (D fragment: rows lane/4 and lane/4 + 8,
-  // token columns 8g + 2(lane%4) + {0,1})
-  float *red = sRed + warp * kRows * kRS;
+  // warp partials -> shared memory, one [16][kMpad] tile per k-phase (D
+  // fragment: rows lane/4 and lane/4 + 8, token columns 16 g2w + 8g +
+  // 2(lane%4) + {0,1})
+  if (g2w < NG2) {
+    float *red = sRed + kp * kRows * kRS;
 #pragma unroll
-  for (int g = 0; g < 2 * NG2; ++g) {
-    const int r = lane >> 2, t = 8 * g + 2 * (lane & 3);
-    red[r * kRS + t] = acc[g][0];
-    red[r * kRS + t + 1] = acc[g][1];
-    red[(r + 8) * kRS + t] = acc[g][2];
-    red[(r + 8) * kRS + t + 1] = acc[g][3];
+    for (int g = 0; g < 2; ++g) {
+      const int r = lane >> 2, t = 16 * g2w + 8 * g + 2 * (lane & 3);
+      red[r * kRS + t] = acc[g][0];
+      red[r * kRS + t + 1] = acc[g][1];
+      red[(r + 8) * kRS + t] = acc[g][2];
+      red[(r + 8) * kRS + t + 1] = acc[g][3];
+    }
   }
   __syncthreads();
 
-  // this CTA's partial (sum of the 4 warps) in its own shared memory
+  // this CTA's partial (sum over the k-phases) in its own shared memory
   for (int i = tid; i < kRows * kMpad; i += kThreads) {
     const int r = i % kRows, t = i / kRows;
-    sCl[r * kRS + t] = sRed[r * kRS + t] + sRed[kRows * kRS + r * kRS + t] +
-                       sRed[2 * kRows * kRS + r * kRS + t] + sRed[3 * kRows * kRS + r * kRS + t];
+    float v = sRed[r * kRS + t];
+#pragma unroll
+    for (int p = 1; p < KP; ++p) v += sRed[p * kRows * kRS + r * kRS + t];
+    sCl[r * kRS + t] = v;
   }
   // Every CTA of the cluster has written its partial (release / acquire).
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -180,12 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int e = static_cast<int>(rank) * per + tid; e < min(total, static_cast<int>(rank + 1) * per); e += kThreads) {
     const int r = e % kRows, t = e / kRows;
     const uint32_t off = 4u * static_cast<uint32_t>(r * kRS + t);
+    float pq[kMaxKS];   // all loads in flight before the (rank-ordered) sum
+#pragma unroll
+    for (int q = 0; q < kMaxKS; ++q)
+      if (q < KS) asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(pq[q]) : "r"(map_rank(my_part + off, q)));
     float v = 0.f;
-    for (int q = 0; q < KS; ++q) {
-      float pq;
-      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(pq) : "r"(map_rank(my_part + off, q)) : "memory");
-      v += pq;
-    }
+#pragma unroll
+    for (int q = 0; q < kMaxKS; ++q)
+      if (q < KS) v += pq[q];
     if (t < M && n0 + r < N) {
       __nv_bfloat16 h = __float2bfloat16_rn(v);
       c[static_cast<size_t>(t) * ldc + n0 + r] = *reinterpret_cast<uint16_t *>(&h);
@@ -195,14 +227,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <int NG2>
+template <int NG2, int NB>
 cudaError_t launch_ng(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N, int64_t K, uint16_t *c,
                       int64_t ldc, cudaStream_t st) {
   const int chunks = static_cast<int>(K / 256);
   const int ks = chunks < kMaxKS ? chunks : kMaxKS;
   const int cpc = (chunks + ks - 1) / ks;
-  auto kern = skinny_bf16_kernel<NG2>;
-  constexpr size_t kSmemBytes = Smem<NG2>::kBytes;
+  auto kern = skinny_bf16_kernel<NG2, NB>;
+  constexpr size_t kSmemBytes = Smem<NG2, NB>::kBytes;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -230,13 +262,23 @@ cudaError_t launch_ng(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N
 
 cudaError_t launch_gemm_skinny(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N, int64_t K, uint16_t *c,
                                int64_t ldc, cudaStream_t st) {
+  // A CTA that walks several 256-wide K chunks double-buffers them. One that
+  // owns a single chunk keeps the smaller single-buffer footprint, except at
+  // 64 tokens, where the larger footprint spreads the CTAs over more SMs
+  // (measured, [256, 2048], one chunk per CTA: M <= 16 3.0 vs 3.2 us and
+  // M = 32 4.3 vs 4.6 us with one buffer; M = 64 5.9 vs 6.6 us with two).
   const int64_t ng2 = ceil_div(M, 16);
+  const bool multi = ceil_div(K / 256, static_cast<int64_t>(skinny::kMaxKS)) > 1 || ng2 == 4;
+#define R4_SK(G)                                                                               \
+  return multi ? skinny::launch_ng<G, 2>(x, w, M, N, K, c, ldc, st)                           \
+               : skinny::launch_ng<G, 1>(x, w, M, N, K, c, ldc, st);
   switch (ng2) {
-    case 1: return skinny::launch_ng<1>(x, w, M, N, K, c, ldc, st);
-    case 2: return skinny::launch_ng<2>(x, w, M, N, K, c, ldc, st);
-    case 3: return skinny::launch_ng<3>(x, w, M, N, K, c, ldc, st);
-    default: return skinny::launch_ng<4>(x, w, M, N, K, c, ldc, st);
+    case 1: R4_SK(1)
+    case 2: R4_SK(2)
+    case 3: R4_SK(3)
+    default: R4_SK(4)
   }
+#undef R4_SK
 }
 
 }  // namespace r4
