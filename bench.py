@@ -510,8 +510,49 @@ def run_ours(args, rank, world, local_rank):
         off += M * N
     h2d_bytes = sum(v.numel() * v.element_size() for v in xs_host.values())
     d2h_bytes = chost.numel() * chost.element_size()
+    hview, off = {}, 0
+    for (M, N, K) in sweep.combos:
+        hview[(M, N, K)] = chost[off:off + M * N]
+        off += M * N
+    # Copies ride their own streams so that they overlap the kernels: each
+    # activation buffer is copied in on a side stream and the first quant
+    # that reads it waits for that copy alone; each GEMM's output is copied
+    # out on a second side stream as soon as that GEMM ends, while the next
+    # shapes compute. The step ends when the last output has reached the host.
+    s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
 
     def e2e_step():
+        main = torch.cuda.current_stream()
+        s_in.wait_stream(main)
+        s_out.wait_stream(main)
+        ready = {}
+        with torch.cuda.stream(s_in):
+            for K in xdev:
+                xdev[K].copy_(xs_host[K], non_blocking=True)
+                ready[K] = torch.cuda.Event()
+                ready[K].record(s_in)
+        occ, waited = {}, set()
+        for (M, N, K) in sweep.combos:
+            i = occ.get((N, K), 0)
+            occ[(N, K)] = i + 1
+            if K not in waited:
+                main.wait_event(ready[K])
+                waited.add(K)
+            q, s, c = sweep.q[(M, K)], sweep.s[(M, K)], cview[(M, N, K)]
+            r4q.r4_quant_fp8_per_token(xdev[K][:M], M, K, K, K, q, s)
+            r4q.r4_gemm_w4a8_mxfp4(q, s, sweep.packed[(N, K)][i % sweep.copies], M, N, K, c, N, sweep.ws[(M, N, K)])
+            done = torch.cuda.Event()
+            done.record(main)
+            s_out.wait_event(done)
+            with torch.cuda.stream(s_out):
+                hview[(M, N, K)].copy_(c.reshape(-1), non_blocking=True)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
+
+    def e2e_step_eager():
+        # Issued from Python without a graph: one stream, copies in order
+        # (per-call events and stream switches would cost more host time
+        # than the overlap saves).
         for K in xdev:
             xdev[K].copy_(xs_host[K], non_blocking=True)
         occ = {}
@@ -539,7 +580,7 @@ def run_ours(args, rank, world, local_rank):
 
     ge2e = capture(e2e_step)
     e2e_ms = time_e2e(ge2e.replay)
-    e2e_eager_ms = time_e2e(e2e_step)
+    e2e_eager_ms = time_e2e(e2e_step_eager)
     del ge2e
     e2e_value, _ = aggregate([dist_max(e2e_ms / 1e3, world)], sweep.wbytes, world)
     e2e_eager_value, _ = aggregate([dist_max(e2e_eager_ms / 1e3, world)], sweep.wbytes, world)
@@ -564,8 +605,11 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "e2e": {"value": round(e2e_value / 1e9, 2), "unit": "GB/s (decode weight bytes)",
                 "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
-                "how": "step captured in a CUDA graph: 3 pinned H2D activation copies, 15 x (quant + GEMM) "
-                       "through the C ABI, 1 D2H copy of every output",
+                "how": "step captured in a CUDA graph: 3 pinned H2D activation copies on a side stream (each "
+                       "quant waits only for its own input), 15 x (quant + GEMM) through the C ABI, each output "
+                       "copied to pinned host memory on a second side stream as soon as its GEMM ends; the step "
+                       "ends when every output is on the host; eager_value: the same calls issued from "
+                       "Python on one stream, copies in order",
                 "eager_value": round(e2e_eager_value / 1e9, 2)},
     }
     if rank == 0:

@@ -223,7 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       c[static_cast<size_t>(t) * ldc + n0 + r] = *reinterpret_cast<uint16_t *>(&h);
     }
   }
-  // No CTA leaves while another may still read its partial.
+  // No CTA leaves while another may still read its partial. The arrive must
+  // be a release: it is what orders this CTA's remote loads (some of whose
+  // values are never used, for padded tokens) before the peers may exit. A
+  // relaxed arrive let a CTA leave under a peer's load still in flight.
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
