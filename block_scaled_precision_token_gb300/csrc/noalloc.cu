@@ -57,6 +57,10 @@ extern "C" int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, cons
   if (!q || !s || !packed || !c) return R4_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1 || ldc < N || M > (1 << 30) || N > (1 << 30)) return R4_ERR_INVALID_ARG;
   if (K % 32 || K < 128) return R4_ERR_UNSUPPORTED_SHAPE;
+  // the same alignment rules as r4_gemm_w4a8_mxfp4, checked before any device query
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(packed) % 256 ||
+      reinterpret_cast<uintptr_t>(s) % 4 || reinterpret_cast<uintptr_t>(c) % 2)
+    return R4_ERR_MISALIGNED;
   const GemmPlan pl = plan_w4a8(M, N, K, device_sm_count());
   if (pl.ws_bytes > kNoallocScratchBytes) return R4_ERR_WORKSPACE;   // beyond the static maximum
   void *ws = nullptr;

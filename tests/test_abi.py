@@ -82,6 +82,49 @@ def test_validation_rejects_before_launch(r4q):
     assert lib.r4_prepack_blockfp8(good, good, 256, 256, good, 100, S) == r4q.R4_ERR_WORKSPACE
 
 
+def test_validation_of_the_later_entry_points(r4q):
+    """Fused producers, the no-allocation GEMM and the quotient self-check
+    reject bad arguments on the host, before any device work."""
+    lib = r4q.lib()
+    P = ctypes.c_void_p
+    good = P(1 << 20)
+    odd8 = P((1 << 20) + 8)
+    odd4 = P((1 << 20) + 4)
+    S = P(0)
+    f = ctypes.c_float
+    arq = lib.r4_add_rmsnorm_quant_fp8
+    assert arq(None, good, good, f(1e-6), 8, 5120, good, good, good, S) == r4q.R4_ERR_INVALID_ARG
+    assert arq(good, good, good, f(1e-6), 0, 5120, good, good, good, S) == r4q.R4_ERR_INVALID_ARG
+    assert arq(good, good, good, f(-1.0), 8, 5120, good, good, good, S) == r4q.R4_ERR_INVALID_ARG
+    assert arq(good, good, good, f(float("nan")), 8, 5120, good, good, good, S) == r4q.R4_ERR_INVALID_ARG
+    assert arq(good, good, good, f(1e-6), 8, 5124, good, good, good, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert arq(good, good, good, f(1e-6), 8, 24584, good, good, good, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert arq(odd8, good, good, f(1e-6), 8, 5120, good, good, good, S) == r4q.R4_ERR_MISALIGNED
+    assert arq(good, good, good, f(1e-6), 8, 5120, good, odd4, good, S) == r4q.R4_ERR_MISALIGNED
+    smq = lib.r4_silu_mul_quant_fp8
+    assert smq(None, 8, 17408, good, good, S) == r4q.R4_ERR_INVALID_ARG
+    assert smq(good, 0, 17408, good, good, S) == r4q.R4_ERR_INVALID_ARG
+    assert smq(good, 8, 17412, good, good, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert smq(good, 8, 24584, good, good, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert smq(odd8, 8, 17408, good, good, S) == r4q.R4_ERR_MISALIGNED
+    na = lib.r4_gemm_w4a8_mxfp4_noalloc
+    assert na(good, good, None, 8, 256, 2048, good, 256, S) == r4q.R4_ERR_INVALID_ARG
+    assert na(good, good, good, 8, 256, 2048, good, 100, S) == r4q.R4_ERR_INVALID_ARG
+    assert na(good, good, good, 8, 256, 2000, good, 256, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert na(good, good, odd8, 8, 256, 2048, good, 256, S) == r4q.R4_ERR_MISALIGNED
+    assert na(odd8, good, good, 8, 256, 2048, good, 256, S) == r4q.R4_ERR_MISALIGNED
+    assert lib.r4_check_quotients(None, good, S) == r4q.R4_ERR_INVALID_ARG
+    assert lib.r4_check_quotients(odd4, good, S) == r4q.R4_ERR_MISALIGNED
+
+
+def test_row_kernel_options(r4q):
+    lib = r4q.lib()
+    for key, bad, ok in [(11, 3, 8), (11, 16, 1), (13, 96, 128), (13, 512, 64)]:
+        assert lib.r4_set_option(key, bad) == r4q.R4_ERR_INVALID_ARG
+        assert lib.r4_set_option(key, ok) == 0
+        assert lib.r4_set_option(key, 0) == 0
+
+
 def test_product_path_has_no_oracle_import():
     """The package must not import the oracle (or any CPU fallback)."""
     import ast
