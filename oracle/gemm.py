@@ -55,6 +55,36 @@ def gemm_w4a8(q, s, w_packed, w_scale, rows=None, chunk=1024, exact_check=False)
     return out, bf16_round(out)
 
 
+def gemm_w4a4(x_packed, x_scale, w_packed, w_scale, rows=None, chunk=1024, exact_check=False):
+    """W4A4 MXFP4 x MXFP4 (next step; oracle only):
+    C[m,n] = bf16( sum_k e2m1(x[m,k]) 2^(a[m,k/32]-127) * e2m1(w[n,k]) 2^(e[n,k/32]-127) ).
+
+    radiance_mxfp4.py: the W4A4 path the page's W4A8 kernel replaces (module
+    docstring; ``_debug_compare``). Both operands in checkpoint order (low
+    nibble = even k) with one ue8m0 scale per 32 K. e2m1 x e2m1 products carry
+    at most 4 significant bits, so the float64 sum is exact for the workloads'
+    scale ranges (``exact_check`` re-sums with K reversed).
+
+    Returns (c64 float64 [M, n], c_bf16 float64 [M, n]).
+    """
+    x_packed = np.asarray(x_packed, dtype=np.uint8)
+    M = x_packed.shape[0]
+    K = 2 * x_packed.shape[1]
+    A = e2m1_decode(unpack_e2m1(x_packed, K)) * np.repeat(ue8m0_decode(x_scale), 32, axis=1)
+    idx = np.arange(w_packed.shape[0]) if rows is None else np.asarray(rows)
+    out = np.empty((M, len(idx)), dtype=np.float64)
+    for a, b in _chunks(len(idx), chunk):
+        r = idx[a:b]
+        W = e2m1_decode(unpack_e2m1(w_packed[r], K)) * np.repeat(ue8m0_decode(w_scale[r]), 32, axis=1)
+        acc = A @ W.T
+        if exact_check:
+            acc_rev = A[:, ::-1] @ W[:, ::-1].T
+            if not np.array_equal(acc, acc_rev):
+                raise AssertionError("gemm_w4a4: float64 sum is not exact for these inputs")
+        out[:, a:b] = acc
+    return out, bf16_round(out)
+
+
 def gemm_blockfp8(q, As, w, Ws, rows=None, chunk=1024, exact_check=False):
     """Block-FP8 W8A8: C[m,n] = bf16( sum_kb As[m,kb] Ws[n/128,kb] sum_{k in kb} e4m3(q[m,k]) e4m3(w[n,k]) ).
 

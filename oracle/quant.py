@@ -79,6 +79,22 @@ def quant_mxfp4_ocp(w):
     return pack_e2m1(codes), code.astype(np.uint8)
 
 
+def quant_act_mxfp4(x):
+    """MXFP4 activations for the W4A4 variant (next step; oracle only).
+
+    radiance_mxfp4.py names the W4A4 path only as the library fallback that
+    quantizes activations to MXFP4 (module docstring; ``_debug_compare``,
+    "aiter quantizes x to mxfp4") and prints neither its rule nor its kernel.
+    Reading taken: the OCP MX v1.0 rule the weights follow, per 32-element
+    block along K of each token -- X = floor(log2 amax) - 2, scale code X + 127
+    clamped to [0, 254], elements e2m1_rne_sat(x / 2^X), an all-zero block
+    code 127 (``quant_mxfp4_ocp``).
+
+    x: [M, K] float (bf16 values). Returns (packed uint8 [M, K/2], scale uint8 [M, K/32]).
+    """
+    return quant_mxfp4_ocp(x)
+
+
 def quant_blockfp8_w(w, block=128):
     """Block e4m3 weight quantization (test inputs only).
 
@@ -111,5 +127,5 @@ def dequant_mxfp4(packed, scale, K):
     return e2m1_decode(codes) * np.repeat(sc, 32, axis=1)
 
 
-__all__ = ["quant_act", "quant_mxfp4_ocp", "quant_blockfp8_w", "dequant_mxfp4",
+__all__ = ["quant_act", "quant_mxfp4_ocp", "quant_act_mxfp4", "quant_blockfp8_w", "dequant_mxfp4",
            "FP8_MAX", "MIN_SCALE", "E2M1_MAX", "E4M3_MAX"]
