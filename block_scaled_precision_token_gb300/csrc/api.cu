@@ -136,7 +136,7 @@ using namespace r4;
 
 extern "C" {
 
-int r4_version(void) { return (0 << 16) | 1; }
+int r4_version(void) { return (0 << 16) | 2; }   // 0.2: fused producers, quotient self-check, options 11 and 13
 
 const char *r4_status_string(int status) {
   switch (status) {
