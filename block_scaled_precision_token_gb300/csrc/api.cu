@@ -74,8 +74,11 @@ int row_threads(RowKind kind, int64_t M, int64_t vecs) {
   // more rows resident per SM -- per-token quant M=8192, K=5120: 30.9 ->
   // 24.3 us; the norm producer gains only with many rows (M=8192: 67.6 ->
   // 63.1 us; M=64: 3.8 -> 4.6 us, so it keeps 256 below 2 rows per SM); the
-  // SiLU producer is issue-bound and loses (M=2048: 72.5 -> 86.1 us).
-  if (vecs > 768 || kind == RowKind::kSilu) return 256;
+  // SiLU producer is issue-bound and loses (M=2048: 72.5 -> 86.1 us); its
+  // long rows at many tokens take 512 threads instead (fewer vectors per
+  // thread, more warps per SM).
+  if (kind == RowKind::kSilu) return (vecs > 1536 && M >= device_sm_count()) ? 512 : 256;
+  if (vecs > 768) return 256;
   if (kind == RowKind::kNorm && M < 2 * static_cast<int64_t>(device_sm_count())) return 256;
   return 128;
 }

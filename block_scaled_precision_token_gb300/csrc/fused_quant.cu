@@ -30,6 +30,7 @@ namespace {
 using namespace qc;
 
 constexpr int kThreads = 256;
+constexpr int kSiluThreads = 512;   // the SiLU producer's long rows at many tokens (row_threads)
 
 __device__ __forceinline__ uint32_t bf16_rn_bits(float v) {
   const __nv_bfloat16 h = __float2bfloat16_rn(v);
@@ -154,12 +155,12 @@ __device__ __forceinline__ float silu_f32(float g) {
 }
 
 template <int VPT>
-__global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const uint16_t *__restrict__ gu, int N, int cols,
+__global__ void __launch_bounds__(kSiluThreads) silu_mul_quant_kernel(const uint16_t *__restrict__ gu, int N, int cols,
                                                                 int C, uint8_t *__restrict__ q,
                                                                 float *__restrict__ s) {
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait();   // gu comes from the preceding kernel
-  __shared__ float red[kThreads / 32];
+  __shared__ float red[kSiluThreads / 32];
   __shared__ float slot;
   const int row = blockIdx.x / C, part = blockIdx.x - row * C, tid = threadIdx.x, nt = blockDim.x;
   const int c0 = part * cols, c1 = min(N, c0 + cols);

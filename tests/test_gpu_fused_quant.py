@@ -116,7 +116,8 @@ def test_add_rmsnorm_quant_prefill_rows_sampled(r4q):
     _check_quant(q[rt], s[rt], h_lo, h_hi, "prefill sampled rows")
 
 
-@pytest.mark.parametrize("M,N", [(1, 8), (6, 17408), (64, 2048), (257, 1024), (3, 24576)])
+@pytest.mark.parametrize("M,N", [(1, 8), (6, 17408), (64, 2048), (257, 1024), (3, 24576),
+                                 (160, 17408), (153, 24576)])   # the last two: 512-thread blocks
 def test_silu_mul_quant(r4q, M, N):
     g = _randn((M, N), M + N, 3.0)
     u = _randn((M, N), M + 2 * N, 1.0)
