@@ -291,8 +291,9 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * automatically (short batches spread each row over a cluster of up to 8
  * CTAs), 1/2/4/8 force it; other values return R4_ERR_INVALID_ARG;
  * key 13: threads per CTA at most in the same quantizers: 0 (default)
- * chooses (128 for slices of up to 6144 columns where that gains, else
- * 256), 64/128/256 cap it (a row that would need more than 12 vectors of 8
+ * chooses (128 for slices of up to 6144 columns where that gains, 512 for
+ * the SiLU producer's rows over 12288 columns at many tokens, else 256),
+ * 64/128/256 cap it (a row that would need more than 12 vectors of 8
  * per thread widens the block again); other values return
  * R4_ERR_INVALID_ARG.
  */
