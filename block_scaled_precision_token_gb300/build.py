@@ -22,7 +22,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
           "-I" + os.path.join(ROOT, "include")]
 SOURCES = ["api.cu", "quant.cu", "fused_quant.cu", "prepack.cu", "gemm_w4a8.cu", "gemm_blockfp8.cu",
-           "gemm_skinny.cu", "noalloc.cu"]
+           "gemm_skinny.cu", "noalloc.cu", "peak.cu"]
 
 
 def _nvcc():

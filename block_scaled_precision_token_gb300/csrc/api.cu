@@ -178,6 +178,7 @@ int r4_set_option(int key, int64_t value) {
       return R4_OK;
     case 3: options().fp8_splits = static_cast<int>(value); return R4_OK;
     case 4: options().pdl = value ? 1 : 0; return R4_OK;
+    case 14: options().early_weights = value ? 1 : 0; return R4_OK;
     case 5: options().l2_prefetch = value ? 1 : 0; return R4_OK;
     case 6: options().cluster_split = value ? 1 : 0; return R4_OK;
     case 9: options().fp8_stage_scales = value ? 1 : 0; return R4_OK;
@@ -208,6 +209,14 @@ int r4_quant_fp8_per_token(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
   return launch_quant_act(x, M, K, ldx, group, q, s, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? R4_OK
              : R4_ERR_CUDA;
+}
+
+int r4_mma_peak(int kind, int n, int blocks, int iters, r4_stream_t stream) {
+  if (kind < 1 || kind > 3 || (n != 128 && n != 256) || blocks < 1 || blocks > 65535 || iters < 1)
+    return R4_ERR_INVALID_ARG;
+  if (device_error_word() == nullptr) return R4_ERR_CUDA;
+  return launch_mma_peak(kind, n, blocks, iters, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? R4_OK
+                                                                                                      : R4_ERR_CUDA;
 }
 
 int r4_check_quotients(unsigned long long *count, float *example, r4_stream_t stream) {

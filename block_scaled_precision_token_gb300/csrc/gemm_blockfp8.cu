@@ -51,6 +51,8 @@ struct Params {
   int t_tiles, splits, kb_per_split, units;
   int ldc;
   int as_tma;          // 1: As and Ws travel with each pipeline stage (TMA), needs KB % 4 == 0
+  int inject_stall;    // test of the bounded waits: CTA 0 withholds its first activation copy
+  int early_w;         // 1: weight tiles are requested before waiting for the preceding kernel
   const float *As;     // [M, KB]
   const float *Ws;     // [N/128, KB]
   uint16_t *c;
@@ -254,6 +256,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       const uint32_t tx = C::kTxBytes + (p.as_tma ? C::kAsTx : 0u);
       // Weights first (independent of the preceding kernel), then wait for
       // it before the first activation tile.
+      if (!p.early_w) pdl_wait();
       {
         SlotCursor cu;
         cu.start(p);
@@ -279,7 +282,10 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
           mbar_arrive_expect_tx(&full_bar[stage], tx);
           tma_load_3d(st, &tm_w, &full_bar[stage], 0, 0, cu.nt * p.KB + cu.kb, pol_w);
         }
-        tma_load_2d(st + kWSmem, &tm_x, &full_bar[stage], cu.kb * 128, cu.tt * BT, pol_x);
+        // (Failure-detection test: with inject_stall, CTA 0 never issues its
+        // first activation copy, so the stage's transaction never completes.)
+        if (!(p.inject_stall && blockIdx.x == 0 && g == 0))
+          tma_load_2d(st + kWSmem, &tm_x, &full_bar[stage], cu.kb * 128, cu.tt * BT, pol_x);
         if (p.as_tma) {
           const int kb4 = cu.kb & ~3;
           tma_load_2d(st + kWSmem + C::kXSmem, &tm_as, &full_bar[stage], kb4, cu.tt * BT, pol_x);
@@ -411,6 +417,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
     SlotCursor cu;
     cu.start(p);
     int g = 0;
+    int abort_u = -1;                  // unit at which an expired wait stopped the epilogue
     while (cu.valid(p)) {
       const int nt = cu.nt, tt = cu.tt, sp = cu.sp, u = cu.u;
       const int t0 = tt * BT;
@@ -459,7 +466,10 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       }
       // Every epilogue thread reaches this barrier once per unit, whether or
       // not its waits succeeded, so the stop decision is the same everywhere.
-      if (named_bar_any(1, C::kEpiThreads, !ok)) break;
+      if (named_bar_any(1, C::kEpiThreads, !ok)) {
+        abort_u = u;
+        break;
+      }
       const int tcol = t0 + col0;
       if (p.splits == 1) {
 #pragma unroll
@@ -473,17 +483,27 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
         named_bar_sync(2, C::kEpiThreads);
         if (e == 0) {
           const int prev = atomicAdd(p.counters + tile, 1);
-          *is_last = (prev == p.splits - 1) ? 1 : 0;
+          // 1: last arrival, sum; 2: last arrival after a poisoned one, no sum
+          *is_last = ((prev & kArrivalMask) == p.splits - 1) ? ((prev >> kPoisonShift) ? 2 : 1) : 0;
         }
         named_bar_sync(2, C::kEpiThreads);
-        if (*is_last) {
+        if (*is_last == 1) {
           __threadfence();
           const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (128 * BT);
           reduce_partials_store<BT>(base, p.splits, min(BT, p.M - t0), nt * 128, nt * 128 + 128, nullptr, t0, p.c,
                                     p.ldc, e, C::kEpiThreads);
-          if (e == 0) p.counters[tile] = 0;
         }
+        if (*is_last && e == 0) p.counters[tile] = 0;
         named_bar_sync(2, C::kEpiThreads);
+      }
+    }
+    // An expired wait stopped this CTA: it still arrives, poisoned, at the
+    // counter of every split-K tile it owed, so every counter ends at zero.
+    if (abort_u >= 0 && p.splits > 1 && e == 0) {
+      for (int u2 = abort_u; u2 < p.units; u2 += gridDim.x) {
+        const int tile2 = u2 / p.splits;
+        const int prev = atomicAdd(p.counters + tile2, 1 + kPoisonArrival);
+        if ((prev & kArrivalMask) == p.splits - 1) atomicExch(p.counters + tile2, 0);
       }
     }
   }
@@ -533,6 +553,8 @@ int launch_bt(const uint8_t *q, const float *As, const uint8_t *packed, int64_t 
   p.M = static_cast<int>(M);
   p.KB = pl.KB;
   p.as_tma = as_tma;
+  p.inject_stall = options().inject_stall;
+  p.early_w = options().early_weights;
   p.t_tiles = pl.t_tiles;
   p.splits = pl.splits;
   p.kb_per_split = pl.kb_per_split;

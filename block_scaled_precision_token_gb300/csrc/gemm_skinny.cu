@@ -88,7 +88,7 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
 template <int NG2, int NB>  // token groups of 16 (Mpad = 16 * NG2); NB staging buffers
 __global__ void __launch_bounds__(kThreads, 1)
     skinny_bf16_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w, int M, int N, int K,
-                       int chunks_per_cta, uint16_t *__restrict__ c, int ldc) {
+                       int chunks_per_cta, uint16_t *__restrict__ c, int ldc, int early_w) {
   using S = Smem<NG2, NB>;
   constexpr int kMpad = S::kMpad;
   constexpr int kRS = S::kRS;
@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kend = min(K, kbeg + chunks_per_cta * 256);
 
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!early_w) asm volatile("griddepcontrol.wait;" ::: "memory");   // w may come from the preceding kernel
 
   // Warp roles: NGW token-group slots x KP k-phases (4 warps). Warp w
   // multiplies token group w % NGW over the k-steps of phase w / NGW, so with
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t my_part = smem_addr(sCl);
   for (int e = static_cast<int>(rank) * per + tid; e < min(total, static_cast<int>(rank + 1) * per); e += kThreads) {
     const int r = e % kRows, t = e / kRows;
+    if (t >= M || n0 + r >= N) continue;   // padded token or row: no load without a consumer
     const uint32_t off = 4u * static_cast<uint32_t>(r * kRS + t);
     float pq[kMaxKS];   // all loads in flight before the (rank-ordered) sum
 #pragma unroll
@@ -218,15 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int q = 0; q < kMaxKS; ++q)
       if (q < KS) v += pq[q];
-    if (t < M && n0 + r < N) {
-      __nv_bfloat16 h = __float2bfloat16_rn(v);
-      c[static_cast<size_t>(t) * ldc + n0 + r] = *reinterpret_cast<uint16_t *>(&h);
-    }
+    __nv_bfloat16 h = __float2bfloat16_rn(v);
+    c[static_cast<size_t>(t) * ldc + n0 + r] = *reinterpret_cast<uint16_t *>(&h);
   }
   // No CTA leaves while another may still read its partial. The arrive must
-  // be a release: it is what orders this CTA's remote loads (some of whose
-  // values are never used, for padded tokens) before the peers may exit. A
-  // relaxed arrive let a CTA leave under a peer's load still in flight.
+  // be a release: it is what orders this CTA's remote loads before the peers
+  // may exit (a relaxed arrive, tried when padded tokens were still loaded,
+  // let a CTA leave under a peer's load still in flight).
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
@@ -255,7 +255,7 @@ cudaError_t launch_ng(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N
   cfg.attrs = attr;
   cfg.numAttrs = options().pdl ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kern, x, w, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), cpc, c,
-                         static_cast<int>(ldc));
+                         static_cast<int>(ldc), options().early_weights);
   set_last_kernel(NG2 == 1 ? "skinny_bf16_kernel<1>" : NG2 == 2 ? "skinny_bf16_kernel<2>"
                   : NG2 == 3 ? "skinny_bf16_kernel<3>" : "skinny_bf16_kernel<4>");
   return e;

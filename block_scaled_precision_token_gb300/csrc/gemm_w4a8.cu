@@ -85,6 +85,7 @@ struct Params {
   int cluster;           // 1: the `splits` CTAs of a cluster split K and exchange partials in DSMEM
   int xchg_stage;        // 1 (cluster, one unit per CTA): exchange the whole tile from the pipeline stages
   int inject_stall;      // test of the bounded waits: CTA 0 withholds its first activation copy
+  int early_w;           // 1: weight tiles are requested before waiting for the preceding kernel
   const uint8_t *w;      // packed weight codes [NT][KB][128][64]
   const float *s;
   const uint8_t *sf;     // scale atoms of the prepacked weight
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       // Optionally ask L2 for this CTA's whole weight range up front: the
       // stream then runs at HBM rate while this kernel waits for its
       // predecessor, not only for the ring's depth.
+      if (!p.early_w) pdl_wait();   // weights may come from the preceding kernel
       if (p.l2_prefetch && pw == 0)
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) prefetch_unit_l2(p, u);
       {
@@ -380,6 +382,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
     uint32_t out_chunk = 0;   // running count of staged output chunks (selects the buffer)
     uint32_t xchg = 0;        // running count of cluster split-K exchanges
     bool stop = false;
+    int abort_u = -1;         // unit at which an expired wait stopped the epilogue
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
       int nt, tt, sp, kb0, kb1;
       decode_unit(p, u, nt, tt, sp, kb0, kb1);
@@ -389,7 +392,10 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       // before the barrier and read after it.
       if (!mbar_wait(&accf_bar[acc], acc_phase, abort_flag, p.err, DEV_ERR_WAIT_ACC_FULL)) *epi_abort = 1;
       named_bar_sync(1, 128);
-      if (*epi_abort) break;
+      if (*epi_abort) {
+        abort_u = u;
+        break;
+      }
       tc_fence_after();
       const int n = nt * 128 + q * 32 + lane;
       const int t0 = tt * BT;
@@ -486,7 +492,10 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
           const int rank = static_cast<int>(cluster_ctarank());
           const int qlo = rank * 32 / p.splits, nq = (rank + 1) * 32 / p.splits - qlo;
           const uint32_t red_base = smem_u32(red);
-          for (int idx = ew * 32 + lane; idx < rows * nq; idx += 128) {
+          // Only token rows that exist (t < M) are read from the peers: a
+          // load whose value has no consumer is never issued.
+          const int vrows = min(rows, p.M - tbase);
+          for (int idx = ew * 32 + lane; idx < vrows * nq; idx += 128) {
             const int j = idx / nq, qd = qlo + (idx - j * nq);
             const uint32_t off = red_base + static_cast<uint32_t>((j * 128 + qd * 4) * 4);
             float4 a4;
@@ -545,21 +554,32 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
         named_bar_sync(1, 128);
         if (ew == 0 && lane == 0) {
           const int prev = atomicAdd(p.counters + tile, 1);
-          *is_last = (prev == p.splits - 1) ? 1 : 0;
+          // 1: last arrival, sum; 2: last arrival after a poisoned one, no sum
+          *is_last = ((prev & kArrivalMask) == p.splits - 1) ? ((prev >> kPoisonShift) ? 2 : 1) : 0;
         }
         named_bar_sync(1, 128);
-        if (*is_last) {
+        if (*is_last == 1) {
           __threadfence();
           const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (128 * BT);
           reduce_partials_store<BT>(base, p.splits, min(BT, p.M - t0), nt * 128, p.N, p.s, t0, p.c, p.ldc,
                                     ew * 32 + lane, 128);
-          if (ew == 0 && lane == 0) p.counters[tile] = 0;
         }
+        if (*is_last && ew == 0 && lane == 0) p.counters[tile] = 0;
         named_bar_sync(1, 128);
       }
       if (++acc == C::kNumAcc) {
         acc = 0;
         acc_phase ^= 1u;
+      }
+    }
+    // An expired wait stopped this CTA: it still arrives, poisoned, at the
+    // counter of every workspace split-K tile it owed (the one it stopped in
+    // and all later ones), so that every counter ends the launch at zero.
+    if (abort_u >= 0 && p.splits > 1 && !p.cluster && leader) {
+      for (int u2 = abort_u; u2 < p.units; u2 += gridDim.x) {
+        const int tile2 = u2 / p.splits;
+        const int prev = atomicAdd(p.counters + tile2, 1 + kPoisonArrival);
+        if ((prev & kArrivalMask) == p.splits - 1) atomicExch(p.counters + tile2, 0);
       }
     }
     if (leader) bulk_wait_all();   // output stores complete before the CTA's smem goes away
@@ -624,6 +644,7 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
   p.cluster = pl.cluster;
   p.xchg_stage = (pl.cluster && pl.units <= pl.grid) ? 1 : 0;
   p.inject_stall = options().inject_stall;
+  p.early_w = options().early_weights;
   p.w = packed;
   p.s = s;
   p.sf = packed + mx_packed_codes_bytes(N, K);

@@ -48,6 +48,10 @@ __global__ void __launch_bounds__(512) prepack_mxfp4_kernel(const uint8_t *__res
     }
     *reinterpret_cast<uint32_t *>(sf + tile * 512 + 4 * tid) = word;
   }
+  // The GEMMs read the packed weight before their dependency wait (they may
+  // start once this kernel's blocks have exited): make every write visible
+  // device-wide before the block exits.
+  __threadfence();
 }
 
 __global__ void __launch_bounds__(256) prepack_fp8_kernel(const uint8_t *__restrict__ w, int64_t K, int KB,
@@ -59,6 +63,7 @@ __global__ void __launch_bounds__(256) prepack_fp8_kernel(const uint8_t *__restr
     const uint4 v = __ldg(reinterpret_cast<const uint4 *>(w + (nt * 128 + r) * K + kb * 128 + c));
     *reinterpret_cast<uint4 *>(codes + tile * 16384 + r * 128 + c) = v;
   }
+  __threadfence();   // visible device-wide before the block exits (see prepack_mxfp4_kernel)
 }
 
 }  // namespace

@@ -33,6 +33,17 @@ enum : int {
   DEV_ERR_WAIT_PEER = 6      // split-K exchange gave up waiting for another CTA of the cluster
 };
 
+// Split-K arrival counters (one int per output tile in the caller's
+// workspace): every unit of a tile adds 1 when its partial is written; the
+// last of the tile's `splits` arrivals sums the partials and resets the
+// counter to 0. A launch that stopped early (an expired wait) still arrives,
+// for every unit it owed, with kPoisonArrival added: the last arrival then
+// skips the sum (its partials are incomplete) but still resets the counter,
+// so the workspace is zero again for the next call either way.
+constexpr int kArrivalMask = 0xFFFF;      // arrivals (splits <= 64)
+constexpr int kPoisonShift = 16;
+constexpr int kPoisonArrival = 1 << kPoisonShift;
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -303,6 +314,21 @@ __device__ __forceinline__ void tc_mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[smem] x B[smem]^T with packed e2m1 operands (two per byte)
+// and ue8m0 block scales from tensor memory, one scale per 32 K: kind::mxf4,
+// M = 128, K = 64 per instruction, scale_vec::2X (scale id 0 or 2 selects the
+// byte pair of each row's 32-bit scale column).
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");

@@ -34,6 +34,7 @@ struct Options {
   int fp8_stage_scales = 1; // block-FP8: activation scales ride with the pipeline stage when possible
   int inject_stall = 0;     // tests only: the next W4A8 launches withhold one copy (bounded-wait test)
   int pdl = 1;              // launch with programmatic stream serialization
+  int early_weights = 1;    // GEMMs read their weight operand before waiting for the preceding kernel
   int l2_prefetch = 0;      // W4A8: bulk L2 prefetch of the CTA's whole weight range at kernel start
   int cluster_split = 1;    // W4A8 decode tiles: split-K across a thread-block cluster when possible
   int row_split = 0;        // row-wise quantizers: CTAs per row (0 = automatic, else 1/2/4/8)
@@ -145,6 +146,8 @@ int launch_gemm_w4a8(const uint8_t *q, const float *s, const uint8_t *packed, in
                      uint16_t *c, int64_t ldc, void *ws, const GemmPlan &plan, cudaStream_t st);
 int launch_gemm_blockfp8(const uint8_t *q, const float *As, const uint8_t *packed, int64_t M, int64_t N,
                          int64_t K, uint16_t *c, int64_t ldc, void *ws, const GemmPlan &plan, cudaStream_t st);
+// Tensor-core issue-rate probe (kind 1 mxf8f6f4, 2 f8f6f4, 3 mxf4; n = 128 or 256).
+cudaError_t launch_mma_peak(int kind, int n, int blocks, int iters, cudaStream_t st);
 cudaError_t launch_gemm_skinny(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N, int64_t K, uint16_t *c,
                                int64_t ldc, cudaStream_t st);
 

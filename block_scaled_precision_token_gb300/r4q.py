@@ -55,6 +55,7 @@ _SIGS = {
     "r4_add_rmsnorm_quant_fp8": ([_P, _P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P, _P], _I),
     "r4_silu_mul_quant_fp8": ([_P, _I64, _I64, _P, _P, _P], _I),
     "r4_check_quotients": ([_P, _P, _P], _I),
+    "r4_mma_peak": ([_I, _I, _I, _I, _P], _I),
 }
 
 
@@ -226,6 +227,10 @@ def r4_add_rmsnorm_quant_fp8(y, residual, weight, eps, M, K, residual_out, q, s,
 def r4_check_quotients(count, example, stream=None):
     _need(count, torch.int64, "count"); _need(example, torch.float32, "example")
     _check(lib().r4_check_quotients(_ptr(count), _ptr(example), _stream(stream)), "r4_check_quotients")
+
+
+def r4_mma_peak(kind, n, blocks, iters, stream=None):
+    _check(lib().r4_mma_peak(int(kind), int(n), int(blocks), int(iters), _stream(stream)), "r4_mma_peak")
 
 
 def r4_silu_mul_quant_fp8(gu, M, N, q, s, stream=None):

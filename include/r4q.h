@@ -25,13 +25,27 @@
  *    r4_device_error() reads and clears it.
  *  - The per-token path (quantization and the three GEMMs) is launched with
  *    programmatic dependent launch: a kernel may start while its predecessor
- *    in the stream is still running, and reads its WEIGHT operand before
- *    waiting for that predecessor (activations, scales, outputs and the
- *    workspace are touched only after it completed). Weights must therefore
- *    not be written by the immediately preceding kernel unless that kernel
- *    completes normally (every kernel outside this library does; within it,
- *    only the prepack and weight-quantizer calls write weights, and they are
- *    launched without programmatic dependence). r4_set_option(4, 0) turns it off.
+ *    in the stream is still running. Activations, scales, outputs and the
+ *    workspace are touched only after the kernel's dependency wait, which
+ *    returns once every preceding kernel has completed and its writes are
+ *    visible. The GEMMs read their WEIGHT operand (the prepacked buffer; the
+ *    bf16 matrix w of the skinny GEMM) BEFORE that wait, so that the weight
+ *    stream overlaps the tail of the preceding kernel. Rule for whoever writes
+ *    a weight:
+ *      * r4_prepack_mxfp4 / r4_prepack_blockfp8 may be followed by a GEMM
+ *        directly: their kernels are launched without programmatic
+ *        dependence and make every write visible device-wide before they
+ *        exit.
+ *      * A weight written by anything else (a kernel of another library, a
+ *        copy) must be separated from the GEMM by a full stream
+ *        serialization point: a cudaMemcpy*Async, an event wait, a host
+ *        synchronization, or a kernel launched without programmatic
+ *        dependence. This library's own per-token kernels are NOT such a
+ *        point (they are launched with programmatic dependence).
+ *      * Callers that cannot guarantee this turn the early weight read off
+ *        with r4_set_option(14, 0) (the GEMMs then wait first and read
+ *        after), or turn programmatic dependent launch off altogether with
+ *        r4_set_option(4, 0).
  */
 #ifndef R4Q_H
 #define R4Q_H
@@ -103,6 +117,24 @@ int r4_quant_fp8_per_token(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
  * Asynchronous on `stream`; ~1.07e9 pairs, about a millisecond on GB300.
  */
 int r4_check_quotients(unsigned long long *count, float *example, r4_stream_t stream);
+
+/*
+ * r4_mma_peak -- tensor-core issue-rate probe, the denominator of the GEMMs'
+ * roofline fractions. The pages measured their own matrix-instruction peak
+ * the same way: a register-resident loop that touches no memory
+ * ("radiance_mxfp4.py", module docstring, fp8 WMMA throughput). Launches
+ * `blocks` CTAs (one per SM when blocks = the SM count); each zero-fills its
+ * operand tiles in shared memory and one thread issues iters x 4 MMAs,
+ * M = 128, N = n, into one tensor-memory accumulator:
+ *   kind 1: kind::mxf8f6f4, e2m1 x e4m3, ue8m0 scales, K = 32 (the W4A8 GEMM);
+ *   kind 2: kind::f8f6f4, e4m3 x e4m3, K = 32 (the block-FP8 GEMM);
+ *   kind 3: kind::mxf4, e2m1 x e2m1, ue8m0 scales, K = 64.
+ * Flops per launch = blocks * iters * 4 * 2 * 128 * n * K. Time it with
+ * events on `stream`. Requirements: n = 128 or 256, 1 <= blocks <= 65535,
+ * iters >= 1. No memory argument: nothing is read or written outside the
+ * kernel's own shared and tensor memory.
+ */
+int r4_mma_peak(int kind, int n, int blocks, int iters, r4_stream_t stream);
 
 /*
  * r4_add_rmsnorm_quant_fp8 -- residual add + Gemma RMS norm + per-token e4m3
@@ -195,8 +227,13 @@ int r4_prepack_blockfp8(const uint8_t *w, const float *w_scale, int64_t N, int64
  * split-K fp32 partials plus one int32 arrival counter per output tile. 0 when
  * the chosen schedule needs none. The counters must be zero when the
  * workspace is first used (e.g. cudaMemsetAsync once after allocation); every
- * call leaves them zero again. One workspace must not serve two calls that can
- * run at the same time (two streams).
+ * call leaves them zero again, including a call whose kernel stopped early
+ * because a bounded device wait expired (r4_device_error reports it): such a
+ * launch still arrives, marked incomplete, at every counter it owed, and the
+ * last arrival at a tile resets the counter without summing (that tile's
+ * output is then unspecified, like the rest of that call's output). One
+ * workspace must not serve two calls that can run at the same time (two
+ * streams).
  */
 size_t r4_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
 
@@ -282,10 +319,11 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * automatic, else 16/32/64/128); key 9: block-FP8 activation scales carried
  * by each pipeline stage (1, default, when K/128 is a multiple of 4) or
  * loaded by the scale warp (0); key 10 (tests of failure detection only):
- * 1 makes the next W4A8 launches withhold one activation copy in their
- * first CTA, so a pipeline wait never completes, expires after ~2 s and is
- * reported by r4_device_error (the launch itself returns R4_OK, the output
- * is unspecified and the context stays usable); 0 (default) turns it off;
+ * 1 makes the next W4A8 and block-FP8 launches withhold one activation copy
+ * in their first CTA, so a pipeline wait never completes, expires after
+ * ~2 s and is reported by r4_device_error (the launch itself returns R4_OK,
+ * the output is unspecified, the workspace counters end at zero and the
+ * context stays usable); 0 (default) turns it off;
  * key 11: CTAs that share one row in the row-wise activation quantizers
  * (per-token, group-128 and the two fused producers): 0 (default) chooses
  * automatically (short batches spread each row over a cluster of up to 8
@@ -295,7 +333,10 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * the SiLU producer's rows over 12288 columns at many tokens, else 256),
  * 64/128/256 cap it (a row that would need more than 12 vectors of 8
  * per thread widens the block again); other values return
- * R4_ERR_INVALID_ARG.
+ * R4_ERR_INVALID_ARG;
+ * key 14: the GEMMs request their weight operand before waiting for the
+ * preceding kernel (1, default) or only after it (0); see the weight-writer
+ * rule at the top of this header.
  */
 int r4_set_option(int key, int64_t value);
 

@@ -1,9 +1,12 @@
 """Failure detection and capture safety, on the GPU without a fault.
 
 * A pipeline wait that can never complete (a test option withholds one TMA
-  copy in the first CTA of a W4A8 launch) must expire after its ~2 s limit,
-  leave a device error word that r4_device_error reports, and leave the
-  context usable: the next launch is correct.
+  copy in the first CTA of a W4A8 or block-FP8 launch) must expire after its
+  ~2 s limit, leave a device error word that r4_device_error reports, and
+  leave the context usable: the next launch is correct.
+* Such a launch must also leave the caller's split-K workspace as it found
+  it: every arrival counter back at zero, so the next call on the SAME
+  workspace elects the right last CTA and gives the oracle's result.
 * Every entry point must be capturable in a CUDA graph (the library never
   allocates or synchronizes), and the graph's results must equal the eager
   ones bit for bit."""
@@ -35,6 +38,9 @@ def r4q():
     m = require_gpu()
     yield m
     m.r4_set_option(10, 0)
+    m.r4_set_option(1, 0)
+    m.r4_set_option(3, 0)
+    m.r4_set_option(6, 1)
 
 
 def _w4a8_inputs(r4q, M, N, K):
@@ -69,6 +75,60 @@ def test_bounded_wait_expires_and_reports(r4q):
     assert_gemm_matches(c, c64, "after the stalled launch")
 
 
+def _blockfp8_inputs(r4q, M, N, K):
+    x = synth.activations(M, K, synth.CFG_BLOCKFP8)
+    w = synth.weights_fp32(N, K, synth.CFG_BLOCKFP8)
+    wq, Ws = Q.quant_blockfp8_w(w.numpy())
+    q, As = Q.quant_act(x.float().numpy(), group=128)
+    pk = r4q.prepack_blockfp8(torch.from_numpy(wq).cuda(), torch.from_numpy(Ws).cuda(), N, K)
+    return torch.from_numpy(q).cuda(), torch.from_numpy(As).cuda(), pk, (q, As, wq, Ws)
+
+
+@pytest.mark.parametrize("op", ["w4a8", "blockfp8"])
+def test_expired_wait_leaves_the_workspace_reusable(r4q, op):
+    """Split-K through the caller's workspace (forced: 4 splits, no cluster
+    exchange). The first CTA's stalled unit never writes its partial; the
+    launch must still end with every arrival counter at zero, and the next
+    call on the same workspace must match the oracle."""
+    M, N, K = 8, 512, 1024
+    tiles = (N // 128) * 1                       # 16-token tiles: one token tile
+    if op == "w4a8":
+        q, s, pk, ref = _w4a8_inputs(r4q, M, N, K)
+        r4q.r4_set_option(1, 4)
+        r4q.r4_set_option(6, 0)
+        opid = r4q.R4_OP_W4A8_MXFP4
+        call = lambda ws: r4q.gemm_w4a8(q, s, pk, N, K, ws=ws)
+        exact = lambda: G.gemm_w4a8(*ref)[0]
+    else:
+        q, As, pk, ref = _blockfp8_inputs(r4q, M, N, K)
+        r4q.r4_set_option(3, 4)
+        opid = r4q.R4_OP_BLOCKFP8
+        call = lambda ws: r4q.gemm_blockfp8(q, As, pk, N, K, ws=ws)
+        exact = lambda: G.gemm_blockfp8(*ref)[0]
+    try:
+        ws = r4q.workspace(opid, M, N, K)
+        assert ws is not None, "the forced schedule should use the workspace"
+        r4q.r4_device_error(clear=True)
+        r4q.r4_set_option(10, 1)
+        try:
+            call(ws)
+            torch.cuda.synchronize()
+        finally:
+            r4q.r4_set_option(10, 0)
+        code = r4q.r4_device_error(clear=True)
+        assert code in (WAIT_FULL, WAIT_ACC_FULL, WAIT_DRAIN), f"device error word {code}"
+        counters = ws[:4 * tiles].view(torch.int32).cpu()
+        assert torch.count_nonzero(counters) == 0, f"arrival counters left at {counters.tolist()}"
+        c = call(ws)                              # the same workspace, reused
+        torch.cuda.synchronize()
+        assert r4q.r4_device_error(clear=True) == 0
+    finally:
+        r4q.r4_set_option(1, 0)
+        r4q.r4_set_option(3, 0)
+        r4q.r4_set_option(6, 1)
+    assert_gemm_matches(c, exact(), f"{op} after the stalled launch, reused workspace")
+
+
 def test_every_entry_point_captures_in_a_graph(r4q):
     dev = torch.device("cuda")
     M, K, N = 16, 2048, 1024
@@ -97,6 +157,7 @@ def test_every_entry_point_captures_in_a_graph(r4q):
     s3 = torch.empty((M,), dtype=torch.float32, device=dev)
     ws1 = r4q.workspace(r4q.R4_OP_W4A8_MXFP4, M, N, K, dev)
     ws2 = r4q.workspace(r4q.R4_OP_BLOCKFP8, M, N, K, dev)
+    c4 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
 
     def step():
         r4q.r4_quant_fp8_per_token(x, M, K, K, K, q, s)
@@ -106,8 +167,18 @@ def test_every_entry_point_captures_in_a_graph(r4q):
         r4q.r4_gemm_bf16_nt_skinny(x, wb, M, 256, K, c3, 256)
         r4q.r4_add_rmsnorm_quant_fp8(x, res, nw, 1e-6, M, K, ro, q2, s2)
         r4q.r4_silu_mul_quant_fp8(gu, M, K, q3, s3)
+        # the no-allocation GEMM on a split-K schedule, so that its clearing
+        # of the static scratch and the split-K reduction are in the graph
+        # (the eager call below also looks up the scratch address first)
+        r4q.r4_set_option(1, 4)
+        r4q.r4_set_option(6, 0)
+        try:
+            r4q.r4_gemm_w4a8_mxfp4_noalloc(q, s, pk, M, N, K, c4, N)
+        finally:
+            r4q.r4_set_option(1, 0)
+            r4q.r4_set_option(6, 1)
 
-    outs = (q, s, qg, sg, c1, c2, c3, q2, s2, ro, q3, s3)
+    outs = (q, s, qg, sg, c1, c2, c3, q2, s2, ro, q3, s3, c4)
     step()
     torch.cuda.synchronize()
     eager = [t.clone() for t in outs]

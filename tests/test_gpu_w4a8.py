@@ -143,14 +143,17 @@ def _sampled_full_size(r4q, M, N, K, seed, nsample=384):
     assert torch.isfinite(c.float()).all()
 
 
-@pytest.mark.parametrize("M", [6, 64])
+# Every (M, N, K) the benchmark times, at full size, through the planner's
+# automatic schedule (token tile, split factor, cluster or workspace split):
+# the schedule is chosen per shape, so each timed plan is checked here.
+@pytest.mark.parametrize("M", synth.DECODE_M)
 @pytest.mark.parametrize("N,K", synth.DECODE_NK)
 def test_decode_full_size_sampled(r4q, M, N, K):
     _sampled_full_size(r4q, M, N, K, seed=100 + M)
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 5120, 17408), (256, 34816, 5120), (2048, 10240, 5120),
-                                   (8192, 34816, 5120)])
+@pytest.mark.parametrize("M", synth.PREFILL_M)
+@pytest.mark.parametrize("N,K", synth.PREFILL_NK)
 def test_prefill_full_size_sampled(r4q, M, N, K):
     _sampled_full_size(r4q, M, N, K, seed=200 + M, nsample=128)
 
