@@ -194,7 +194,8 @@ def mma_peaks(r4q, sms, reps=5):
     operands in shared memory, back-to-back MMAs into tensor memory), with
     the SM clock sampled while it runs. TFLOP/s per instruction shape."""
     import torch
-    shapes = (("mxf8f6f4_n256", 1, 256, 32), ("mxf8f6f4_n128", 1, 128, 32), ("f8f6f4_n128", 2, 128, 32))
+    shapes = (("mxf8f6f4_n256", 1, 256, 32), ("mxf8f6f4_n128", 1, 128, 32), ("f8f6f4_n128", 2, 128, 32),
+              ("mxf4_n256", 3, 256, 64))
     out = {}
     with ClockSampler(torch.cuda.current_device()) as clk:
         t_end = time.perf_counter() + 1.0
@@ -466,6 +467,7 @@ def run_sections(r4q, synth, device, sweep, l2_bytes, peaks, mma):
         fq[f"silu_mul_quant_M{M}_N{N}"] = {"us": round(ms * 1e3, 2), "GBps": round((5 * M * N + 4 * M) / ms / 1e6, 1)}
         del g
     out["fused_quant"] = fq
+    out["w4a4"] = run_w4a4(r4q, synth, device, sweep, extra, l2_bytes, mma)
     # tiny W4A8 linear (quant + GEMM per call, as a decode step issues it)
     M, N, K = synth.TINY["M"], synth.TINY["N"], synth.TINY["K"]
     w = synth.weights_fp32(N, K, synth.CFG_TINY).to(device)
@@ -488,6 +490,73 @@ def run_sections(r4q, synth, device, sweep, l2_bytes, peaks, mma):
     out["tiny_w4a8"] = {f"M{M}_N{N}_K{K}": {"us_quant_plus_gemm": round(ms * 1e3, 2)}}
     del g
     return out
+
+
+def run_w4a4(r4q, synth, device, sweep, prefill_weights, l2_bytes, mma):
+    """The W4A4 variant on the W4A8 workloads' shapes: the GEMM alone with cold
+    weights (decode: weight GB/s; prefill: TFLOP/s against the measured
+    kind::mxf4 rate), and the MXFP4 activation quantizer."""
+    import torch
+    res = {"decode": {}, "prefill": {}, "quant": {}}
+    peak = mma.get("mxf4_n256")
+    for (M, N, K) in sweep.combos:
+        x = sweep.x[K][:M]
+        q, sc = r4q.quant_mxfp4(x)
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        ws = r4q.workspace(r4q.R4_OP_W4A4_MXFP4, M, N, K, device)
+        pool = pooled_copies(sweep.packed[(N, K)][0], weight_bytes(N, K), l2_bytes)
+        R = max(len(pool), 12)
+
+        def fn():
+            for i in range(R):
+                r4q.r4_gemm_w4a4_mxfp4(q, sc, pool[i % len(pool)], M, N, K, c, N, ws)
+
+        g = capture(fn)
+        ms = time_graph(g, 10) / R
+        res["decode"][f"M{M}_N{N}_K{K}"] = {"us": round(ms * 1e3, 3),
+                                            "weight_GBps": round(weight_bytes(N, K) / ms / 1e6, 1)}
+        del g, pool
+    for M in synth.PREFILL_M:
+        for (N, K) in synth.PREFILL_NK:
+            x = synth.activations(M, K, synth.CFG_PREFILL, outliers=True).to(device)
+            q, sc = r4q.quant_mxfp4(x)
+            c = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+            ws = r4q.workspace(r4q.R4_OP_W4A4_MXFP4, M, N, K, device)
+            pk = prefill_weights[(N, K)]
+            pool = pooled_copies(pk, weight_bytes(N, K), l2_bytes, min_copies=2) if M <= 2048 else [pk]
+            R = max(len(pool), 4)
+
+            def fn():
+                for i in range(R):
+                    r4q.r4_gemm_w4a4_mxfp4(q, sc, pool[i % len(pool)], M, N, K, c, N, ws)
+
+            g = capture(fn)
+            ms = time_graph(g, 10) / R
+            tf = 2.0 * M * N * K / ms / 1e9
+            res["prefill"][f"M{M}_N{N}_K{K}"] = {"us": round(ms * 1e3, 1), "TFLOPs": round(tf, 1),
+                                                 "frac_mxf4_peak": round(tf / peak, 3) if peak else None}
+            del g, pool, x, q, sc, c, ws
+    for (M, K) in [(8, 5120), (2048, 5120), (8192, 5120)]:
+        x = synth.activations(M, K, synth.CFG_PREFILL).to(device)
+        q = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
+        sc = torch.empty(r4q.r4_quant_mxfp4_act_scale_bytes(M, K), dtype=torch.uint8, device=device)
+        R = 20
+
+        def fn():
+            for _ in range(R):
+                r4q.r4_quant_mxfp4_act(x, M, K, K, q, sc)
+
+        g = capture(fn)
+        ms = time_graph(g, 10) / R
+        res["quant"][f"M{M}_K{K}"] = {"us": round(ms * 1e3, 2),
+                                      "GBps": round((2 * M * K + M * K // 2 + sc.numel()) / ms / 1e6, 1)}
+        del g
+    res["digest"] = {
+        "decode_GBps": {_shape_key(k): round(v["weight_GBps"]) for k, v in res["decode"].items()},
+        "prefill_TFLOPs": {_shape_key(k): round(v["TFLOPs"]) for k, v in res["prefill"].items()},
+        "mxf4_peak_TFLOPs": peak,
+    }
+    return res
 
 
 def run_ours(args, rank, world, local_rank):
@@ -707,7 +776,7 @@ def digest(per, sec, hbm):
     d["prefill_TFLOPs"] = {_shape_key(k): round(v["TFLOPs"]) for k, v in pre.items()}
     d["prefill_frac"] = {_shape_key(k): v["frac_fp8_peak"] for k, v in pre.items()}
     mma = sec.get("mma_peak_TFLOPs", {})
-    d["mma_peak_TFLOPs"] = {k: mma.get(k) for k in ("mxf8f6f4_n256", "f8f6f4_n128", "sm_mhz")}
+    d["mma_peak_TFLOPs"] = {k: mma.get(k) for k in ("mxf8f6f4_n256", "f8f6f4_n128", "mxf4_n256", "sm_mhz")}
     bf = sec.get("blockfp8", {})
     d["blockfp8_TFLOPs_M2048_GBps_else"] = {
         _shape_key(k): (round(v["TFLOPs"]) if k.startswith("M2048") else round(v["weight_GBps"])) for k, v in bf.items()}
@@ -815,6 +884,15 @@ def run_one(spec):
         q, s = r4q.quant_fp8(synth.activations(M, K, synth.CFG_DECODE, outliers=True).to(dev))
         for _ in range(3):
             r4q.gemm_w4a8(q, s, pk, N, K)
+    elif kind == "w4a4":
+        M, N, K = dims
+        w = synth.weights_fp32(N, K, synth.CFG_DECODE).to(dev)
+        p, sc = r4q.quantize_mxfp4_weight(w)
+        del w
+        pk = r4q.prepack_mxfp4(p, sc, N, K)
+        q, qs = r4q.quant_mxfp4(synth.activations(M, K, synth.CFG_DECODE, outliers=True).to(dev))
+        for _ in range(3):
+            r4q.gemm_w4a4(q, qs, pk, N, K)
     elif kind == "fp8":
         M, N, K = dims
         w = synth.weights_fp32(N, K, synth.CFG_BLOCKFP8).to(dev)
@@ -860,7 +938,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--one", nargs="+", metavar="ARG",
-                    help="profiling driver: KIND M N K (KIND = w4a8 | fp8 | skinny), quant M K, "
+                    help="profiling driver: KIND M N K (KIND = w4a8 | w4a4 | fp8 | skinny), quant M K, "
                          "arq M K (add + RMS norm + quant) or smq M N (SiluAndMul + quant); "
                          "runs three launches of that one call and exits")
     args = ap.parse_args(argv)

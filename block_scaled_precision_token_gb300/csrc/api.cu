@@ -139,7 +139,7 @@ using namespace r4;
 
 extern "C" {
 
-int r4_version(void) { return (0 << 16) | 2; }   // 0.2: fused producers, quotient self-check, options 11 and 13
+int r4_version(void) { return (0 << 16) | 3; }   // 0.3: W4A4 (MXFP4 activations, kind::mxf4), option 14, r4_mma_peak
 
 const char *r4_status_string(int status) {
   switch (status) {
@@ -268,6 +268,25 @@ int r4_quantize_blockfp8_weight(const float *w, int64_t N, int64_t K, uint8_t *q
              : R4_ERR_CUDA;
 }
 
+size_t r4_quant_mxfp4_act_scale_bytes(int64_t M, int64_t K) {
+  if (M < 1 || K < 32 || K % 32) return 0;
+  return mx_act_scale_bytes(M, K);
+}
+
+int r4_quant_mxfp4_act(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, uint8_t *scale,
+                       size_t scale_bytes, r4_stream_t stream) {
+  if (!x || !q || !scale) return R4_ERR_INVALID_ARG;
+  if (M < 1 || K < 32 || ldx < K || M > (1 << 30) || K > (1 << 30)) return R4_ERR_INVALID_ARG;
+  if (K % 32 || ldx % 8) return R4_ERR_UNSUPPORTED_SHAPE;
+  // one warp per 256 columns of a token: the grid must fit a launch
+  if (ceil_div(M * ceil_div(K, 256), 8) + ceil_div(K, 128) + 1 > 0x7fffffff) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 16)) return R4_ERR_MISALIGNED;
+  if (scale_bytes < mx_act_scale_bytes(M, K)) return R4_ERR_WORKSPACE;
+  return launch_quant_mxfp4_act(x, M, K, ldx, q, scale, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? R4_OK
+             : R4_ERR_CUDA;
+}
+
 size_t r4_prepack_mxfp4_bytes(int64_t N, int64_t K) {
   if (N < 1 || K < 32 || K % 32) return 0;
   return mx_packed_bytes(N, K);
@@ -311,6 +330,9 @@ size_t r4_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
     case R4_OP_BLOCKFP8:
       if (N % 128 || K % 128) return 0;
       return plan_blockfp8(M, N, K, device_sm_count()).ws_bytes;
+    case R4_OP_W4A4_MXFP4:
+      if (K % 32 || K < 128) return 0;
+      return plan_w4a4(M, N, K, device_sm_count()).ws_bytes;
     default: return 0;
   }
 }
@@ -328,6 +350,22 @@ int r4_gemm_w4a8_mxfp4(const uint8_t *q, const float *s, const void *packed, int
   }
   if (device_error_word() == nullptr) return R4_ERR_CUDA;
   return launch_gemm_w4a8(q, s, static_cast<const uint8_t *>(packed), M, N, K, c, ldc,
+                          pl.ws_bytes ? workspace : nullptr, pl, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int r4_gemm_w4a4_mxfp4(const uint8_t *q, const uint8_t *q_scale, const void *packed, int64_t M, int64_t N, int64_t K,
+                       uint16_t *c, int64_t ldc, void *workspace, size_t workspace_bytes, r4_stream_t stream) {
+  if (!q || !q_scale || !packed || !c) return R4_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldc < N || M > (1 << 30) || N > (1 << 30)) return R4_ERR_INVALID_ARG;
+  if (K % 32 || K < 128) return R4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(q, 16) || !aligned(q_scale, 16) || !aligned(packed, 256) || !aligned(c, 2)) return R4_ERR_MISALIGNED;
+  const GemmPlan pl = plan_w4a4(M, N, K, device_sm_count());
+  if (pl.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < pl.ws_bytes) return R4_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return R4_ERR_MISALIGNED;
+  }
+  if (device_error_word() == nullptr) return R4_ERR_CUDA;
+  return launch_gemm_w4a4(q, q_scale, static_cast<const uint8_t *>(packed), M, N, K, c, ldc,
                           pl.ws_bytes ? workspace : nullptr, pl, reinterpret_cast<cudaStream_t>(stream));
 }
 

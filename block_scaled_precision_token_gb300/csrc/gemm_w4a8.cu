@@ -73,11 +73,13 @@ constexpr uint32_t kSfBytes = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfaCol = 256;       // 4 columns per stage, up to 16 stages
 constexpr uint32_t kSfbCol = 320;       // 16 columns of constant 127 per MMA warp (up to 4)
+constexpr uint32_t kSfbColA4 = 320;     // W4A4: 8 columns of activation scales per stage (up to 16)
 constexpr int kMaxStages = 16;
 constexpr int kMaxClusterSplit = 6;   // the planner splits K across a cluster of 2..6 CTAs
 
 struct Params {
   int M, N, KB;
+  const uint8_t *xsf;    // W4A4: activation scale atoms [tokens/128][KB][512]
   int t_tiles, splits, kb_per_split, units;
   int ldc;
   int tma_store;         // 1: bf16 output tiles leave through smem + TMA tensor stores
@@ -104,20 +106,29 @@ struct Params {
 // to producer g % kIss and MMA warp g % kIss, lives in ring stage g % kStages,
 // and is accumulated into MMA warp (g % kIss)'s own tensor-memory accumulator;
 // the epilogue sums the kIss partial accumulators.
-template <int BT>
+//
+// A4 = true is the W4A4 variant (kind::mxf4): both operands are packed e2m1
+// (two per byte, loaded as plain bytes in the 64-byte swizzle: 8 KiB of
+// weight and BT x 64 bytes of activations per 128-K block), and each stage
+// also carries the activation scale atom(s) of its K block; the MMA applies
+// both operands' ue8m0 scales, so the epilogue has no per-token scale.
+template <int BT, bool A4 = false>
 struct Cfg {
   static constexpr int kIss = BT <= 64 ? 4 : 1;
   static constexpr int kNumAcc = (kIss * 2 * BT <= 256) ? 2 : 1;
   static constexpr int kThreads = 32 * (2 * kIss + 4);   // kIss producers, kIss MMA issuers, 4 epilogue
   static constexpr int kEpiWarp0 = 2 * kIss;
-  static constexpr uint32_t kXSmem = BT * 128;
-  static constexpr uint32_t kStageBytes = ((kWSmem + kXSmem + kSfBytes + 1023) / 1024) * 1024;
+  static constexpr uint32_t kWBytes = A4 ? 8192u : kWSmem;      // weight tile in shared memory
+  static constexpr uint32_t kXSmem = A4 ? BT * 64 : BT * 128;   // activation tile
+  static constexpr int kXAtoms = A4 ? (BT > 128 ? 2 : 1) : 0;   // activation scale atoms per stage
+  static constexpr uint32_t kSfOff = kWBytes + kXSmem;          // weight scale atom, then activation atoms
+  static constexpr uint32_t kStageBytes = ((kSfOff + kSfBytes * (1 + kXAtoms) + 1023) / 1024) * 1024;
   static constexpr int kOutChunk = BT < 32 ? BT : 32;                // tokens per output chunk
   static constexpr uint32_t kOutBytes = 2u * kOutChunk * 128u * 2u;  // two bf16 [chunk][128] buffers
   static constexpr int kStagesRaw = static_cast<int>((208u * 1024u) / kStageBytes);
   static constexpr int kStagesCap = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
   static constexpr int kStages = (kStagesCap / kIss) * kIss;        // every issuer owns fixed stages
-  static constexpr uint32_t kTxBytes = kWTxBytes + kXSmem + kSfBytes;
+  static constexpr uint32_t kTxBytes = kWTxBytes + kXSmem + kSfBytes * (1 + kXAtoms);
   static constexpr uint32_t kMiscBytes = 1024;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kMiscBytes + kOutBytes + 1024;  // + align slack
   static_assert(kIss * kNumAcc * BT <= 256, "accumulators overlap the scale columns");
@@ -144,11 +155,40 @@ __device__ __forceinline__ void prefetch_unit_l2(const Params &p, int u) {
   bulk_prefetch_l2(p.sf + blk * kSfBytes, nkb * kSfBytes);
 }
 
-template <int BT>
-__global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
+// Shared-memory descriptor of a K-major operand in the 64-byte swizzle
+// (rows of 64 bytes, 8-row groups 512 bytes apart, tile base 512-byte
+// aligned): the W4A4 tiles, 128 packed e2m1 per row.
+__device__ __forceinline__ uint64_t sdesc_sw64_kmajor(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;                 // LBO (unused for swizzled K-major)
+  d |= static_cast<uint64_t>(512u >> 4) << 32;          // SBO: 8 rows x 64 B
+  d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version (tcgen05)
+  d |= static_cast<uint64_t>(4u) << 61;                 // 64-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::mxf4 with ue8m0 block scales (scale_vec::2X):
+// A = B = e2m1 (format 1 in this kind), K-major, M = 128.
+__host__ __device__ constexpr uint32_t idesc_mxf4_e2m1(int n, int a_sf_id, int b_sf_id) {
+  return (static_cast<uint32_t>(b_sf_id & 3) << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (1u << 23) | (static_cast<uint32_t>(128 >> 4) << 24) | (static_cast<uint32_t>(a_sf_id & 3) << 29);
+}
+
+template <int BT, bool A4>
+__global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
     w4a8_mxf8f6f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                          const __grid_constant__ CUtensorMap tm_c, const Params p) {
-  using C = Cfg<BT>;
+  using C = Cfg<BT, A4>;
+  constexpr int kXStep = A4 ? 64 : kBK;   // activation tile x coordinate per 128-K block (bytes)
+  // per-token output scale: s[t] for W4A8; none for W4A4 (both scales are in the MMA)
+  auto out_scale = [&](int t) -> float {
+    if constexpr (A4) {
+      return 1.f;
+    } else {
+      return __ldg(p.s + t);
+    }
+  };
   constexpr int ISS = C::kIss;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -239,7 +279,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
               const int kb = kb0 + i;
               mbar_arrive_expect_tx(&full_bar[s_], C::kTxBytes);
               tma_load_3d(st, &tm_w, &full_bar[s_], 0, 0, nt * p.KB + kb, pol_w);
-              bulk_load(st + kWSmem + C::kXSmem, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
+              bulk_load(st + C::kSfOff, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
                         &full_bar[s_], pol_w);
             } else {
               mbar_arrive(&full_bar[s_]);
@@ -268,7 +308,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
             if (i < nkb) {
               mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
               tma_load_3d(st, &tm_w, &full_bar[stage], 0, 0, nt * p.KB + kb, pol_w);
-              bulk_load(st + kWSmem + C::kXSmem, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
+              bulk_load(st + C::kSfOff, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
                         &full_bar[stage], pol_w);
             } else {
               mbar_arrive(&full_bar[stage]);
@@ -278,7 +318,15 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
           // first activation copy, so that stage's transaction never completes
           // and the consumer's bounded wait must expire and report.)
           const bool withhold = p.inject_stall && blockIdx.x == 0 && gbase + i == 0;
-          if (i < nkb && !withhold) tma_load_2d(st + kWSmem, &tm_x, &full_bar[stage], kb * kBK, tt * BT, pol_x);
+          if (i < nkb && !withhold) tma_load_2d(st + C::kWBytes, &tm_x, &full_bar[stage], kb * kXStep, tt * BT, pol_x);
+          if constexpr (A4) {
+            // the activation scale atom(s) of this token tile and K block
+            if (i < nkb)
+              for (int a = 0; a < C::kXAtoms; ++a)
+                bulk_load(st + C::kSfOff + kSfBytes * (1 + a),
+                          p.xsf + (static_cast<size_t>(tt * BT / 128 + a) * p.KB + kb) * kSfBytes, kSfBytes,
+                          &full_bar[stage], pol_x);
+          }
           // Record the newest phase of every stage, padding slots included: a
           // parity wait cannot tell phase k from k + 2, and a stage only
           // advances after its earlier phases completed.
@@ -306,9 +354,11 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
     const int mw = warp - ISS;
     if (lane == 0) {
       const uint32_t sfb = tmem + kSfbCol + 16u * static_cast<uint32_t>(mw);
-      const uint64_t sfb_desc = sdesc_sf_32x16(smem_u32(sfb_const));
+      if constexpr (!A4) {
+        const uint64_t sfb_desc = sdesc_sf_32x16(smem_u32(sfb_const));
 #pragma unroll
-      for (int j = 0; j < 4; ++j) tc_cp_32x128b_warpx4(sfb + 4 * j, sfb_desc);
+        for (int j = 0; j < 4; ++j) tc_cp_32x128b_warpx4(sfb + 4 * j, sfb_desc);
+      }
       int stage = mw;
       uint32_t phase = 0;
       int acc = 0;
@@ -332,16 +382,33 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
             tc_fence_after();
             uint8_t *st = smem + stage * C::kStageBytes;
             const uint32_t sfa = tmem + kSfaCol + 4u * static_cast<uint32_t>(stage);
-            tc_cp_32x128b_warpx4(sfa, sdesc_sf_32x16(smem_u32(st + kWSmem + C::kXSmem)));
+            tc_cp_32x128b_warpx4(sfa, sdesc_sf_32x16(smem_u32(st + C::kSfOff)));
             const uint32_t a_base = smem_u32(st);
-            const uint32_t b_base = smem_u32(st + kWSmem);
+            const uint32_t b_base = smem_u32(st + C::kWBytes);
+            if constexpr (A4) {
+              // activation scales: column 4a + (token / 32) of this stage's slot holds
+              // tokens 128a .. 128a + 127 of the tile, one byte per 32 K
+              const uint32_t sfbs = tmem + kSfbColA4 + 8u * static_cast<uint32_t>(stage);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sdesc_sw128_kmajor(a_base + 32u * kk);
-              const uint64_t bd = sdesc_sw128_kmajor(b_base + 32u * kk);
-              const uint32_t idesc = idesc_mxf8f6f4_e2m1_e4m3(BT, kk, 0);
-              tc_mma_mxf8f6f4(d_tmem, ad, bd, idesc, sfa | (static_cast<uint32_t>(kk) << 30), sfb,
-                              (!first || kk > 0) ? 1u : 0u);
+              for (int a = 0; a < C::kXAtoms; ++a)
+                tc_cp_32x128b_warpx4(sfbs + 4u * a, sdesc_sf_32x16(smem_u32(st + C::kSfOff + kSfBytes * (1 + a))));
+              // two MMAs of K = 64; scale id 0 / 2 picks the byte pair of 32-K blocks (0,1) / (2,3)
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk) {
+                const uint32_t id = 2u * kk;
+                tc_mma_mxf4(d_tmem, sdesc_sw64_kmajor(a_base + 32u * kk), sdesc_sw64_kmajor(b_base + 32u * kk),
+                            idesc_mxf4_e2m1(BT, id, id), sfa | (id << 30), sfbs | (id << 30),
+                            (!first || kk > 0) ? 1u : 0u);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = sdesc_sw128_kmajor(a_base + 32u * kk);
+                const uint64_t bd = sdesc_sw128_kmajor(b_base + 32u * kk);
+                const uint32_t idesc = idesc_mxf8f6f4_e2m1_e4m3(BT, kk, 0);
+                tc_mma_mxf8f6f4(d_tmem, ad, bd, idesc, sfa | (static_cast<uint32_t>(kk) << 30), sfb,
+                                (!first || kk > 0) ? 1u : 0u);
+              }
             }
             first = false;
             tc_commit(&empty_bar[stage]);
@@ -432,7 +499,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
 #pragma unroll
           for (int j = 0; j < CH; ++j) {
             const int t = t0 + c0 + j;
-            const float sc = (t < p.M) ? __ldg(p.s + t) : 0.f;
+            const float sc = (t < p.M) ? out_scale(t) : 0.f;
             stg[j * 128 + q * 32 + lane] = f32_to_bf16_rn(v[j] * sc);
           }
           fence_proxy_async_smem();
@@ -447,7 +514,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
               const int t = t0 + c0 + j;
-              if (t < p.M) p.c[static_cast<size_t>(t) * p.ldc + n] = f32_to_bf16_rn(v[j] * __ldg(p.s + t));
+              if (t < p.M) p.c[static_cast<size_t>(t) * p.ldc + n] = f32_to_bf16_rn(v[j] * out_scale(t));
             }
           }
         } else if (p.cluster) {
@@ -530,7 +597,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
             }
             const int t = tbase + j;
             if (t < p.M) {
-              const float sc = __ldg(p.s + t);
+              const float sc = out_scale(t);
               const int n0 = nt * 128 + qd * 4;
               uint16_t *dst = p.c + static_cast<size_t>(t) * p.ldc + n0;
               const float o[4] = {a4.x * sc, a4.y * sc, a4.z * sc, a4.w * sc};
@@ -561,8 +628,8 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
         if (*is_last == 1) {
           __threadfence();
           const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (128 * BT);
-          reduce_partials_store<BT>(base, p.splits, min(BT, p.M - t0), nt * 128, p.N, p.s, t0, p.c, p.ldc,
-                                    ew * 32 + lane, 128);
+          reduce_partials_store<BT>(base, p.splits, min(BT, p.M - t0), nt * 128, p.N, A4 ? nullptr : p.s, t0, p.c,
+                                    p.ldc, ew * 32 + lane, 128);
         }
         if (*is_last && ew == 0 && lane == 0) p.counters[tile] = 0;
         named_bar_sync(1, 128);
@@ -596,27 +663,47 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
   if (p.cluster) cluster_sync_all();
 }
 
-template <int BT>
-int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M, int64_t N, int64_t K, uint16_t *c,
-              int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st) {
-  using C = Cfg<BT>;
+template <int BT, bool A4>
+int launch_bt(const uint8_t *q, const float *s, const uint8_t *xsf, const uint8_t *packed, int64_t M, int64_t N,
+              int64_t K, uint16_t *c, int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st) {
+  using C = Cfg<BT, A4>;
   const int64_t NT = ceil_div(N, 128);
   CUtensorMap tm_w, tm_x, tm_c;
-  {
-    const uint64_t dims[3] = {128, 128, static_cast<uint64_t>(NT * pl.KB)};
-    const uint64_t strides[2] = {64, 8192};
-    const uint32_t box[3] = {128, 128, 1};
-    if (encode_tiled(&tm_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t *>(packed), dims, strides,
-                     box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-      return R4_ERR_CUDA;
-  }
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(K)};
-    const uint32_t box[2] = {128, static_cast<uint32_t>(BT)};
-    if (encode_tiled(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(q), dims, strides, box,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-      return R4_ERR_CUDA;
+  if constexpr (A4) {
+    // packed e2m1 bytes as they are: 128 rows x 64 bytes per tile, 64-byte swizzle
+    {
+      const uint64_t dims[3] = {64, 128, static_cast<uint64_t>(NT * pl.KB)};
+      const uint64_t strides[2] = {64, 8192};
+      const uint32_t box[3] = {64, 128, 1};
+      if (encode_tiled(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(packed), dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
+        return R4_ERR_CUDA;
+    }
+    {
+      const uint64_t dims[2] = {static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M)};
+      const uint64_t strides[1] = {static_cast<uint64_t>(K / 2)};
+      const uint32_t box[2] = {64, static_cast<uint32_t>(BT)};
+      if (encode_tiled(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(q), dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
+        return R4_ERR_CUDA;
+    }
+  } else {
+    {
+      const uint64_t dims[3] = {128, 128, static_cast<uint64_t>(NT * pl.KB)};
+      const uint64_t strides[2] = {64, 8192};
+      const uint32_t box[3] = {128, 128, 1};
+      if (encode_tiled(&tm_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t *>(packed), dims, strides,
+                       box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return R4_ERR_CUDA;
+    }
+    {
+      const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+      const uint64_t strides[1] = {static_cast<uint64_t>(K)};
+      const uint32_t box[2] = {128, static_cast<uint32_t>(BT)};
+      if (encode_tiled(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(q), dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return R4_ERR_CUDA;
+    }
   }
   // Output through TMA tensor stores when C's base, row stride and row length
   // are 16-byte multiples. (Measured on GB300: a tensor store whose row ends
@@ -634,6 +721,7 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.KB = pl.KB;
+  p.xsf = xsf;
   p.t_tiles = pl.t_tiles;
   p.splits = pl.splits;
   p.kb_per_split = pl.kb_per_split;
@@ -652,30 +740,37 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M
   p.counters = reinterpret_cast<int *>(ws);
   p.partials = ws ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) + pl.counters_bytes) : nullptr;
   p.err = device_error_word();
-  auto kern = w4a8_mxf8f6f4_kernel<BT>;
+  auto kern = w4a8_mxf8f6f4_kernel<BT, A4>;
   if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::kSmemBytes) != cudaSuccess) return R4_ERR_CUDA;
   const cudaError_t le =
       pl.cluster ? launch_pdl_cluster(kern, dim3(pl.grid), dim3(C::kThreads), C::kSmemBytes, st, pl.splits, tm_w, tm_x,
                                       tm_c, p)
                  : launch_pdl(kern, dim3(pl.grid), dim3(C::kThreads), C::kSmemBytes, st, tm_w, tm_x, tm_c, p);
   if (le != cudaSuccess) return R4_ERR_CUDA;
-  set_last_kernel(BT == 16    ? "w4a8_mxf8f6f4_kernel<16>"
-                  : BT == 32  ? "w4a8_mxf8f6f4_kernel<32>"
-                  : BT == 64  ? "w4a8_mxf8f6f4_kernel<64>"
-                  : BT == 128 ? "w4a8_mxf8f6f4_kernel<128>"
-                              : "w4a8_mxf8f6f4_kernel<256>");
+  if constexpr (A4)
+    set_last_kernel(BT == 16    ? "w4a8_mxf8f6f4_kernel<16,mxf4>"
+                    : BT == 32  ? "w4a8_mxf8f6f4_kernel<32,mxf4>"
+                    : BT == 64  ? "w4a8_mxf8f6f4_kernel<64,mxf4>"
+                    : BT == 128 ? "w4a8_mxf8f6f4_kernel<128,mxf4>"
+                                : "w4a8_mxf8f6f4_kernel<256,mxf4>");
+  else
+    set_last_kernel(BT == 16    ? "w4a8_mxf8f6f4_kernel<16>"
+                    : BT == 32  ? "w4a8_mxf8f6f4_kernel<32>"
+                    : BT == 64  ? "w4a8_mxf8f6f4_kernel<64>"
+                    : BT == 128 ? "w4a8_mxf8f6f4_kernel<128>"
+                                : "w4a8_mxf8f6f4_kernel<256>");
   return cudaGetLastError() == cudaSuccess ? R4_OK : R4_ERR_CUDA;
 }
 
 // Co-resident clusters of `s` CTAs (2..8) the BT kernel can have on this
 // device (0: none / unsupported). Cached after the first query.
-template <int BT>
+template <int BT, bool A4>
 int max_clusters_bt(int s) {
-  using C = Cfg<BT>;
+  using C = Cfg<BT, A4>;
   static int cache[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};   // 0 unknown, -1 none
   if (s < 2 || s > 8) return 0;
   if (cache[s] != 0) return cache[s] > 0 ? cache[s] : 0;
-  auto kern = w4a8_mxf8f6f4_kernel<BT>;
+  auto kern = w4a8_mxf8f6f4_kernel<BT, A4>;
   int n = 0;
   if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::kSmemBytes) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
@@ -696,13 +791,13 @@ int max_clusters_bt(int s) {
   return n > 0 ? n : 0;
 }
 
-int max_clusters(int bt, int s) {
+int max_clusters(int bt, int s, bool a4) {
   switch (bt) {
-    case 16: return max_clusters_bt<16>(s);
-    case 32: return max_clusters_bt<32>(s);
-    case 64: return max_clusters_bt<64>(s);
-    case 128: return max_clusters_bt<128>(s);
-    case 256: return max_clusters_bt<256>(s);
+    case 16: return a4 ? max_clusters_bt<16, true>(s) : max_clusters_bt<16, false>(s);
+    case 32: return a4 ? max_clusters_bt<32, true>(s) : max_clusters_bt<32, false>(s);
+    case 64: return a4 ? max_clusters_bt<64, true>(s) : max_clusters_bt<64, false>(s);
+    case 128: return a4 ? max_clusters_bt<128, true>(s) : max_clusters_bt<128, false>(s);
+    case 256: return a4 ? max_clusters_bt<256, true>(s) : max_clusters_bt<256, false>(s);
     default: return 0;
   }
 }
@@ -720,15 +815,23 @@ int max_clusters(int bt, int s) {
 // prefill shapes. Prefill tiles (BT >= 128) are never split once the tile
 // count is a quarter of the SM count: there the partial tiles cost more than
 // the idle SMs.
-GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
+//
+// The W4A4 variant (a4) uses the same model with its own bytes and rate per
+// K block (packed e2m1 activations, two scale atoms, the mxf4 rate is twice
+// the f8 one) and one more rule: a token tile starts on a 128-token scale
+// atom (tiles of 128 or 256 tokens, or a single tile of up to 64 tokens
+// starting at token 0), so that every activation scale of a tile sits at the
+// start of the atom copied into tensor memory.
+static GemmPlan plan_mx(int64_t M, int64_t N, int64_t K, int sms, bool a4) {
   GemmPlan pl;
   int bt = options().w4a8_token_tile;
+  if (a4 && bt != 0 && bt < 128 && M > bt) bt = 0;   // a forced small tile must hold every token
   // 33..64 tokens against a narrow weight (few 128-row tiles) run as two
   // 32-token tiles: twice the tiles to spread over the SMs (measured: M=64,
   // 2048x5120 9.2 vs 10.2 us; at 5120x17408 the 64-token tile wins, 19.4 vs
   // 25.3 us).
   if (bt == 0)
-    bt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? (ceil_div(N, 128) <= 24 ? 32 : 64) : M <= 128 ? 128 : 256;
+    bt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? ((!a4 && ceil_div(N, 128) <= 24) ? 32 : 64) : M <= 128 ? 128 : 256;
   pl.BT = bt;
   pl.n_tiles = static_cast<int>(ceil_div(N, 128));
   pl.t_tiles = static_cast<int>(ceil_div(M, bt));
@@ -736,8 +839,11 @@ GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
   const int64_t tiles = static_cast<int64_t>(pl.n_tiles) * pl.t_tiles;
   // 16-token partial tiles (8 KiB) sum faster per byte than larger ones
   // (fitted: 2048x5120 decode, 5 splits 6.1 us vs 4 splits 7.3 us).
-  const double hbm = 6.0e12, sm_bw = 70e9, sm_flops = 4.5e15 / 152.0, red_bw = bt <= 16 ? 40e9 : 20e9;
-  const double kb_bytes = 128.0 * 128 * 0.5 + 512 + 128.0 * bt;      // weight + scales + activations
+  const double hbm = 6.0e12, sm_bw = 70e9, sm_flops = (a4 ? 9.0e15 : 4.5e15) / 152.0,
+               red_bw = bt <= 16 ? 40e9 : 20e9;
+  // weight + its scales + activations (+ their scale atoms for W4A4)
+  const double kb_bytes = a4 ? 128.0 * 128 * 0.5 + 512 + 64.0 * bt + 512.0 * (bt > 128 ? 2 : 1)
+                             : 128.0 * 128 * 0.5 + 512 + 128.0 * bt;
   const double kb_flops = 2.0 * 128 * bt * 128;
   const double part_bytes = 128.0 * bt * 4;
   const double xchg_s = (bt <= 64 ? 2.5e-6 : 1.0e-6) * ((bt + 31) / 32);   // one cluster exchange per 32 tokens
@@ -769,7 +875,7 @@ GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
     // from the drained pipeline stages in one round (per-32-token rounds ate
     // the gain at 256 tokens: M=256, 5120x17408, 3 splits 49.9 us vs 49.8 us
     // unsplit).
-    int ncl = (options().cluster_split && bt >= 32 && s >= 2 && s <= 6) ? w4a8::max_clusters(bt, s) : 0;
+    int ncl = (options().cluster_split && bt >= 32 && s >= 2 && s <= 6) ? w4a8::max_clusters(bt, s, a4) : 0;
     if (bt >= 128 && !forced_s && tiles > ncl) ncl = 0;
     if (bt >= 128 && !forced_s && s > 1 && ncl == 0 && !prefill_ws_ok) continue;
     double t;
@@ -813,14 +919,29 @@ GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) {
   return pl;
 }
 
+GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) { return plan_mx(M, N, K, sms, false); }
+GemmPlan plan_w4a4(int64_t M, int64_t N, int64_t K, int sms) { return plan_mx(M, N, K, sms, true); }
+
 int launch_gemm_w4a8(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M, int64_t N, int64_t K,
                      uint16_t *c, int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st) {
   switch (pl.BT) {
-    case 16: return w4a8::launch_bt<16>(q, s, packed, M, N, K, c, ldc, ws, pl, st);
-    case 32: return w4a8::launch_bt<32>(q, s, packed, M, N, K, c, ldc, ws, pl, st);
-    case 64: return w4a8::launch_bt<64>(q, s, packed, M, N, K, c, ldc, ws, pl, st);
-    case 128: return w4a8::launch_bt<128>(q, s, packed, M, N, K, c, ldc, ws, pl, st);
-    case 256: return w4a8::launch_bt<256>(q, s, packed, M, N, K, c, ldc, ws, pl, st);
+    case 16: return w4a8::launch_bt<16, false>(q, s, nullptr, packed, M, N, K, c, ldc, ws, pl, st);
+    case 32: return w4a8::launch_bt<32, false>(q, s, nullptr, packed, M, N, K, c, ldc, ws, pl, st);
+    case 64: return w4a8::launch_bt<64, false>(q, s, nullptr, packed, M, N, K, c, ldc, ws, pl, st);
+    case 128: return w4a8::launch_bt<128, false>(q, s, nullptr, packed, M, N, K, c, ldc, ws, pl, st);
+    case 256: return w4a8::launch_bt<256, false>(q, s, nullptr, packed, M, N, K, c, ldc, ws, pl, st);
+    default: return R4_ERR_INVALID_ARG;
+  }
+}
+
+int launch_gemm_w4a4(const uint8_t *q, const uint8_t *q_scale, const uint8_t *packed, int64_t M, int64_t N,
+                     int64_t K, uint16_t *c, int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st) {
+  switch (pl.BT) {
+    case 16: return w4a8::launch_bt<16, true>(q, nullptr, q_scale, packed, M, N, K, c, ldc, ws, pl, st);
+    case 32: return w4a8::launch_bt<32, true>(q, nullptr, q_scale, packed, M, N, K, c, ldc, ws, pl, st);
+    case 64: return w4a8::launch_bt<64, true>(q, nullptr, q_scale, packed, M, N, K, c, ldc, ws, pl, st);
+    case 128: return w4a8::launch_bt<128, true>(q, nullptr, q_scale, packed, M, N, K, c, ldc, ws, pl, st);
+    case 256: return w4a8::launch_bt<256, true>(q, nullptr, q_scale, packed, M, N, K, c, ldc, ws, pl, st);
     default: return R4_ERR_INVALID_ARG;
   }
 }

@@ -172,6 +172,77 @@ __global__ void quant_mxfp4_weight_kernel(const float *__restrict__ w, int64_t N
   scale[row * nblk + kb] = static_cast<uint8_t>(code);
 }
 
+// MXFP4 activations for the W4A4 GEMM: the OCP MX rule of the weights, per
+// 32 K of each token. One warp quantizes 256 consecutive columns of one
+// token: lane l holds columns [8l, 8l + 8) as one 16-byte load, lanes
+// 4j .. 4j + 3 form 32-element block j (their maximum by two shuffles), and
+// each lane packs its 8 codes into one 32-bit store (column 2i in the low
+// nibble of byte i). The four scale codes of a 128-K block are one 32-bit
+// word of the token's scale atom row (byte j = 32-K block j), OR-combined
+// over the 16 lanes by shuffles and stored by one lane:
+//   scale atom (a, kb): 512 bytes, byte 16 r0 + 4 r1 + j = token
+//   128 a + 32 r1 + r0, 32-K block 4 kb + j  (a = token / 128).
+// Blocks past K and padding tokens (M .. the atoms' end) get code 127 (x1).
+// Blocks of the grid past `real_blocks` write those padding tokens' words.
+__global__ void __launch_bounds__(256) quant_mxfp4_act_kernel(const uint16_t *__restrict__ x, int M, int K,
+                                                              int64_t ldx, int segs, int KB, int real_blocks,
+                                                              int pad_tokens, uint8_t *__restrict__ q,
+                                                              uint8_t *__restrict__ sf) {
+  if (threadIdx.x == 0) pdl_launch_dependents();   // the next kernel may start its weight stream
+  pdl_wait();                                       // x (and the q, sf buffers) follow the stream order
+  const int lane = threadIdx.x & 31;
+  if (static_cast<int>(blockIdx.x) >= real_blocks) {
+    // padding tokens M .. M + pad_tokens: every word of their atom rows is 0x7F7F7F7F
+    const int64_t i = static_cast<int64_t>(blockIdx.x - real_blocks) * blockDim.x + threadIdx.x;
+    if (i >= static_cast<int64_t>(pad_tokens) * KB) return;
+    const int t = M + static_cast<int>(i / KB), kb = static_cast<int>(i % KB);
+    const int r = t & 127;
+    *reinterpret_cast<uint32_t *>(sf + (static_cast<size_t>(t >> 7) * KB + kb) * 512 + 16 * (r & 31) + 4 * (r >> 5)) =
+        0x7F7F7F7Fu;
+    return;
+  }
+  const int64_t wg = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (wg >= static_cast<int64_t>(M) * segs) return;   // whole warps only
+  const int row = static_cast<int>(wg / segs), seg = static_cast<int>(wg % segs);
+  const int k = seg * 256 + lane * 8;
+  const bool in = k < K;
+  const uint4 v = in ? __ldg(reinterpret_cast<const uint4 *>(x + static_cast<size_t>(row) * ldx + k))
+                     : make_uint4(0, 0, 0, 0);
+  float a = absmax8(v);
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  int X = 0;
+  if (a > 0.f) {
+    int e;
+    frexpf(a, &e);           // a = m 2^e, 0.5 <= m < 1
+    X = (e - 1) - 2;         // floor(log2 amax) - emax(e2m1)
+  }
+  int code = X + 127;
+  code = code < 0 ? 0 : (code > 254 ? 254 : code);
+  X = code - 127;
+  if (in) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float f = (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
+      const uint32_t c =
+          static_cast<uint32_t>(__nv_cvt_float_to_fp4(ldexpf(f, -X), __NV_E2M1, cudaRoundNearest)) & 0xFu;
+      out |= c << (4 * i);
+    }
+    *reinterpret_cast<uint32_t *>(q + static_cast<size_t>(row) * (K / 2) + k / 2) = out;
+  }
+  uint32_t word = static_cast<uint32_t>(code) << (8 * ((lane >> 2) & 3));
+  word |= __shfl_xor_sync(0xffffffffu, word, 4);
+  word |= __shfl_xor_sync(0xffffffffu, word, 8);
+  const int kb = seg * 2 + (lane >> 4);
+  if ((lane & 15) == 0 && kb < KB) {
+    const int r = row & 127;
+    *reinterpret_cast<uint32_t *>(sf + (static_cast<size_t>(row >> 7) * KB + kb) * 512 + 16 * (r & 31) + 4 * (r >> 5)) =
+        word;
+  }
+}
+
 // 128x128 block e4m3: one CTA (256 threads) per block.
 __global__ void __launch_bounds__(256) quant_blockfp8_weight_kernel(const float *__restrict__ w, int64_t N,
                                                                     int64_t K, uint8_t *__restrict__ q,
@@ -300,6 +371,22 @@ cudaError_t launch_quant_mxfp4_weight(const float *w, int64_t N, int64_t K, uint
   const int64_t blocks = N * (K / 32);
   quant_mxfp4_weight_kernel<<<static_cast<unsigned>(ceil_div(blocks, 256)), 256, 0, st>>>(w, N, K, packed, scale);
   set_last_kernel("quant_mxfp4_weight_kernel");
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_mxfp4_act(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, uint8_t *sf,
+                                   cudaStream_t st) {
+  const int segs = static_cast<int>(ceil_div(K, 256));
+  const int KB = static_cast<int>(ceil_div(K, 128));
+  const int64_t real_blocks = ceil_div(M * segs, 8);
+  const int64_t pad_tokens = mx_act_tokens_padded(M) - M;
+  const int64_t pad_blocks = ceil_div(pad_tokens * KB, 256);
+  const dim3 grid(static_cast<unsigned>(real_blocks + pad_blocks));
+  const cudaError_t e = launch_pdl(quant_mxfp4_act_kernel, grid, dim3(256), 0, st, x, static_cast<int>(M),
+                                   static_cast<int>(K), ldx, segs, KB, static_cast<int>(real_blocks),
+                                   static_cast<int>(pad_tokens), q, sf);
+  if (e != cudaSuccess) return e;
+  set_last_kernel("quant_mxfp4_act_kernel");
   return cudaGetLastError();
 }
 

@@ -104,6 +104,7 @@ struct GemmPlan {
 };
 
 GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms);
+GemmPlan plan_w4a4(int64_t M, int64_t N, int64_t K, int sms);
 GemmPlan plan_blockfp8(int64_t M, int64_t N, int64_t K, int sms);
 
 // ------------------------------------------------------------------ prepack layout
@@ -121,6 +122,13 @@ inline size_t mx_packed_bytes(int64_t N, int64_t K) {
   return mx_packed_codes_bytes(N, K) + static_cast<size_t>(ceil_div(N, 128) * ceil_div(K, 128) * kMxTileSfBytes);
 }
 inline size_t fp8_packed_codes_bytes(int64_t N, int64_t K) { return static_cast<size_t>(N * K); }
+// MXFP4 activation scales (W4A4): 512-byte atoms of 128 tokens x 128 K, for
+// the token count rounded up to a multiple of 256 (so a 256-token tile
+// always has both of its atoms).
+inline int64_t mx_act_tokens_padded(int64_t M) { return ceil_div(M, 256) * 256; }
+inline size_t mx_act_scale_bytes(int64_t M, int64_t K) {
+  return static_cast<size_t>(mx_act_tokens_padded(M) / 128 * ceil_div(K, 128) * 512);
+}
 inline size_t fp8_packed_bytes(int64_t N, int64_t K) {
   return round_up(fp8_packed_codes_bytes(N, K) + static_cast<size_t>((N / 128) * (K / 128) * 4), 256);
 }
@@ -133,6 +141,8 @@ cudaError_t launch_silu_mul_quant(const uint16_t *gu, int64_t M, int64_t N, uint
 cudaError_t launch_check_quotients(unsigned long long *count, float *example, cudaStream_t st);
 cudaError_t launch_quant_act(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int64_t group, uint8_t *q,
                              float *s, cudaStream_t st);
+cudaError_t launch_quant_mxfp4_act(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, uint8_t *sf,
+                                   cudaStream_t st);
 cudaError_t launch_quant_mxfp4_weight(const float *w, int64_t N, int64_t K, uint8_t *packed, uint8_t *scale,
                                       cudaStream_t st);
 cudaError_t launch_quant_blockfp8_weight(const float *w, int64_t N, int64_t K, uint8_t *q, float *s,
@@ -144,6 +154,8 @@ cudaError_t launch_prepack_blockfp8(const uint8_t *w, const float *ws, int64_t N
 // Returns an r4_status (tensor-map encoding can fail with R4_ERR_CUDA).
 int launch_gemm_w4a8(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M, int64_t N, int64_t K,
                      uint16_t *c, int64_t ldc, void *ws, const GemmPlan &plan, cudaStream_t st);
+int launch_gemm_w4a4(const uint8_t *q, const uint8_t *q_scale, const uint8_t *packed, int64_t M, int64_t N,
+                     int64_t K, uint16_t *c, int64_t ldc, void *ws, const GemmPlan &plan, cudaStream_t st);
 int launch_gemm_blockfp8(const uint8_t *q, const float *As, const uint8_t *packed, int64_t M, int64_t N,
                          int64_t K, uint16_t *c, int64_t ldc, void *ws, const GemmPlan &plan, cudaStream_t st);
 // Tensor-core issue-rate probe (kind 1 mxf8f6f4, 2 f8f6f4, 3 mxf4; n = 128 or 256).

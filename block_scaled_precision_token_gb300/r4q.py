@@ -22,7 +22,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "r4q.h")
 
 R4_OK, R4_ERR_INVALID_ARG, R4_ERR_UNSUPPORTED_SHAPE, R4_ERR_MISALIGNED = 0, 1, 2, 3
 R4_ERR_WORKSPACE, R4_ERR_CUDA, R4_ERR_DEVICE_TIMEOUT = 4, 5, 6
-R4_OP_W4A8_MXFP4, R4_OP_BLOCKFP8, R4_OP_BF16_SKINNY = 1, 2, 3
+R4_OP_W4A8_MXFP4, R4_OP_BLOCKFP8, R4_OP_BF16_SKINNY, R4_OP_W4A4_MXFP4 = 1, 2, 3, 4
 
 
 class R4Error(RuntimeError):
@@ -56,6 +56,9 @@ _SIGS = {
     "r4_silu_mul_quant_fp8": ([_P, _I64, _I64, _P, _P, _P], _I),
     "r4_check_quotients": ([_P, _P, _P], _I),
     "r4_mma_peak": ([_I, _I, _I, _I, _P], _I),
+    "r4_quant_mxfp4_act_scale_bytes": ([_I64, _I64], _SZ),
+    "r4_quant_mxfp4_act": ([_P, _I64, _I64, _I64, _P, _P, _SZ, _P], _I),
+    "r4_gemm_w4a4_mxfp4": ([_P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
 }
 
 
@@ -156,6 +159,16 @@ def r4_quantize_blockfp8_weight(w, N, K, q, s, stream=None):
            "r4_quantize_blockfp8_weight")
 
 
+def r4_quant_mxfp4_act_scale_bytes(M, K):
+    return int(lib().r4_quant_mxfp4_act_scale_bytes(M, K))
+
+
+def r4_quant_mxfp4_act(x, M, K, ldx, q, scale, stream=None):
+    _need(x, torch.bfloat16, "x"); _need(q, torch.uint8, "q"); _need(scale, torch.uint8, "scale")
+    _check(lib().r4_quant_mxfp4_act(_ptr(x), M, K, ldx, _ptr(q), _ptr(scale), scale.numel(), _stream(stream)),
+           "r4_quant_mxfp4_act")
+
+
 def r4_prepack_mxfp4_bytes(N, K):
     return int(lib().r4_prepack_mxfp4_bytes(N, K))
 
@@ -199,6 +212,13 @@ def r4_gemm_w4a8_mxfp4_noalloc(q, s, packed, M, N, K, c, ldc, stream=None):
     _need(q, torch.uint8, "q"); _need(s, torch.float32, "s"); _need(c, torch.bfloat16, "c")
     _check(lib().r4_gemm_w4a8_mxfp4_noalloc(_ptr(q), _ptr(s), _ptr(packed), M, N, K, _ptr(c), ldc, _stream(stream)),
            "r4_gemm_w4a8_mxfp4_noalloc")
+
+
+def r4_gemm_w4a4_mxfp4(q, q_scale, packed, M, N, K, c, ldc, workspace=None, stream=None):
+    _need(q, torch.uint8, "q"); _need(q_scale, torch.uint8, "q_scale"); _need(c, torch.bfloat16, "c")
+    wp, wb = _ws(workspace)
+    _check(lib().r4_gemm_w4a4_mxfp4(_ptr(q), _ptr(q_scale), _ptr(packed), M, N, K, _ptr(c), ldc, wp, wb,
+                                    _stream(stream)), "r4_gemm_w4a4_mxfp4")
 
 
 def r4_gemm_blockfp8(q, As, packed, M, N, K, c, ldc, workspace=None, stream=None):
@@ -249,6 +269,17 @@ def quant_fp8(x, group=None, stream=None):
     s = torch.empty((M,) if group is None else (M, K // g), dtype=torch.float32, device=x.device)
     r4_quant_fp8_per_token(x, M, K, x.stride(0), g, q, s, stream)
     return q, s
+
+
+def quant_mxfp4(x, stream=None):
+    """x bf16 [M, K] (row stride may exceed K) -> (q uint8 [M, K/2] packed e2m1,
+    scale uint8 atoms for r4_gemm_w4a4_mxfp4)."""
+    M, K = x.shape
+    assert x.stride(1) == 1
+    q = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
+    sc = torch.empty(r4_quant_mxfp4_act_scale_bytes(M, K), dtype=torch.uint8, device=x.device)
+    r4_quant_mxfp4_act(x, M, K, x.stride(0), q, sc, stream)
+    return q, sc
 
 
 def add_rmsnorm_quant(y, residual, weight, eps, residual_out=None, stream=None):
@@ -316,6 +347,15 @@ def gemm_w4a8(q, s, packed, N, K, ws=None, out=None, stream=None):
     if ws is None:
         ws = workspace(R4_OP_W4A8_MXFP4, M, N, K, q.device)
     r4_gemm_w4a8_mxfp4(q, s, packed, M, N, K, c, c.stride(0), ws, stream)
+    return c
+
+
+def gemm_w4a4(q, q_scale, packed, N, K, ws=None, out=None, stream=None):
+    M = q.shape[0]
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=q.device) if out is None else out
+    if ws is None:
+        ws = workspace(R4_OP_W4A4_MXFP4, M, N, K, q.device)
+    r4_gemm_w4a4_mxfp4(q, q_scale, packed, M, N, K, c, c.stride(0), ws, stream)
     return c
 
 

@@ -70,7 +70,7 @@ enum r4_status {
 };
 
 /* GEMM identifiers for r4_gemm_workspace_bytes(). */
-enum r4_gemm_op { R4_OP_W4A8_MXFP4 = 1, R4_OP_BLOCKFP8 = 2, R4_OP_BF16_SKINNY = 3 };
+enum r4_gemm_op { R4_OP_W4A8_MXFP4 = 1, R4_OP_BLOCKFP8 = 2, R4_OP_BF16_SKINNY = 3, R4_OP_W4A4_MXFP4 = 4 };
 
 int r4_version(void);                 /* (major << 16) | minor */
 const char *r4_status_string(int status);
@@ -192,6 +192,36 @@ int r4_quantize_blockfp8_weight(const float *w, int64_t N, int64_t K, uint8_t *q
                                 float *s, r4_stream_t stream);
 
 /*
+ * r4_quant_mxfp4_act -- MXFP4 activation quantization for the W4A4 GEMM.
+ * Source: "radiance_mxfp4.py", module docstring and _debug_compare: the W4A4
+ * path that the page's W4A8 kernel replaces quantizes the activations to
+ * MXFP4 (the page measures its error against the exact product: relative
+ * Frobenius 0.1119, against 0.0265 for W4A8). The page does not print that
+ * quantizer's rule; this library reads it as the OCP MX v1.0 rule of the
+ * weights (r4_quantize_mxfp4_weight), per 32 K of each token:
+ *   X = floor(log2(amax)) - 2 (all-zero block: X = 0), scale code X + 127
+ *   clamped to [0, 254], element = e2m1_rne_sat(x / 2^X).
+ *   x      bf16 [M, ldx] row-major, first K columns used; 16-byte aligned.
+ *   q      uint8 [M, K/2] packed e2m1, element 2j in the low nibble of byte j
+ *          (the checkpoint order of the weights); 16-byte aligned.
+ *   scale  the ue8m0 scale codes in the GEMM's scale-atom layout, 16-byte
+ *          aligned, at least r4_quant_mxfp4_act_scale_bytes(M, K) bytes:
+ *          atoms of 512 bytes, atom (a, kb) at byte offset
+ *          (a * ceil(K/128) + kb) * 512 for tokens [128 a, 128 a + 128) and
+ *          K block [128 kb, 128 kb + 128); inside it, byte 16 r0 + 4 r1 + j
+ *          is the scale of token 128 a + 32 r1 + r0, 32-K block 4 kb + j --
+ *          the order in which tcgen05.cp 32x128b.warpx4 lays a scale block
+ *          across tensor memory, the same as the weight's prepacked atoms.
+ *          Tokens are padded to a multiple of 256 and K to a multiple of
+ *          128; the padding holds code 127 (x1).
+ * Requirements: M >= 1, K >= 32, K % 32 == 0, ldx >= K, ldx % 8 == 0.
+ * Non-finite input gives unspecified codes for its 32-element block.
+ */
+size_t r4_quant_mxfp4_act_scale_bytes(int64_t M, int64_t K);
+int r4_quant_mxfp4_act(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q,
+                       uint8_t *scale, size_t scale_bytes, r4_stream_t stream);
+
+/*
  * r4_prepack_mxfp4 -- one-time permutation of a checkpoint-order MXFP4 weight
  * into the GEMM-native layout (no re-quantization). Source of the idea:
  * "radiance_mxfp4.py", permute_w (a byte permutation done once at load so the
@@ -251,6 +281,25 @@ size_t r4_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
  * Requirements: M >= 1, N >= 1, K % 32 == 0, ldc >= N.
  */
 int r4_gemm_w4a8_mxfp4(const uint8_t *q, const float *s, const void *packed, int64_t M,
+                       int64_t N, int64_t K, uint16_t *c, int64_t ldc, void *workspace,
+                       size_t workspace_bytes, r4_stream_t stream);
+
+/*
+ * r4_gemm_w4a4_mxfp4 -- the W4A4 variant, MXFP4 activations x MXFP4 weights:
+ *   C = bf16( sum_k e2m1(q[m,k]) 2^(a[m,k/32]-127) * e2m1(w[n,k]) 2^(e[n,k/32]-127) ).
+ * Source: "radiance_mxfp4.py", module docstring and _debug_compare (the W4A4
+ * path). tcgen05 kind::mxf4 (twice the f8 rate): both operands packed e2m1
+ * in shared memory, both ue8m0 scales in tensor memory, so there is no
+ * per-token epilogue scale. Same kernel structure, schedules and split-K as
+ * r4_gemm_w4a8_mxfp4 (workspace: r4_gemm_workspace_bytes(R4_OP_W4A4_MXFP4, ...)),
+ * with token tiles of 128 or 256, or one tile of up to 64 tokens.
+ *   q        packed e2m1 [M, K/2] from r4_quant_mxfp4_act, 16-byte aligned.
+ *   q_scale  its scale atoms (r4_quant_mxfp4_act), 16-byte aligned.
+ *   packed   prepacked weight from r4_prepack_mxfp4(N, K) (the W4A8 weight).
+ *   c        bf16 [M, ldc]; columns [0, N) are written, nothing else.
+ * Requirements: M >= 1, N >= 1, K % 32 == 0, K >= 128, ldc >= N.
+ */
+int r4_gemm_w4a4_mxfp4(const uint8_t *q, const uint8_t *q_scale, const void *packed, int64_t M,
                        int64_t N, int64_t K, uint16_t *c, int64_t ldc, void *workspace,
                        size_t workspace_bytes, r4_stream_t stream);
 
