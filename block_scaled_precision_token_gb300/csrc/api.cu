@@ -179,7 +179,14 @@ int r4_set_option(int key, int64_t value) {
     case 3: options().fp8_splits = static_cast<int>(value); return R4_OK;
     case 4: options().pdl = value ? 1 : 0; return R4_OK;
     case 14: options().early_weights = value ? 1 : 0; return R4_OK;
-    case 5: options().l2_prefetch = value ? 1 : 0; return R4_OK;
+    case 15:
+      if (value < 0 || value > 4) return R4_ERR_INVALID_ARG;
+      options().skinny_groups = static_cast<int>(value);
+      return R4_OK;
+    case 5:
+      if (value < 0 || value > 2) return R4_ERR_INVALID_ARG;
+      options().l2_prefetch = static_cast<int>(value);
+      return R4_OK;
     case 6: options().cluster_split = value ? 1 : 0; return R4_OK;
     case 9: options().fp8_stage_scales = value ? 1 : 0; return R4_OK;
     case 10: options().inject_stall = value ? 1 : 0; return R4_OK;

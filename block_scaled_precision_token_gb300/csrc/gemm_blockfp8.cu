@@ -13,15 +13,20 @@
 //    fp32 accumulator in tensor memory. Slot g uses accumulator buffer
 //    g % kNumBuf; with 512 columns there are 4 (BT = 128) to 16 buffers, so
 //    the MMAs run several K blocks ahead of the promotion epilogue;
-//  * a scale warp turns As[t0.., kb] and Ws[nt, kb] into the per-token
-//    products As * Ws of each K block and publishes them in a ring of shared
-//    memory slots. With K/128 a multiple of 4 the scales arrive with the
-//    pipeline stage (a TMA box of As and a 16-byte copy of Ws); otherwise the
-//    warp loads As in coalesced row chunks, one chunk ahead in registers;
 //  * 4 x kH epilogue warps (one per tensor-memory lane quarter and column
-//    group of 32 tokens) load the block result and fold it into fp32
-//    registers: acc[t] += (As[t,kb] * Ws[nt,kb]) * D_kb[n,t], two columns per
-//    packed f32x2 FMA;
+//    group of 32 tokens) load each block result and fold it into fp32
+//    registers: acc[t] += As[t,kb] * (Ws[nt,kb] * D_kb[n,t]), the scaling
+//    and the accumulation each one packed f32x2 instruction per two columns;
+//  * the scales reach the epilogue without a handshake per K block: the
+//    epilogue threads themselves copy As and Ws for a chunk of 16 K blocks
+//    of their tile into shared memory (As transposed, [kb][token], so a
+//    warp's 32 token columns of one K block are 128 contiguous bytes read
+//    as broadcasts), one chunk ahead: the global loads of chunk c + 1 are in
+//    flight while chunk c is promoted, and one barrier of the epilogue
+//    threads per chunk publishes them. (Measured on GB300 against a scale
+//    warp publishing As * Ws in a ring with ready / empty barriers per K
+//    block: that handshake alone held the pipeline -- no MMA, no promotion
+//    -- at 50 us for M=2048, N=6144, K=2048, 37 us without it.)
 //  * decode tiles (BT <= 64) run two TMA producer warps: one thread issuing
 //    every weight and activation copy caps the weight stream (each TMA issue
 //    holds its thread for a few hundred cycles on GB300).
@@ -41,16 +46,12 @@ namespace fp8 {
 constexpr uint32_t kWSmem = 128 * 128;
 constexpr int kMaxStages = 16;
 constexpr int kMaxBuf = 16;
-constexpr int kMaxRing = 16;        // published scale slots (products As * Ws for one K block)
-// K blocks of As staged per coalesced load (the scale warp holds one chunk
-// in registers: BT * chunk / 32 values per lane).
-constexpr int chunk_of(int bt) { return bt >= 128 ? 8 : 16; }
+constexpr int kChunk = 16;          // K blocks of scales staged per epilogue chunk
 
 struct Params {
   int M, KB;           // KB = K / 128 (blocks per row of As / Ws)
   int t_tiles, splits, kb_per_split, units;
   int ldc;
-  int as_tma;          // 1: As and Ws travel with each pipeline stage (TMA), needs KB % 4 == 0
   int inject_stall;    // test of the bounded waits: CTA 0 withholds its first activation copy
   int early_w;         // 1: weight tiles are requested before waiting for the preceding kernel
   const float *As;     // [M, KB]
@@ -65,8 +66,7 @@ template <int BT>
 struct Cfg {
   static constexpr int kProd = BT <= 64 ? 2 : 1;           // TMA producer warps
   static constexpr int kMmaWarp = kProd;
-  static constexpr int kScaleWarp = kProd + 1;
-  static constexpr int kEpiWarp0 = kProd + 2;
+  static constexpr int kEpiWarp0 = kProd + 1;
   static constexpr int kCW = BT < 32 ? BT : 32;            // token columns per epilogue warp
   static constexpr int kH = BT / kCW;                      // column groups
   static constexpr int kEpiWarps = 4 * kH;
@@ -76,27 +76,17 @@ struct Cfg {
   static constexpr int kNumBuf = kNumBufRaw > kMaxBuf ? kMaxBuf : kNumBufRaw;
   static constexpr uint32_t kTmemCols = static_cast<uint32_t>(kNumBuf * BT);
   static constexpr uint32_t kXSmem = BT * 128;
-  // With KB % 4 == 0 each stage also carries As[t0.., kb & ~3 .. +4) as a
-  // [BT][4] fp32 TMA box and Ws[nt, kb & ~3 .. +4) (16 bytes).
-  static constexpr uint32_t kAsSmem = BT * 16;
-  static constexpr uint32_t kAsTx = kAsSmem + 16;
-  static constexpr uint32_t kStageBytes = ((kWSmem + kXSmem + kAsTx + 1023) / 1024) * 1024;
-  static constexpr int kRing = BT >= 128 ? 8 : kMaxRing;
-  static constexpr uint32_t kSlotFloats = BT + 4;          // BT products, then Ws (16-byte pitch)
-  static constexpr uint32_t kRingBytes = kRing * kSlotFloats * 4;
-  // As staging: 2 buffers of [BT rows][kChunk + 1] (+1: conflict-free column
-  // reads) and the chunk's Ws values.
-  static constexpr int kChunk = chunk_of(BT);
-  static constexpr uint32_t kStageRow = kChunk + 1;
-  static constexpr uint32_t kAsBufFloats = ((BT * kStageRow + kChunk + 3) / 4) * 4;
-  static constexpr uint32_t kAsBytes = 2 * kAsBufFloats * 4;
+  static constexpr uint32_t kStageBytes = ((kWSmem + kXSmem + 1023) / 1024) * 1024;
+  // scale chunks: 2 buffers of As [kChunk][BT] and Ws [kChunk]
+  static constexpr uint32_t kScFloats = kChunk * BT + kChunk;
+  static constexpr uint32_t kScBytes = 2 * kScFloats * 4;
+  static constexpr int kScPer = (BT * kChunk + kEpiThreads - 1) / kEpiThreads;   // As values per thread
   static constexpr uint32_t kMiscBytes = 1024;             // barriers and flags
-  static constexpr int kStagesRaw =
-      static_cast<int>((227u * 1024u - 1024u - kMiscBytes - kRingBytes - kAsBytes) / kStageBytes);
+  static constexpr int kStagesRaw = static_cast<int>((227u * 1024u - 1024u - kMiscBytes - kScBytes) / kStageBytes);
   static constexpr int kStagesCap = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
   static constexpr int kStages = (kStagesCap / kProd) * kProd;   // each producer owns fixed stages
   static constexpr uint32_t kTxBytes = kWSmem + kXSmem;
-  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kRingBytes + kAsBytes + kMiscBytes + 1024;
+  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kScBytes + kMiscBytes + 1024;
   static_assert(kTmemCols >= 32 && (kTmemCols & (kTmemCols - 1)) == 0, "tensor-memory allocation");
   static_assert(kThreads <= 1024, "block size");
   static_assert(kStages >= kProd, "stage count");
@@ -126,8 +116,7 @@ struct SlotCursor {
   }
 };
 
-// Walks this CTA's units in chunks of up to CH consecutive K blocks.
-template <int CH>
+// Walks this CTA's units in chunks of up to kChunk consecutive K blocks.
 struct ChunkCursor {
   int u, kb, kb1, nt, tt;
   __device__ __forceinline__ void decode(const Params &p) {
@@ -143,9 +132,9 @@ struct ChunkCursor {
     if (u < p.units) decode(p);
   }
   __device__ __forceinline__ bool valid(const Params &p) const { return u < p.units; }
-  __device__ __forceinline__ int len() const { return min(CH, kb1 - kb); }
+  __device__ __forceinline__ int len() const { return min(kChunk, kb1 - kb); }
   __device__ __forceinline__ void next(const Params &p) {
-    kb += CH;
+    kb += kChunk;
     if (kb >= kb1) {
       u += gridDim.x;
       if (u < p.units) decode(p);
@@ -153,57 +142,51 @@ struct ChunkCursor {
   }
 };
 
-// One chunk of scales in registers: As[t0 + c, kb .. kb + n) for the tile's
-// BT rows (0 past M) and Ws[nt, kb .. kb + n). Element e = lane + 32 i walks
-// the [BT][n] block row-major, so a warp's load covers whole row segments.
+// 4-byte asynchronous copy global -> shared; src_bytes = 0 writes zero.
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+// Copies one scale chunk into `buf` with cp.async (no registers held while
+// it is in flight): As transposed, buf[i * BT + t] = As[t0 + t, kb + i], then
+// buf[kChunk * BT + i] = Ws[nt, kb + i]; 0 past M or past the chunk. Element
+// r of thread e is (t, i) = divmod(e + kEpiThreads * r, kChunk): consecutive
+// threads walk a token's 16 consecutive K blocks (64 contiguous bytes).
 template <int BT>
-struct AsChunk {
-  static constexpr int kChunk = chunk_of(BT);
-  static constexpr int kPer = BT * kChunk / 32;   // elements per lane
-  float v[kPer];
-  float w;
-  __device__ __forceinline__ void load(const Params &p, const ChunkCursor<kChunk> &ch, int lane) {
-    const int n = ch.len();
-    const int t0 = ch.tt * BT;
+__device__ __forceinline__ void copy_scale_chunk(const Params &p, const ChunkCursor &ch, float *buf, int e) {
+  using C = Cfg<BT>;
+  const int n = ch.len();
+  const int t0 = ch.tt * BT;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int idx = lane + 32 * i;
-      const int c = idx / n, j = idx - c * n;
-      const int t = t0 + c;
-      v[i] = (c < BT && t < p.M) ? __ldg(p.As + static_cast<size_t>(t) * p.KB + ch.kb + j) : 0.f;
+  for (int r = 0; r < C::kScPer; ++r) {
+    const int idx = e + C::kEpiThreads * r;
+    const int t = idx / kChunk, i = idx - t * kChunk;
+    if (t < BT) {
+      const bool in = i < n && t0 + t < p.M;
+      cp_async4(buf + i * BT + t, in ? p.As + static_cast<size_t>(t0 + t) * p.KB + ch.kb + i : p.As, in ? 4u : 0u);
     }
-    w = lane < n ? __ldg(p.Ws + static_cast<size_t>(ch.nt) * p.KB + ch.kb + lane) : 0.f;
   }
-  // Into buf[c * (kChunk + 1) + j], Ws after the BT rows.
-  __device__ __forceinline__ void store(const ChunkCursor<kChunk> &ch, float *buf, int lane) const {
-    const int n = ch.len();
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int idx = lane + 32 * i;
-      const int c = idx / n, j = idx - c * n;
-      if (c < BT) buf[c * (kChunk + 1) + j] = v[i];
-    }
-    if (lane < n) buf[BT * (kChunk + 1) + lane] = w;
-  }
-};
+  if (e < kChunk)
+    cp_async4(buf + kChunk * BT + e, e < n ? p.Ws + static_cast<size_t>(ch.nt) * p.KB + ch.kb + e : p.Ws,
+              e < n ? 4u : 0u);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
 
 template <int BT>
 __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
     blockfp8_f8f6f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                           const __grid_constant__ CUtensorMap tm_as, const Params p) {
+                           const Params p) {
   using C = Cfg<BT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float *ring = reinterpret_cast<float *>(smem + C::kStages * C::kStageBytes);   // [kRing][kSlotFloats]
-  float *as_stage = ring + C::kRing * C::kSlotFloats;                            // [2][kAsBufFloats]
-  uint8_t *misc = reinterpret_cast<uint8_t *>(as_stage) + C::kAsBytes;
+  float *scbuf = reinterpret_cast<float *>(smem + C::kStages * C::kStageBytes);   // [2][kScFloats]
+  uint8_t *misc = reinterpret_cast<uint8_t *>(scbuf) + C::kScBytes;
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(misc);   // [kMaxStages]
   uint64_t *empty_bar = full_bar + kMaxStages;               // [kMaxStages]
   uint64_t *accf_bar = empty_bar + kMaxStages;               // [kMaxBuf]
   uint64_t *acce_bar = accf_bar + kMaxBuf;                   // [kMaxBuf]
-  uint64_t *sready_bar = acce_bar + kMaxBuf;                 // [kRing] products published
-  uint64_t *sempty_bar = sready_bar + kMaxRing;              // [kRing] read by every epilogue warp
-  uint64_t *drain_bar = sempty_bar + kMaxRing;
+  uint64_t *drain_bar = acce_bar + kMaxBuf;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain_bar + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *is_last = abort_flag + 1;
@@ -214,15 +197,11 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], p.as_tma ? 2 : 1);   // MMA commit (+ scale warp when As rides along)
+      mbar_init(&empty_bar[s], 1);   // the MMA commit
     }
     for (int b = 0; b < C::kNumBuf; ++b) {
       mbar_init(&accf_bar[b], 1);
       mbar_init(&acce_bar[b], C::kEpiWarps);
-    }
-    for (int r = 0; r < C::kRing; ++r) {
-      mbar_init(&sready_bar[r], 1);
-      mbar_init(&sempty_bar[r], C::kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -232,7 +211,6 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_x);
-    if (p.as_tma) tma_prefetch_desc(&tm_as);
     pdl_launch_dependents();
   }
   if (warp == C::kMmaWarp) {
@@ -252,8 +230,6 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       uint32_t issued_mask = 0, issued_phase = 0;
-      bool ok = true;
-      const uint32_t tx = C::kTxBytes + (p.as_tma ? C::kAsTx : 0u);
       // Weights first (independent of the preceding kernel), then wait for
       // it before the first activation tile.
       if (!p.early_w) pdl_wait();
@@ -262,7 +238,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
         cu.start(p);
         for (int g = 0; cu.valid(p) && g < C::kStages; ++g, cu.next(p))
           if (g % C::kProd == pw) {
-            mbar_arrive_expect_tx(&full_bar[g], tx);
+            mbar_arrive_expect_tx(&full_bar[g], C::kTxBytes);
             tma_load_3d(smem + g * C::kStageBytes, &tm_w, &full_bar[g], 0, 0, cu.nt * p.KB + cu.kb, pol_w);
           }
       }
@@ -275,30 +251,20 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
         const uint32_t phase = static_cast<uint32_t>(g / C::kStages) & 1u;
         uint8_t *st = smem + stage * C::kStageBytes;
         if (g >= C::kStages) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full_bar[stage], tx);
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) break;
+          mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
           tma_load_3d(st, &tm_w, &full_bar[stage], 0, 0, cu.nt * p.KB + cu.kb, pol_w);
         }
         // (Failure-detection test: with inject_stall, CTA 0 never issues its
         // first activation copy, so the stage's transaction never completes.)
         if (!(p.inject_stall && blockIdx.x == 0 && g == 0))
           tma_load_2d(st + kWSmem, &tm_x, &full_bar[stage], cu.kb * 128, cu.tt * BT, pol_x);
-        if (p.as_tma) {
-          const int kb4 = cu.kb & ~3;
-          tma_load_2d(st + kWSmem + C::kXSmem, &tm_as, &full_bar[stage], kb4, cu.tt * BT, pol_x);
-          bulk_load(st + kWSmem + C::kXSmem + C::kAsSmem, p.Ws + static_cast<size_t>(cu.nt) * p.KB + kb4, 16,
-                    &full_bar[stage], pol_w);
-        }
         // Record the newest phase of every stage: a parity wait cannot tell
         // phase k from k + 2, and a stage only advances once its earlier
         // phases completed.
         issued_mask |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
       }
-      (void)ok;
       // Never leave a copy in flight: wait (bounded, even after an abort)
       // for the last load issued into each of this producer's stages.
       for (int s_ = 0; s_ < C::kStages; ++s_)
@@ -338,82 +304,25 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       mbar_wait(drain_bar, 0, &dummy, p.err, DEV_ERR_WAIT_DRAIN);
     }
     __syncwarp();
-  } else if (warp == C::kScaleWarp) {
-    // ------------------------------------------------------------ scale warp
-    // Ring slot r = g % kRing holds the products As[t, kb] * Ws[nt, kb] of K
-    // block g: empty -> written -> ready -> read by every epilogue warp ->
-    // empty. With KB % 4 == 0 the scales arrive with the pipeline stage (the
-    // warp is a second consumer of its full barrier and a second arrival on
-    // its empty barrier); otherwise they are loaded in coalesced chunks.
-    if (p.as_tma) {
-      SlotCursor cu;
-      cu.start(p);
-      for (int g = 0; cu.valid(p); ++g, cu.next(p)) {
-        const int stage = g % C::kStages;
-        const uint32_t phase = static_cast<uint32_t>(g / C::kStages) & 1u;
-        const int r = g % C::kRing;
-        const uint32_t ph = static_cast<uint32_t>(g / C::kRing) & 1u;
-        if (!warp_wait(&sempty_bar[r], ph ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) break;
-        if (!warp_wait(&full_bar[stage], phase, abort_flag, p.err, DEV_ERR_WAIT_FULL)) break;
-        const float *as_s = reinterpret_cast<const float *>(smem + stage * C::kStageBytes + kWSmem + C::kXSmem);
-        const int j = cu.kb & 3;
-        const float ws = as_s[BT * 4 + j];
-        float *slot = ring + r * C::kSlotFloats;
-        for (int c = lane; c < BT; c += 32) slot[c] = as_s[c * 4 + j] * ws;
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sready_bar[r]);
-          mbar_arrive(&empty_bar[stage]);
-        }
-      }
-    } else {
-    pdl_wait();   // As comes from the preceding kernel
-    ChunkCursor<C::kChunk> cl, cn;   // chunk being published, chunk being loaded
-    cl.start(p);
-    cn.start(p);
-    AsChunk<BT> regs;
-    if (cn.valid(p)) {
-      regs.load(p, cn, lane);
-      regs.store(cn, as_stage, lane);
-      cn.next(p);
-    }
-    __syncwarp();
-    bool ok = true;
-    int g = 0;
-    for (int ci = 0; cl.valid(p) && ok; ++ci, cl.next(p)) {
-      const bool more = cn.valid(p);
-      if (more) regs.load(p, cn, lane);   // in flight during the publishing below
-      const float *buf = as_stage + (ci & 1) * C::kAsBufFloats;
-      const int n = cl.len();
-      for (int j = 0; j < n; ++j, ++g) {
-        const int r = g % C::kRing;
-        const uint32_t ph = static_cast<uint32_t>(g / C::kRing) & 1u;
-        if (!warp_wait(&sempty_bar[r], ph ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) {
-          ok = false;
-          break;
-        }
-        float *slot = ring + r * C::kSlotFloats;
-        const float ws = buf[BT * C::kStageRow + j];
-        for (int c = lane; c < BT; c += 32) slot[c] = buf[c * C::kStageRow + j] * ws;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sready_bar[r]);
-      }
-      if (more) {
-        regs.store(cn, as_stage + ((ci + 1) & 1) * C::kAsBufFloats, lane);
-        cn.next(p);
-      }
-      __syncwarp();
-    }
-    }
   } else {
     // ------------------------------------------------------------ promotion epilogue
-    pdl_wait();                        // C and the workspace follow the stream order
+    pdl_wait();                        // As, C and the workspace follow the stream order
     const int ew = warp - C::kEpiWarp0;
     const int e = ew * 32 + lane;      // 0 .. kEpiThreads-1
     const int q = warp & 3;            // tensor-memory lane quarter this warp may access
     const int h = ew >> 2;             // column group
     const int col0 = h * C::kCW;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(col0);
+    // Scale chunks: the first is staged before the loop; each chunk's
+    // barrier makes the next one (stored at the end of the chunk) visible.
+    {
+      ChunkCursor c0;
+      c0.start(p);
+      if (c0.valid(p)) copy_scale_chunk<BT>(p, c0, scbuf, e);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    named_bar_sync(1, C::kEpiThreads);
+    int cur = 0;                       // scale buffer of the chunk being promoted
     SlotCursor cu;
     cu.start(p);
     int g = 0;
@@ -426,47 +335,69 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       float acc[C::kCW];
 #pragma unroll
       for (int j = 0; j < C::kCW; ++j) acc[j] = 0.f;
-      bool ok = true;
-      for (; cu.valid(p) && cu.u == u; ++g, cu.next(p)) {
-        const int buf = g % C::kNumBuf;
-        const uint32_t bphase = static_cast<uint32_t>(g / C::kNumBuf) & 1u;
-        const int r = g % C::kRing;
-        const uint32_t rphase = static_cast<uint32_t>(g / C::kRing) & 1u;
-        // Warp-uniform waits (tcgen05.ld needs the whole warp).
-        if (!warp_wait(&accf_bar[buf], bphase, abort_flag, p.err, DEV_ERR_WAIT_ACC_FULL)) {
-          ok = false;
-          break;
+      bool ok = true, stop = false;
+      while (cu.valid(p) && cu.u == u) {
+        // one chunk: up to kChunk K blocks of this unit
+        const int kbc = cu.kb;
+        const int nblk = min(kChunk, cu.kb1 - kbc);
+        {                              // next chunk's scales, in flight during the promotion
+          ChunkCursor cn;
+          cn.u = u;
+          cn.nt = nt;
+          cn.tt = tt;
+          cn.kb = kbc;
+          cn.kb1 = cu.kb1;
+          cn.next(p);
+          if (cn.valid(p)) copy_scale_chunk<BT>(p, cn, scbuf + (cur ^ 1) * C::kScFloats, e);
         }
-        tc_fence_after();
-        uint32_t d[32];
-        if constexpr (C::kCW == 32) {
-          tc_ld_32x32b_x32(lane_base + static_cast<uint32_t>(buf * BT), d);
-        } else {
-          tc_ld_32x32b_x16(lane_base + static_cast<uint32_t>(buf * BT), d);
-        }
-        tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce_bar[buf]);
-        if (!warp_wait(&sready_bar[r], rphase, abort_flag, p.err, DEV_ERR_WAIT_FULL)) {
-          ok = false;
-          break;
-        }
-        const float4 *s4 = reinterpret_cast<const float4 *>(ring + r * C::kSlotFloats + col0);
+        const float *sc = scbuf + cur * C::kScFloats;
+        for (int i = 0; i < nblk; ++i, ++g, cu.next(p)) {
+          if (!ok) continue;           // stopped: skip to the chunk barrier
+          const int buf = g % C::kNumBuf;
+          const uint32_t bphase = static_cast<uint32_t>(g / C::kNumBuf) & 1u;
+          // Warp-uniform wait (tcgen05.ld needs the whole warp).
+          if (!warp_wait(&accf_bar[buf], bphase, abort_flag, p.err, DEV_ERR_WAIT_ACC_FULL)) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+          uint32_t d[32];
+          if constexpr (C::kCW == 32) {
+            tc_ld_32x32b_x32(lane_base + static_cast<uint32_t>(buf * BT), d);
+          } else {
+            tc_ld_32x32b_x16(lane_base + static_cast<uint32_t>(buf * BT), d);
+          }
+          tc_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce_bar[buf]);
+          const float ws = sc[kChunk * BT + i];
+          const float4 *a4 = reinterpret_cast<const float4 *>(sc + i * BT + col0);
+          // acc[t] += As[t,kb] * (Ws[kb] * D[n,t]): the weight scale is applied
+          // to the block result in place (no extra registers), then the
+          // activation scale in the accumulating FMA.
 #pragma unroll
-        for (int j4 = 0; j4 < C::kCW / 4; ++j4) {
-          const float4 f = s4[j4];
-          fma_f32x2(acc[4 * j4 + 0], acc[4 * j4 + 1], f.x, f.y, __uint_as_float(d[4 * j4 + 0]),
-                    __uint_as_float(d[4 * j4 + 1]));
-          fma_f32x2(acc[4 * j4 + 2], acc[4 * j4 + 3], f.z, f.w, __uint_as_float(d[4 * j4 + 2]),
-                    __uint_as_float(d[4 * j4 + 3]));
+          for (int j4 = 0; j4 < C::kCW / 4; ++j4) {
+            const float4 a = a4[j4];
+            float d0 = __uint_as_float(d[4 * j4 + 0]), d1 = __uint_as_float(d[4 * j4 + 1]);
+            float d2 = __uint_as_float(d[4 * j4 + 2]), d3 = __uint_as_float(d[4 * j4 + 3]);
+            mul_f32x2(d0, d1, ws, ws);
+            mul_f32x2(d2, d3, ws, ws);
+            fma_f32x2(acc[4 * j4 + 0], acc[4 * j4 + 1], a.x, a.y, d0, d1);
+            fma_f32x2(acc[4 * j4 + 2], acc[4 * j4 + 3], a.z, a.w, d2, d3);
+          }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sempty_bar[r]);
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        // Every epilogue thread reaches this barrier once per chunk, whether
+        // or not its waits succeeded: the stop decision is the same
+        // everywhere, and the next chunk's scales are visible after it.
+        if (named_bar_any(1, C::kEpiThreads, !ok)) {
+          stop = true;
+          break;
+        }
+        cur ^= 1;
       }
-      // Every epilogue thread reaches this barrier once per unit, whether or
-      // not its waits succeeded, so the stop decision is the same everywhere.
-      if (named_bar_any(1, C::kEpiThreads, !ok)) {
+      if (stop) {
         abort_u = u;
         break;
       }
@@ -520,7 +451,7 @@ template <int BT>
 int launch_bt(const uint8_t *q, const float *As, const uint8_t *packed, int64_t M, int64_t N, int64_t K,
               uint16_t *c, int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st) {
   using C = Cfg<BT>;
-  CUtensorMap tm_w, tm_x, tm_as;
+  CUtensorMap tm_w, tm_x;
   {
     const uint64_t dims[3] = {128, 128, static_cast<uint64_t>((N / 128) * (K / 128))};
     const uint64_t strides[2] = {128, 16384};
@@ -537,22 +468,9 @@ int launch_bt(const uint8_t *q, const float *As, const uint8_t *packed, int64_t 
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return R4_ERR_CUDA;
   }
-  // The activation scales ride along with each stage when their rows are
-  // 16-byte multiples (TMA) and the pointers are 16-byte aligned.
-  const float *Ws = reinterpret_cast<const float *>(packed + fp8_packed_codes_bytes(N, K));
-  int as_tma = 0;
-  if (options().fp8_stage_scales && pl.KB % 4 == 0 && reinterpret_cast<uintptr_t>(Ws) % 16 == 0) {
-    const uint64_t dims[2] = {static_cast<uint64_t>(pl.KB), static_cast<uint64_t>(M)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(pl.KB) * 4};
-    const uint32_t box[2] = {4, static_cast<uint32_t>(BT)};
-    as_tma = encode_tiled(&tm_as, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(As), dims, strides, box,
-                          CU_TENSOR_MAP_SWIZZLE_NONE) == CUDA_SUCCESS;
-  }
-  if (!as_tma) tm_as = tm_x;   // not read by the kernel in that case
   Params p;
   p.M = static_cast<int>(M);
   p.KB = pl.KB;
-  p.as_tma = as_tma;
   p.inject_stall = options().inject_stall;
   p.early_w = options().early_weights;
   p.t_tiles = pl.t_tiles;
@@ -568,7 +486,7 @@ int launch_bt(const uint8_t *q, const float *As, const uint8_t *packed, int64_t 
   p.err = device_error_word();
   auto kern = blockfp8_f8f6f4_kernel<BT>;
   if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::kSmemBytes) != cudaSuccess) return R4_ERR_CUDA;
-  if (launch_pdl(kern, dim3(pl.grid), dim3(C::kThreads), C::kSmemBytes, st, tm_w, tm_x, tm_as, p) != cudaSuccess)
+  if (launch_pdl(kern, dim3(pl.grid), dim3(C::kThreads), C::kSmemBytes, st, tm_w, tm_x, p) != cudaSuccess)
     return R4_ERR_CUDA;
   set_last_kernel(BT == 16   ? "blockfp8_f8f6f4_kernel<16>"
                   : BT == 32 ? "blockfp8_f8f6f4_kernel<32>"

@@ -5,9 +5,13 @@
 // The page's diagnosis: a sub-megabyte weight gives a library GEMM only a
 // handful of CTAs, each walking all of K while the rest of the GPU idles; the
 // cure is split-K. Here the split is across a thread-block cluster:
-//  * grid = (KS, ceil(N/16)), cluster = (KS, 1, 1): each CTA owns 16 weight
-//    rows (the mma M dimension -- weight-stationary, tokens are the mma N) and
-//    a contiguous K range; KS <= 8 CTAs of a cluster share one row tile.
+//  * grid = (KS, ceil(N/16), token slices), cluster = (KS, 1, 1): each CTA
+//    owns 16 weight rows (the mma M dimension -- weight-stationary, tokens
+//    are the mma N), a contiguous K range and one slice of up to 16 * NG2
+//    tokens; KS <= 8 CTAs of a cluster share one row tile and token slice.
+//    Splitting the tokens over more CTAs (each re-reads the sub-megabyte
+//    weight from L2) keeps the per-CTA work, and so the latency, close to
+//    that of a few tokens as M grows.
 //  * operands are staged in shared memory with cp.async (16-byte chunks,
 //    rows padded by 16 bytes so ldmatrix is conflict-free) and multiplied
 //    with mma.sync m16n8k16 bf16 -> fp32. The problem is latency- and
@@ -22,6 +26,8 @@
 //    kernel.
 
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "r4_internal.h"
 
@@ -103,6 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_rank();
   const int KS = gridDim.x;
   const int n0 = blockIdx.y * kRows;
+  const int t_off = blockIdx.z * kMpad;           // this CTA's token slice
   const int kbeg = static_cast<int>(rank) * chunks_per_cta * 256;
   const int kend = min(K, kbeg + chunks_per_cta * 256);
 
@@ -139,8 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = tid; i < kMpad * cpr; i += kThreads) {
       const int r = i / cpr, ch = i % cpr;
       uint16_t *dst = sX + r * kStride + ch * 8;
-      if (r < M)
-        cp_async16(dst, x + static_cast<size_t>(r) * K + kk + ch * 8);
+      if (t_off + r < M)
+        cp_async16(dst, x + static_cast<size_t>(t_off + r) * K + kk + ch * 8);
       else
         *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
     }
@@ -210,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t my_part = smem_addr(sCl);
   for (int e = static_cast<int>(rank) * per + tid; e < min(total, static_cast<int>(rank + 1) * per); e += kThreads) {
     const int r = e % kRows, t = e / kRows;
-    if (t >= M || n0 + r >= N) continue;   // padded token or row: no load without a consumer
+    if (t_off + t >= M || n0 + r >= N) continue;   // padded token or row: no load without a consumer
     const uint32_t off = 4u * static_cast<uint32_t>(r * kRS + t);
     float pq[kMaxKS];   // all loads in flight before the (rank-ordered) sum
 #pragma unroll
@@ -221,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = 0; q < kMaxKS; ++q)
       if (q < KS) v += pq[q];
     __nv_bfloat16 h = __float2bfloat16_rn(v);
-    c[static_cast<size_t>(t) * ldc + n0 + r] = *reinterpret_cast<uint16_t *>(&h);
+    c[static_cast<size_t>(t_off + t) * ldc + n0 + r] = *reinterpret_cast<uint16_t *>(&h);
   }
   // No CTA leaves while another may still read its partial. The arrive must
   // be a release: it is what orders this CTA's remote loads before the peers
@@ -232,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int NG2, int NB>
 cudaError_t launch_ng(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N, int64_t K, uint16_t *c,
-                      int64_t ldc, cudaStream_t st) {
+                      int64_t ldc, int slices, cudaStream_t st) {
   const int chunks = static_cast<int>(K / 256);
   const int ks = chunks < kMaxKS ? chunks : kMaxKS;
   const int cpc = (chunks + ks - 1) / ks;
@@ -241,7 +248,7 @@ cudaError_t launch_ng(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(ks), static_cast<unsigned>(ceil_div(N, kRows)), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(ks), static_cast<unsigned>(ceil_div(N, kRows)), static_cast<unsigned>(slices));
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
@@ -270,11 +277,18 @@ cudaError_t launch_gemm_skinny(const uint16_t *x, const uint16_t *w, int64_t M, 
   // 64 tokens, where the larger footprint spreads the CTAs over more SMs
   // (measured, [256, 2048], one chunk per CTA: M <= 16 3.0 vs 3.2 us and
   // M = 32 4.3 vs 4.6 us with one buffer; M = 64 5.9 vs 6.6 us with two).
-  const int64_t ng2 = ceil_div(M, 16);
+  // Token groups of 16 per CTA: above 32 tokens one group per CTA, the tokens
+  // split over more CTAs (measured on GB300, graph-timed, M = 64: [256,2048]
+  // 6.05 -> 5.45 us, [96,5120] 6.38 -> 5.53 us; at M = 32 neither way wins
+  // clearly: 4.51 / 4.58 and 4.73 / 4.19 us); option 15 forces a count.
+  const int64_t groups = ceil_div(M, 16);
+  int64_t ng2 = groups > 2 ? 1 : groups;
+  if (options().skinny_groups > 0) ng2 = std::min<int64_t>(groups, options().skinny_groups);
+  const int slices = static_cast<int>(ceil_div(groups, ng2));
   const bool multi = ceil_div(K / 256, static_cast<int64_t>(skinny::kMaxKS)) > 1 || ng2 == 4;
 #define R4_SK(G)                                                                               \
-  return multi ? skinny::launch_ng<G, 2>(x, w, M, N, K, c, ldc, st)                           \
-               : skinny::launch_ng<G, 1>(x, w, M, N, K, c, ldc, st);
+  return multi ? skinny::launch_ng<G, 2>(x, w, M, N, K, c, ldc, slices, st)                   \
+               : skinny::launch_ng<G, 1>(x, w, M, N, K, c, ldc, slices, st);
   switch (ng2) {
     case 1: R4_SK(1)
     case 2: R4_SK(2)

@@ -83,7 +83,8 @@ struct Params {
   int t_tiles, splits, kb_per_split, units;
   int ldc;
   int tma_store;         // 1: bf16 output tiles leave through smem + TMA tensor stores
-  int l2_prefetch;       // 1: producer 0 prefetches the CTA's whole weight range into L2 at start
+  int l2_prefetch;       // 1: producer 0 prefetches the CTA's whole weight range into L2 at start;
+                         // 2: decode tiles prefetch a rolling window of kPfAhead K blocks beyond the ring
   int cluster;           // 1: the `splits` CTAs of a cluster split K and exchange partials in DSMEM
   int xchg_stage;        // 1 (cluster, one unit per CTA): exchange the whole tile from the pipeline stages
   int inject_stall;      // test of the bounded waits: CTA 0 withholds its first activation copy
@@ -142,6 +143,44 @@ __device__ __forceinline__ void decode_unit(const Params &p, int u, int &nt, int
   tt = tile - nt * p.t_tiles;
   kb0 = sp * p.kb_per_split;
   kb1 = min(p.KB, kb0 + p.kb_per_split);
+}
+
+// Rolling L2 prefetch of the decode weight stream: one CTA keeps only its
+// ring's worth of weight bytes in flight (~70 KB; measured ~45-50 GB/s per
+// CTA on GB300, latency-bound), so producer 0 asks L2 for the next
+// kPfAhead K blocks beyond the ring as it goes (one bulk prefetch per
+// contiguous run, no shared memory). Measured on GB300 (cold weights,
+// graph-timed): decode 34816x5120 19.1 -> 18.1 us (M=6), 22.9 -> 21.5 us
+// (M=64); 5120x17408 15.0 -> 13.6 us (M=6); larger windows (16, 32) were
+// slower; the whole range at kernel start (option 5 = 1) helps 5120x17408
+// and hurts 34816x5120.
+constexpr int kPfAhead = 8;
+
+// Prefetch cursor over this CTA's unit sequence: unit u, K block kb
+// (relative to the unit's first block).
+struct PfCursor {
+  int u, kb;
+};
+
+// Bulk L2 prefetch of `count` K blocks (weight codes and scale atoms, both
+// contiguous within a unit) from the cursor on, across unit boundaries.
+__device__ __forceinline__ void prefetch_blocks_l2(const Params &p, PfCursor &c, int count) {
+  while (count > 0 && c.u < p.units) {
+    int nt, tt, sp, kb0, kb1;
+    decode_unit(p, c.u, nt, tt, sp, kb0, kb1);
+    const int n = min(count, kb1 - kb0 - c.kb);
+    if (n > 0) {
+      const size_t blk = static_cast<size_t>(nt) * p.KB + kb0 + c.kb;
+      bulk_prefetch_l2(p.w + blk * 8192, static_cast<uint32_t>(n) * 8192u);
+      bulk_prefetch_l2(p.sf + blk * kSfBytes, static_cast<uint32_t>(n) * kSfBytes);
+      c.kb += n;
+      count -= n;
+    }
+    if (c.kb >= kb1 - kb0) {
+      c.u += gridDim.x;
+      c.kb = 0;
+    }
+  }
 }
 
 // Bulk L2 prefetch of unit u's weight codes and scale atoms (both contiguous).
@@ -263,8 +302,33 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
       // stream then runs at HBM rate while this kernel waits for its
       // predecessor, not only for the ring's depth.
       if (!p.early_w) pdl_wait();   // weights may come from the preceding kernel
-      if (p.l2_prefetch && pw == 0)
+      if (p.l2_prefetch == 1 && pw == 0)
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) prefetch_unit_l2(p, u);
+      // Rolling prefetch (decode tiles, producer 0): the cursor starts at the
+      // first K block the ring's initial fill leaves out (the fill below
+      // covers the first kStages slots, padding slots included).
+      PfCursor pf{p.units, 0};
+      const bool rolling = p.l2_prefetch == 2 && pw == 0 && BT <= 64;
+      if (rolling) {
+        int left = C::kStages;
+        pf.u = blockIdx.x;
+        while (pf.u < p.units) {
+          int nt, tt, sp, kb0, kb1;
+          decode_unit(p, pf.u, nt, tt, sp, kb0, kb1);
+          const int nkb = kb1 - kb0, nslots = (nkb + ISS - 1) / ISS * ISS;
+          if (left < nslots) {
+            pf.kb = min(left, nkb);
+            if (pf.kb == nkb) {
+              pf.u += gridDim.x;
+              pf.kb = 0;
+            }
+            break;
+          }
+          left -= nslots;
+          pf.u += gridDim.x;
+        }
+        prefetch_blocks_l2(p, pf, kPfAhead);
+      }
       {
         int g = 0;
         for (int u = blockIdx.x; u < p.units && g < C::kStages; u += gridDim.x) {
@@ -300,6 +364,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
         for (int i = pw; i < nslots; i += ISS) {
           uint8_t *st = smem + stage * C::kStageBytes;
           const int kb = kb0 + i;
+          if (rolling) prefetch_blocks_l2(p, pf, ISS);   // one block per slot, ISS slots per turn
           if (gbase + i >= C::kStages) {   // not pre-issued
             if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) {
               ok = false;

@@ -35,10 +35,12 @@ struct Options {
   int inject_stall = 0;     // tests only: the next W4A8 launches withhold one copy (bounded-wait test)
   int pdl = 1;              // launch with programmatic stream serialization
   int early_weights = 1;    // GEMMs read their weight operand before waiting for the preceding kernel
-  int l2_prefetch = 0;      // W4A8: bulk L2 prefetch of the CTA's whole weight range at kernel start
+  int l2_prefetch = 2;      // W4A8/W4A4 decode tiles: 2 rolling L2 prefetch ahead of the ring, 1 whole range at
+                            // kernel start, 0 none
   int cluster_split = 1;    // W4A8 decode tiles: split-K across a thread-block cluster when possible
   int row_split = 0;        // row-wise quantizers: CTAs per row (0 = automatic, else 1/2/4/8)
   int row_threads = 0;      // row-wise quantizers: threads per CTA at most (0 = automatic, else 64/128/256)
+  int skinny_groups = 0;    // skinny GEMM: 16-token groups per CTA (0 = automatic, else 1..4)
 };
 Options &options();
 

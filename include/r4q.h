@@ -359,9 +359,10 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * (process-wide, not thread-safe). key 1: force the W4A8 split-K factor
  * (0 = automatic); key 2: force the W4A8 token tile (0 = automatic, else
  * 16/32/64/128/256); key 3: force the block-FP8 split-K factor; key 4:
- * programmatic dependent launch on (1, default) or off (0); key 5: W4A8
- * bulk L2 prefetch of each CTA's whole weight range at kernel start (1) or
- * not (0);
+ * programmatic dependent launch on (1, default) or off (0); key 5: L2
+ * prefetch of the weight stream of the W4A8/W4A4 GEMMs: 2 (default) a
+ * rolling window of 8 K blocks beyond each decode CTA's pipeline ring, 1
+ * each CTA's whole weight range at kernel start, 0 none;
  * key 6: W4A8 decode split-K across a thread-block cluster with the partial
  * sums exchanged in distributed shared memory (1, default) or through the
  * caller's workspace (0); key 7: force the block-FP8 token tile (0 =
@@ -385,7 +386,10 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * R4_ERR_INVALID_ARG;
  * key 14: the GEMMs request their weight operand before waiting for the
  * preceding kernel (1, default) or only after it (0); see the weight-writer
- * rule at the top of this header.
+ * rule at the top of this header;
+ * key 15: skinny bf16 GEMM, 16-token groups per CTA: 0 (default) chooses,
+ * 1..4 force it (the tokens are split over that many more CTAs); other
+ * values return R4_ERR_INVALID_ARG.
  */
 int r4_set_option(int key, int64_t value);
 
