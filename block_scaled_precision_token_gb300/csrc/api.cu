@@ -7,6 +7,7 @@
 
 #include <cstdio>
 #include <mutex>
+#include <map>
 #include <set>
 #include <utility>
 
@@ -96,12 +97,15 @@ int *device_error_word() {
 void set_last_kernel(const char *name) { t_last_kernel = name; }
 
 cudaError_t ensure_smem_attr(const void *func, int bytes) {
-  static std::set<std::pair<int, const void *>> done;
+  // largest size set so far per (device, kernel): a later launch of the same
+  // kernel with more dynamic shared memory raises the attribute again
+  static std::map<std::pair<int, const void *>, int> done;
   const int d = current_device();
   std::lock_guard<std::mutex> lk(g_mu);
-  if (done.count({d, func})) return cudaSuccess;
+  const auto it = done.find({d, func});
+  if (it != done.end() && it->second >= bytes) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.insert({d, func});
+  if (e == cudaSuccess) done[{d, func}] = bytes;
   return e;
 }
 

@@ -117,7 +117,8 @@ def test_add_rmsnorm_quant_prefill_rows_sampled(r4q):
 
 
 @pytest.mark.parametrize("M,N", [(1, 8), (6, 17408), (64, 2048), (257, 1024), (3, 24576),
-                                 (160, 17408), (153, 24576)])   # the last two: 512-thread blocks
+                                 (160, 17408), (153, 24576),    # 512-thread blocks
+                                 (305, 2048), (333, 17408), (401, 24576)])   # more rows than SMs
 def test_silu_mul_quant(r4q, M, N):
     g = _randn((M, N), M + N, 3.0)
     u = _randn((M, N), M + 2 * N, 1.0)
