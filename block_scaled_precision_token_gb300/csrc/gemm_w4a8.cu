@@ -79,7 +79,8 @@ constexpr int kMaxClusterSplit = 6;   // the planner splits K across a cluster o
 
 struct Params {
   int M, N, KB;
-  const uint8_t *xsf;    // W4A4: activation scale atoms [tokens/128][KB][512]
+  const uint8_t *xsf;    // W4A4: activation scale atoms [KB][xatoms][512] (K-block-major)
+  int xatoms;            // W4A4: 128-token scale atoms per K block
   int t_tiles, splits, kb_per_split, units;
   int ldc;
   int tma_store;         // 1: bf16 output tiles leave through smem + TMA tensor stores
@@ -106,7 +107,14 @@ struct Params {
 // producer warps and kIss MMA-issuing warps: slot g (one 128-K block) belongs
 // to producer g % kIss and MMA warp g % kIss, lives in ring stage g % kStages,
 // and is accumulated into MMA warp (g % kIss)'s own tensor-memory accumulator;
-// the epilogue sums the kIss partial accumulators.
+// the epilogue sums the kIss partial accumulators. Prefill tiles of the
+// W4A4 mode run two producer warps to one MMA warp (kProd = 2): their
+// kind::mxf4 slots take half the MMA time of the f8 ones, and one thread
+// issuing the slot's five copies (weight, activations, three scale atoms)
+// could not keep up (measured on GB300: dropping two of the five copies
+// alone made M=2048 8-19 % faster). Slot g then belongs to producer
+// g % kProd and MMA warp g % kIss; a unit's slots are padded to a multiple
+// of kPad = max(kProd, kIss).
 //
 // A4 = true is the W4A4 variant (kind::mxf4): both operands are packed e2m1
 // (two per byte, loaded as plain bytes in the 64-byte swizzle: 8 KiB of
@@ -116,9 +124,11 @@ struct Params {
 template <int BT, bool A4 = false>
 struct Cfg {
   static constexpr int kIss = BT <= 64 ? 4 : 1;
+  static constexpr int kProd = BT <= 64 ? 4 : (A4 ? 2 : 1);   // TMA producer warps
+  static constexpr int kPad = kProd > kIss ? kProd : kIss;    // slot padding of a unit
   static constexpr int kNumAcc = (kIss * 2 * BT <= 256) ? 2 : 1;
-  static constexpr int kThreads = 32 * (2 * kIss + 4);   // kIss producers, kIss MMA issuers, 4 epilogue
-  static constexpr int kEpiWarp0 = 2 * kIss;
+  static constexpr int kThreads = 32 * (kProd + kIss + 4);    // producers, MMA issuers, 4 epilogue
+  static constexpr int kEpiWarp0 = kProd + kIss;
   static constexpr uint32_t kWBytes = A4 ? 8192u : kWSmem;      // weight tile in shared memory
   static constexpr uint32_t kXSmem = A4 ? BT * 64 : BT * 128;   // activation tile
   static constexpr int kXAtoms = A4 ? (BT > 128 ? 2 : 1) : 0;   // activation scale atoms per stage
@@ -128,12 +138,12 @@ struct Cfg {
   static constexpr uint32_t kOutBytes = 2u * kOutChunk * 128u * 2u;  // two bf16 [chunk][128] buffers
   static constexpr int kStagesRaw = static_cast<int>((208u * 1024u) / kStageBytes);
   static constexpr int kStagesCap = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
-  static constexpr int kStages = (kStagesCap / kIss) * kIss;        // every issuer owns fixed stages
+  static constexpr int kStages = (kStagesCap / kPad) * kPad;        // every warp owns fixed stages
   static constexpr uint32_t kTxBytes = kWTxBytes + kXSmem + kSfBytes * (1 + kXAtoms);
   static constexpr uint32_t kMiscBytes = 1024;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kMiscBytes + kOutBytes + 1024;  // + align slack
   static_assert(kIss * kNumAcc * BT <= 256, "accumulators overlap the scale columns");
-  static_assert(kStages >= kIss && kStages % kIss == 0, "stage count");
+  static_assert(kStages >= kPad && kStages % kPad == 0, "stage count");
 };
 
 __device__ __forceinline__ void decode_unit(const Params &p, int u, int &nt, int &tt, int &sp, int &kb0, int &kb1) {
@@ -228,7 +238,9 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
       return __ldg(p.s + t);
     }
   };
-  constexpr int ISS = C::kIss;
+  constexpr int ISS = C::kIss;    // MMA-issuing warps
+  constexpr int PROD = C::kProd;  // TMA producer warps
+  constexpr int PAD = C::kPad;    // a unit's slots are padded to a multiple of this
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *misc = smem + C::kStages * C::kStageBytes;
@@ -272,7 +284,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
     tma_prefetch_desc(&tm_x);
     pdl_launch_dependents();   // let the next kernel in the stream start its own prologue
   }
-  if (warp == ISS) {           // first MMA warp owns the tensor-memory allocation
+  if (warp == PROD) {          // first MMA warp owns the tensor-memory allocation
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -284,9 +296,9 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
   // Every CTA of the cluster has initialised its barriers before any remote arrival.
   if (p.cluster) cluster_sync_all();
 
-  if (warp < ISS) {
-    // ------------------------------------------------------------ TMA producers (warps 0..ISS-1)
-    // Slot sequence: every unit's k-blocks, padded to a multiple of ISS. A
+  if (warp < PROD) {
+    // ------------------------------------------------------------ TMA producers (warps 0..PROD-1)
+    // Slot sequence: every unit's k-blocks, padded to a multiple of PAD. A
     // padding slot carries no data: its full barrier gets a plain arrival.
     const int pw = warp;
     if (lane == 0) {
@@ -315,7 +327,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
         while (pf.u < p.units) {
           int nt, tt, sp, kb0, kb1;
           decode_unit(p, pf.u, nt, tt, sp, kb0, kb1);
-          const int nkb = kb1 - kb0, nslots = (nkb + ISS - 1) / ISS * ISS;
+          const int nkb = kb1 - kb0, nslots = (nkb + PAD - 1) / PAD * PAD;
           if (left < nslots) {
             pf.kb = min(left, nkb);
             if (pf.kb == nkb) {
@@ -335,8 +347,8 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
           int nt, tt, sp, kb0, kb1;
           decode_unit(p, u, nt, tt, sp, kb0, kb1);
           const int nkb = kb1 - kb0;
-          const int nslots = (nkb + ISS - 1) / ISS * ISS;
-          for (int i = pw; i < nslots && g + i < C::kStages; i += ISS) {
+          const int nslots = (nkb + PAD - 1) / PAD * PAD;
+          for (int i = pw; i < nslots && g + i < C::kStages; i += PROD) {
             const int s_ = g + i;
             if (i < nkb) {
               uint8_t *st = smem + s_ * C::kStageBytes;
@@ -360,11 +372,11 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
         int nt, tt, sp, kb0, kb1;
         decode_unit(p, u, nt, tt, sp, kb0, kb1);
         const int nkb = kb1 - kb0;
-        const int nslots = (nkb + ISS - 1) / ISS * ISS;
-        for (int i = pw; i < nslots; i += ISS) {
+        const int nslots = (nkb + PAD - 1) / PAD * PAD;
+        for (int i = pw; i < nslots; i += PROD) {
           uint8_t *st = smem + stage * C::kStageBytes;
           const int kb = kb0 + i;
-          if (rolling) prefetch_blocks_l2(p, pf, ISS);   // one block per slot, ISS slots per turn
+          if (rolling) prefetch_blocks_l2(p, pf, PROD);   // one block per slot, PROD slots per turn
           if (gbase + i >= C::kStages) {   // not pre-issued
             if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) {
               ok = false;
@@ -385,19 +397,19 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
           const bool withhold = p.inject_stall && blockIdx.x == 0 && gbase + i == 0;
           if (i < nkb && !withhold) tma_load_2d(st + C::kWBytes, &tm_x, &full_bar[stage], kb * kXStep, tt * BT, pol_x);
           if constexpr (A4) {
-            // the activation scale atom(s) of this token tile and K block
+            // the activation scale atom(s) of this token tile and K block:
+            // adjacent in the K-block-major layout, one copy
             if (i < nkb)
-              for (int a = 0; a < C::kXAtoms; ++a)
-                bulk_load(st + C::kSfOff + kSfBytes * (1 + a),
-                          p.xsf + (static_cast<size_t>(tt * BT / 128 + a) * p.KB + kb) * kSfBytes, kSfBytes,
-                          &full_bar[stage], pol_x);
+              bulk_load(st + C::kSfOff + kSfBytes,
+                        p.xsf + (static_cast<size_t>(kb) * p.xatoms + tt * BT / 128) * kSfBytes,
+                        kSfBytes * C::kXAtoms, &full_bar[stage], pol_x);
           }
           // Record the newest phase of every stage, padding slots included: a
           // parity wait cannot tell phase k from k + 2, and a stage only
           // advances after its earlier phases completed.
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-          stage += ISS;
+          stage += PROD;
           if (stage >= C::kStages) {
             stage -= C::kStages;
             phase ^= 1u;
@@ -414,9 +426,9 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
         }
     }
     __syncwarp();
-  } else if (warp < 2 * ISS) {
-    // ------------------------------------------------------------ MMA issuers (warps ISS..2*ISS-1)
-    const int mw = warp - ISS;
+  } else if (warp < PROD + ISS) {
+    // ------------------------------------------------------------ MMA issuers (warps PROD..PROD+ISS-1)
+    const int mw = warp - PROD;
     if (lane == 0) {
       const uint32_t sfb = tmem + kSfbCol + 16u * static_cast<uint32_t>(mw);
       if constexpr (!A4) {
@@ -433,7 +445,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
         int nt, tt, sp, kb0, kb1;
         decode_unit(p, u, nt, tt, sp, kb0, kb1);
         const int nkb = kb1 - kb0;
-        const int nslots = (nkb + ISS - 1) / ISS * ISS;
+        const int nslots = (nkb + PAD - 1) / PAD * PAD;
         if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_ACC_EMPTY)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>((mw * C::kNumAcc + acc) * BT);
@@ -719,7 +731,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == ISS) {
+  if (warp == PROD) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -787,6 +799,7 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *xsf, const uint8_
   p.N = static_cast<int>(N);
   p.KB = pl.KB;
   p.xsf = xsf;
+  p.xatoms = static_cast<int>(mx_act_tokens_padded(M) / 128);
   p.t_tiles = pl.t_tiles;
   p.splits = pl.splits;
   p.kb_per_split = pl.kb_per_split;

@@ -180,12 +180,14 @@ __global__ void quant_mxfp4_weight_kernel(const float *__restrict__ w, int64_t N
 // nibble of byte i). The four scale codes of a 128-K block are one 32-bit
 // word of the token's scale atom row (byte j = 32-K block j), OR-combined
 // over the 16 lanes by shuffles and stored by one lane:
-//   scale atom (a, kb): 512 bytes, byte 16 r0 + 4 r1 + j = token
-//   128 a + 32 r1 + r0, 32-K block 4 kb + j  (a = token / 128).
+//   scale atom (a, kb) at (kb * A + a) * 512 (A = atoms per K block, the
+//   token count padded to 256, / 128): 512 bytes, byte 16 r0 + 4 r1 + j =
+//   token 128 a + 32 r1 + r0, 32-K block 4 kb + j. K-block-major, so the two
+//   atoms of a 256-token tile are one contiguous 1 KB copy.
 // Blocks past K and padding tokens (M .. the atoms' end) get code 127 (x1).
 // Blocks of the grid past `real_blocks` write those padding tokens' words.
 __global__ void __launch_bounds__(256) quant_mxfp4_act_kernel(const uint16_t *__restrict__ x, int M, int K,
-                                                              int64_t ldx, int segs, int KB, int real_blocks,
+                                                              int64_t ldx, int segs, int KB, int A, int real_blocks,
                                                               int pad_tokens, uint8_t *__restrict__ q,
                                                               uint8_t *__restrict__ sf) {
   if (threadIdx.x == 0) pdl_launch_dependents();   // the next kernel may start its weight stream
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(256) quant_mxfp4_act_kernel(const uint16_t *__
     if (i >= static_cast<int64_t>(pad_tokens) * KB) return;
     const int t = M + static_cast<int>(i / KB), kb = static_cast<int>(i % KB);
     const int r = t & 127;
-    *reinterpret_cast<uint32_t *>(sf + (static_cast<size_t>(t >> 7) * KB + kb) * 512 + 16 * (r & 31) + 4 * (r >> 5)) =
+    *reinterpret_cast<uint32_t *>(sf + (static_cast<size_t>(kb) * A + (t >> 7)) * 512 + 16 * (r & 31) + 4 * (r >> 5)) =
         0x7F7F7F7Fu;
     return;
   }
@@ -238,7 +240,7 @@ __global__ void __launch_bounds__(256) quant_mxfp4_act_kernel(const uint16_t *__
   const int kb = seg * 2 + (lane >> 4);
   if ((lane & 15) == 0 && kb < KB) {
     const int r = row & 127;
-    *reinterpret_cast<uint32_t *>(sf + (static_cast<size_t>(row >> 7) * KB + kb) * 512 + 16 * (r & 31) + 4 * (r >> 5)) =
+    *reinterpret_cast<uint32_t *>(sf + (static_cast<size_t>(kb) * A + (row >> 7)) * 512 + 16 * (r & 31) + 4 * (r >> 5)) =
         word;
   }
 }
@@ -380,10 +382,11 @@ cudaError_t launch_quant_mxfp4_act(const uint16_t *x, int64_t M, int64_t K, int6
   const int KB = static_cast<int>(ceil_div(K, 128));
   const int64_t real_blocks = ceil_div(M * segs, 8);
   const int64_t pad_tokens = mx_act_tokens_padded(M) - M;
+  const int A = static_cast<int>(mx_act_tokens_padded(M) / 128);
   const int64_t pad_blocks = ceil_div(pad_tokens * KB, 256);
   const dim3 grid(static_cast<unsigned>(real_blocks + pad_blocks));
   const cudaError_t e = launch_pdl(quant_mxfp4_act_kernel, grid, dim3(256), 0, st, x, static_cast<int>(M),
-                                   static_cast<int>(K), ldx, segs, KB, static_cast<int>(real_blocks),
+                                   static_cast<int>(K), ldx, segs, KB, A, static_cast<int>(real_blocks),
                                    static_cast<int>(pad_tokens), q, sf);
   if (e != cudaSuccess) return e;
   set_last_kernel("quant_mxfp4_act_kernel");

@@ -206,9 +206,10 @@ int r4_quantize_blockfp8_weight(const float *w, int64_t N, int64_t K, uint8_t *q
  *          (the checkpoint order of the weights); 16-byte aligned.
  *   scale  the ue8m0 scale codes in the GEMM's scale-atom layout, 16-byte
  *          aligned, at least r4_quant_mxfp4_act_scale_bytes(M, K) bytes:
- *          atoms of 512 bytes, atom (a, kb) at byte offset
- *          (a * ceil(K/128) + kb) * 512 for tokens [128 a, 128 a + 128) and
- *          K block [128 kb, 128 kb + 128); inside it, byte 16 r0 + 4 r1 + j
+ *          atoms of 512 bytes, K-block-major: atom (a, kb) at byte offset
+ *          (kb * A + a) * 512, A = ceil(M/256) * 2, for tokens
+ *          [128 a, 128 a + 128) and K block [128 kb, 128 kb + 128) (the two
+ *          atoms of a 256-token tile are adjacent); inside it, byte 16 r0 + 4 r1 + j
  *          is the scale of token 128 a + 32 r1 + r0, 32-K block 4 kb + j --
  *          the order in which tcgen05.cp 32x128b.warpx4 lays a scale block
  *          across tensor memory, the same as the weight's prepacked atoms.

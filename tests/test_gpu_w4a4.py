@@ -25,20 +25,23 @@ def r4q():
 
 def act_scale_atoms(scale, M, K):
     """Test-side permutation of scale codes [M, K/32] into the atom layout the
-    GEMM reads (byte 16 r0 + 4 r1 + j of atom (a, kb) = token 128 a + 32 r1 + r0,
-    32-K block 4 kb + j), padding code 127."""
+    GEMM reads: atoms K-block-major, atom (a, kb) at (kb * A + a) * 512; its
+    byte 16 r0 + 4 r1 + j = token 128 a + 32 r1 + r0, 32-K block 4 kb + j;
+    padding code 127."""
     A = -(-M // 256) * 2
     KB = -(-K // 128)
     full = np.full((A * 128, KB * 4), 127, np.uint8)
     full[:M, :K // 32] = scale
-    return np.ascontiguousarray(full.reshape(A, 4, 32, KB, 4).transpose(0, 3, 2, 1, 4)).reshape(-1)
+    # [a][r1][r0][kb][j] -> [kb][a][r0][r1][j]
+    return np.ascontiguousarray(full.reshape(A, 4, 32, KB, 4).transpose(3, 0, 2, 1, 4)).reshape(-1)
 
 
 def act_scale_codes(atoms, M, K):
     """Inverse of act_scale_atoms: (scale [M, K/32], padding all 127)."""
     A = -(-M // 256) * 2
     KB = -(-K // 128)
-    full = np.asarray(atoms, np.uint8).reshape(A, KB, 32, 4, 4).transpose(0, 3, 2, 1, 4).reshape(A * 128, KB * 4)
+    # [kb][a][r0][r1][j] -> [a][r1][r0][kb][j]
+    full = np.asarray(atoms, np.uint8).reshape(KB, A, 32, 4, 4).transpose(1, 3, 2, 0, 4).reshape(A * 128, KB * 4)
     pad_ok = bool(np.all(full[M:] == 127) and np.all(full[:, K // 32:] == 127))
     return full[:M, :K // 32], pad_ok
 
