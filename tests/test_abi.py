@@ -117,12 +117,53 @@ def test_validation_of_the_later_entry_points(r4q):
     assert lib.r4_check_quotients(odd4, good, S) == r4q.R4_ERR_MISALIGNED
 
 
+def test_validation_of_the_w4a4_entry_points_and_the_probe(r4q):
+    """The MXFP4 activation quantizer, the W4A4 GEMM and the MMA issue-rate
+    probe reject bad arguments on the host, before any device work; the
+    scale-buffer size query follows the documented atom layout."""
+    lib = r4q.lib()
+    P = ctypes.c_void_p
+    good = P(1 << 20)
+    odd8 = P((1 << 20) + 8)
+    S = P(0)
+    # scale atoms: tokens padded to 256, K to 128, 512 bytes per 128 x 128
+    for M, K in [(8, 5120), (256, 2048), (257, 416), (2048, 17408)]:
+        want = math.ceil(M / 256) * 2 * math.ceil(K / 128) * 512
+        assert lib.r4_quant_mxfp4_act_scale_bytes(M, K) == want
+    assert lib.r4_quant_mxfp4_act_scale_bytes(8, 48) == 0
+    assert lib.r4_quant_mxfp4_act_scale_bytes(0, 128) == 0
+    qa = lib.r4_quant_mxfp4_act
+    big = 1 << 30
+    assert qa(None, 8, 2048, 2048, good, good, big, S) == r4q.R4_ERR_INVALID_ARG
+    assert qa(good, 0, 2048, 2048, good, good, big, S) == r4q.R4_ERR_INVALID_ARG
+    assert qa(good, 8, 2048, 1024, good, good, big, S) == r4q.R4_ERR_INVALID_ARG
+    assert qa(good, 8, 2000, 2000, good, good, big, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert qa(good, 8, 2048, 2052, good, good, big, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert qa(odd8, 8, 2048, 2048, good, good, big, S) == r4q.R4_ERR_MISALIGNED
+    assert qa(good, 8, 2048, 2048, good, odd8, big, S) == r4q.R4_ERR_MISALIGNED
+    assert qa(good, 8, 2048, 2048, good, good, 100, S) == r4q.R4_ERR_WORKSPACE
+    g4 = lib.r4_gemm_w4a4_mxfp4
+    assert g4(good, None, good, 8, 256, 2048, good, 256, None, 0, S) == r4q.R4_ERR_INVALID_ARG
+    assert g4(good, good, good, 8, 256, 2048, good, 100, None, 0, S) == r4q.R4_ERR_INVALID_ARG
+    assert g4(good, good, good, 8, 256, 2000, good, 256, None, 0, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert g4(good, good, good, 8, 256, 96, good, 256, None, 0, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert g4(good, odd8, good, 8, 256, 2048, good, 256, None, 0, S) == r4q.R4_ERR_MISALIGNED
+    assert g4(good, good, odd8, 8, 256, 2048, good, 256, None, 0, S) == r4q.R4_ERR_MISALIGNED
+    pk = lib.r4_mma_peak
+    for kind, n, blocks, iters in [(0, 256, 152, 10), (4, 256, 152, 10), (1, 192, 152, 10), (1, 256, 0, 10),
+                                   (1, 256, 70000, 10), (1, 256, 152, 0)]:
+        assert pk(kind, n, blocks, iters, S) == r4q.R4_ERR_INVALID_ARG, (kind, n, blocks, iters)
+
+
 def test_row_kernel_options(r4q):
     lib = r4q.lib()
-    for key, bad, ok in [(11, 3, 8), (11, 16, 1), (13, 96, 128), (13, 512, 64)]:
+    for key, bad, ok in [(11, 3, 8), (11, 16, 1), (13, 96, 128), (13, 512, 64), (5, 3, 1), (5, -1, 2),
+                         (15, 5, 1), (15, -1, 4)]:
         assert lib.r4_set_option(key, bad) == r4q.R4_ERR_INVALID_ARG
         assert lib.r4_set_option(key, ok) == 0
         assert lib.r4_set_option(key, 0) == 0
+    assert lib.r4_set_option(5, 2) == 0          # the default: rolling L2 prefetch
+    assert lib.r4_set_option(14, 0) == 0 and lib.r4_set_option(14, 1) == 0
 
 
 def test_product_path_has_no_oracle_import():
