@@ -755,6 +755,8 @@ def run_ours(args, rank, world, local_rank):
             mma = mma_peaks(r4q, torch.cuda.get_device_properties(device).multi_processor_count)
             sections = run_sections(r4q, synth, device, sweep, l2_bytes, peaks, mma)
             sections["mma_peak_TFLOPs"] = mma
+            if not args.no_cpu_baseline:
+                sections["cpu_oracle"] = cpu_sections()
             sections["per_shape_decode"] = per
             # The full sections on a comment line of their own; the headline
             # line below stays short and carries a numeric digest of them.
@@ -784,6 +786,11 @@ def digest(per, sec, hbm):
     d["skinny_hot_us"] = {_shape_key(k): v["hot_us"] for k, v in sk.items()}
     d["quant_us"] = {k: v["us"] for k, v in sec.get("quant_per_token", {}).items()}
     d["fused_us"] = {k: v["us"] for k, v in sec.get("fused_quant", {}).items()}
+    cpu = sec.get("cpu_oracle")
+    if cpu:
+        d["cpu_oracle"] = {"prefill_TFLOPs": {k: v["TFLOPs"] for k, v in cpu["prefill_w4a8"].items()},
+                           "blockfp8_TFLOPs": {_shape_key(k): v["TFLOPs"] for k, v in cpu["blockfp8"].items()},
+                           "cores": cpu["cores"]}
     for name in ("w4a4", "tiny_w4a8"):
         if name in sec:
             d[name] = sec[name] if name == "tiny_w4a8" else sec[name].get("digest")
@@ -830,6 +837,69 @@ def cpu_baseline(budget_s=15.0):
             "kind": "oracle",
             "sample": f"decode sweep, all 15 (M,N,K), first {rows} weight rows of each shape "
                       f"({t:.1f} s; NumPy float64, BLAS threads = host default)"}
+
+
+def cpu_sections(rows=256):
+    """The oracle (NumPy float64) timed on the host cores for every other
+    configuration: the full problem where it is small (tiny, decode-sized
+    block-FP8, skinny), else the first `rows` tokens of it (prefill W4A8,
+    block-FP8 at M = 2048), with the rate taken over the sample. Synthetic
+    codes and scales (the oracle's cost does not depend on their values)."""
+    import numpy as np
+    from block_scaled_precision_token_gb300 import synth
+    from oracle import gemm as G
+    from oracle import quant as Q
+    out = {}
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    def mx_weight(N, K, seed):
+        return (synth.uniform_bytes((N, K // 2), seed).numpy(),
+                synth.uniform_bytes((N, K // 32), seed + 1, low=117, high=125).numpy())
+
+    def e4m3(shape, seed):
+        q = synth.uniform_bytes(shape, seed).numpy()
+        q[(q & 0x7F) == 0x7F] = 0x3C
+        return q
+
+    M, N, K = synth.TINY["M"], synth.TINY["N"], synth.TINY["K"]
+    x = synth.activations(M, K, synth.CFG_TINY).float().numpy()
+    p, sc = mx_weight(N, K, 71)
+    t = timed(lambda: G.gemm_w4a8(*Q.quant_act(x), p, sc))
+    out["tiny_quant_gemm"] = {"us": round(t * 1e6, 1)}
+    pre = {}
+    for (N, K) in synth.PREFILL_NK:
+        p, sc = mx_weight(N, K, 72)
+        q = e4m3((rows, K), 73)
+        s = np.full(rows, 0.01, np.float32)
+        t = timed(lambda: G.gemm_w4a8(q, s, p, sc))
+        pre[f"N{N}_K{K}"] = {"TFLOPs": round(2.0 * rows * N * K / t / 1e12, 4), "sample": f"{rows} tokens"}
+    out["prefill_w4a8"] = pre
+    bf = {}
+    for (N, K) in synth.BLOCKFP8_NK:
+        w = e4m3((N, K), 74)
+        Ws = np.full((N // 128, K // 128), 1e-3, np.float32)
+        for M in synth.BLOCKFP8_M:
+            m = min(M, rows)
+            q = e4m3((m, K), 75)
+            As = np.full((m, K // 128), 1e-2, np.float32)
+            t = timed(lambda: G.gemm_blockfp8(q, As, w, Ws))
+            bf[f"M{M}_N{N}_K{K}"] = {"TFLOPs": round(2.0 * m * N * K / t / 1e12, 4),
+                                     "sample": "full" if m == M else f"{m} tokens"}
+    out["blockfp8"] = bf
+    sk = {}
+    for (N, K) in synth.SKINNY_NK:
+        w = synth.weights_bf16(N, K, synth.CFG_SKINNY).float().numpy()
+        for M in (8, 64):
+            x = synth.activations(M, K, synth.CFG_SKINNY).float().numpy()
+            t = timed(lambda: G.gemm_bf16(x, w))
+            sk[f"M{M}_N{N}_K{K}"] = {"us": round(t * 1e6, 1)}
+    out["skinny_bf16"] = sk
+    out["cores"] = os.cpu_count()
+    return out
 
 
 def run_reference(args, rank, world):
