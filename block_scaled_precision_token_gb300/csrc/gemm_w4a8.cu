@@ -546,8 +546,112 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
       const int tile = nt * p.t_tiles + tt;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
       float *part = (p.splits > 1 && !p.cluster) ? p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (128 * BT) : nullptr;
+      bool drained = false;
+      if constexpr (ISS == 1 && CH == 32 && BT % 64 == 0) {
+        if (p.splits == 1 && p.tma_store) {
+          // Prefill tile on one accumulator (the MMA waits for it: a second
+          // 256-column accumulator would not leave room for the scale
+          // columns). Every cycle spent here is tensor-pipe idle time, so
+          // the drain is built for throughput:
+          //  * 32-token chunks leave tensor memory in the 16x256b shape
+          //    (two loads of 16 lanes), one chunk in flight while the
+          //    previous one is stored;
+          //  * each thread scales and rounds token PAIRS of one n into a
+          //    bf16x2 word (the per-token scales of the next chunk are read
+          //    one chunk ahead), and four stmatrix.trans per chunk write the
+          //    8x8 blocks as [token][n] rows -- 4 shared stores per chunk
+          //    instead of 32 two-byte ones;
+          //  * each warp owns a [32 token][32 n] region per buffer (64-byte
+          //    rows, 64-byte swizzle: the eight rows of a matrix land in
+          //    eight different bank groups) and issues its own TMA store of
+          //    it, so the four warps never wait for one another.
+          // Measured on GB300 (graph-timed, cold weights), against one
+          // thread storing a [32][128] buffer between two 128-thread
+          // barriers, filled by 32 two-byte stores per thread: the drain of
+          // a 256-token tile 5,500 -> 3,450 cycles (W4A4), M=2048 prefill
+          // 5-7 % faster (W4A8 34816x5120 263 -> 247 us, W4A4 216 -> 201
+          // us). Not kept: the same stmatrix stores into an unswizzled
+          // [32][128] buffer (slower than the two-byte stores: eight rows of
+          // a matrix share four banks); per-token scales staged for the
+          // whole tile in shared memory (as fast here, but the cluster
+          // split-K prefill of the same kernel lost 12 %); draining every
+          // chunk into registers first (255 registers, spills); plain
+          // coalesced global stores (M=2048, 34816x5120: 260 -> 345 us).
+          uint32_t ra[32], rb[32];   // [0,16): lanes 0-15 of the quarter; [16,32): lanes 16-31
+          const uint32_t abase = lane_base + static_cast<uint32_t>(acc * BT);
+          auto load_chunk = [&](uint32_t (&r)[32], int c0) {
+            tc_ld_16x256b_x4(abase + static_cast<uint32_t>(c0), r);
+            tc_ld_16x256b_x4(abase + (16u << 16) + static_cast<uint32_t>(c0), r + 16);
+          };
+          const int tq = 2 * (lane & 3);                 // first of this thread's token pair in an 8-token group
+          const int mrow = lane & 7, mmat = lane >> 3;   // stmatrix row (token) and matrix (8-n group) addressed
+          const uint32_t st_off =
+              static_cast<uint32_t>(q * 2048 + mrow * 64 + ((mmat ^ ((mrow >> 1) & 3)) << 4));
+          const bool q_store = nt * 128 + q * 32 < p.N;  // this warp's 32 n hold at least one column
+          float sc_cur[8], sc_nxt[8];                    // per-token scales of the token pairs, 4 groups
+          auto load_scales = [&](float (&sc)[8], int c0) {
+            if constexpr (!A4) {
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                const int t = t0 + c0 + 8 * g + tq;
+                sc[2 * g] = (t < p.M) ? __ldg(p.s + t) : 0.f;
+                sc[2 * g + 1] = (t + 1 < p.M) ? __ldg(p.s + t + 1) : 0.f;
+              }
+            }
+          };
+          auto stage_and_store = [&](const uint32_t (&r)[32], int c0) {
+            if (c0 + 32 < BT) load_scales(sc_nxt, c0 + 32);
+            uint16_t *stg = staging + (out_chunk & 1u) * (CH * 128);
+            const uint32_t sbase = smem_u32(stg) + st_off;
+            if (lane == 0) bulk_wait_read1();   // this warp's store from two chunks ago has read its region
+            __syncwarp();
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              uint32_t w[4];   // matrix m: n = 8m + lane/4 of the quarter, tokens 8g + tq, +1
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const int b = 16 * (m >> 1) + 4 * g + 2 * (m & 1);
+                float v0 = __uint_as_float(r[b]), v1 = __uint_as_float(r[b + 1]);
+                if constexpr (!A4) {
+                  v0 *= sc_cur[2 * g];
+                  v1 *= sc_cur[2 * g + 1];
+                }
+                w[m] = pack_bf16x2(v0, v1);
+              }
+              stmatrix_x4_trans(sbase + static_cast<uint32_t>(g * 8 * 64), w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (q_store) tma_store_2d(&tm_c, stg + q * 1024, nt * 128 + q * 32, t0 + c0);
+              bulk_commit();   // (an empty group when nothing was stored keeps the count per chunk)
+            }
+            ++out_chunk;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sc_cur[i] = sc_nxt[i];
+          };
+          load_scales(sc_cur, 0);
+          load_chunk(ra, 0);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BT; c0 += CH) {
+          for (int c0 = 0; c0 < BT; c0 += 64) {
+            tc_wait_ld();              // chunk c0 in ra
+            load_chunk(rb, c0 + 32);   // chunk c0 + 32 in flight
+            stage_and_store(ra, c0);
+            tc_wait_ld();              // chunk c0 + 32 in rb
+            if (c0 + 64 < BT) {
+              load_chunk(ra, c0 + 64);
+            } else {
+              tc_fence_before();   // every chunk is in registers: the accumulator is free
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acce_bar[acc]);
+            }
+            stage_and_store(rb, c0 + 32);
+          }
+          drained = true;
+        }
+      }
+#pragma unroll 1
+      for (int c0 = 0; c0 < (drained ? 0 : BT); c0 += CH) {
         uint32_t r[32];
         float v[32];
 #pragma unroll 1
@@ -567,9 +671,11 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce_bar[acc]);
         }
-        if (p.splits == 1 && p.tma_store) {
+        if (BT < 128 && p.splits == 1 && p.tma_store) {
           // Stage [CH tokens][128 n] bf16 in smem, then one TMA tensor store;
-          // the store clips rows >= M and columns >= N.
+          // the store clips rows >= M and columns >= N. (Prefill tiles with a
+          // TMA-storable C took the per-warp drain above: their tensor map
+          // has the per-warp box.)
           uint16_t *stg = staging + (out_chunk & 1u) * (CH * 128);
           if (leader) bulk_wait_read1();   // the store issued two chunks ago has read this buffer
           named_bar_sync(1, 128);
@@ -726,7 +832,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
         if ((prev & kArrivalMask) == p.splits - 1) atomicExch(p.counters + tile2, 0);
       }
     }
-    if (leader) bulk_wait_all();   // output stores complete before the CTA's smem goes away
+    if (lane == 0) bulk_wait_all();   // output stores complete before the CTA's smem goes away
   }
 
   tc_fence_before();
@@ -789,9 +895,11 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *xsf, const uint8_
   if ((reinterpret_cast<uintptr_t>(c) % 16) == 0 && (ldc * 2) % 16 == 0 && (N * 2) % 16 == 0) {
     const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
     const uint64_t strides[1] = {static_cast<uint64_t>(ldc) * 2};
-    const uint32_t box[2] = {128, static_cast<uint32_t>(C::kOutChunk)};
+    // Prefill tiles (BT >= 128) store per warp: [32 tokens][32 n] boxes in
+    // the 64-byte swizzle; decode tiles store [chunk][128 n] unswizzled.
+    const uint32_t box[2] = {BT >= 128 ? 32u : 128u, static_cast<uint32_t>(C::kOutChunk)};
     use_tma_store = encode_tiled(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims, strides, box,
-                                 CU_TENSOR_MAP_SWIZZLE_NONE) == CUDA_SUCCESS;
+                                 BT >= 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE) == CUDA_SUCCESS;
   }
   if (!use_tma_store) tm_c = tm_x;   // not read by the kernel in that case
   Params p;

@@ -384,6 +384,40 @@ __device__ __forceinline__ void tc_ld_32x32b_x16h(uint32_t taddr, uint32_t (&r)[
       : "memory");
 }
 
+// 16 lanes x 32 consecutive 32-bit columns in the 16x256b shape (four
+// 8-column repeats), into r[0..16). Thread i of the warp receives, in repeat
+// g (registers 4g..4g+3): lane i/4 at columns 8g + 2(i%4) and 8g + 2(i%4) + 1,
+// then lane 8 + i/4 at the same two columns -- the accumulator fragment of
+// the warp-level m16n8 MMA, which is the fragment stmatrix consumes. (Checked
+// on GB300: an epilogue built on this reading reproduces the 32x32b one bit
+// for bit.)
+__device__ __forceinline__ void tc_ld_16x256b_x4(uint32_t taddr, uint32_t *r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Two floats to a bf16 pair (round to nearest even): lo in bits 0..15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Four 8x8 b16 matrices to shared memory, transposed: register k of thread i
+// holds row i/4, columns 2(i%4) and 2(i%4) + 1 of matrix k; thread 8k + j
+// supplies the 16-byte-aligned address at which column j of matrix k is
+// stored as 8 consecutive b16.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
