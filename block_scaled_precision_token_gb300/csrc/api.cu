@@ -176,7 +176,7 @@ int r4_set_option(int key, int64_t value) {
   switch (key) {
     case 1: options().w4a8_splits = static_cast<int>(value); return R4_OK;
     case 2:
-      if (value != 0 && value != 16 && value != 32 && value != 64 && value != 128 && value != 256)
+      if (value != 0 && value != 16 && value != 32 && value != 64 && value != 128 && value != 192 && value != 256)
         return R4_ERR_INVALID_ARG;
       options().w4a8_token_tile = static_cast<int>(value);
       return R4_OK;

@@ -71,9 +71,12 @@ constexpr uint32_t kWSmem = 128 * 128;  // expanded e2m1 tile: 128 rows x 128 on
 constexpr uint32_t kWTxBytes = 8192;
 constexpr uint32_t kSfBytes = 512;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfaCol = 256;       // 4 columns per stage, up to 16 stages
-constexpr uint32_t kSfbCol = 320;       // 16 columns of constant 127 per MMA warp (up to 4)
-constexpr uint32_t kSfbColA4 = 320;     // W4A4: 8 columns of activation scales per stage (up to 16)
+// Tensor-memory columns: the accumulators first (kIss x kNumAcc x BT
+// columns), then the scale columns from kSfaCol on -- 256, or 384 behind the
+// two 192-column accumulators of the W4A8 192-token tile:
+//   kSfaCol + 4 x stage          weight scales, 4 columns per stage (up to 16 stages)
+//   kSfaCol + 64 + 16 x warp     W4A8: 16 columns of constant 127 per MMA warp (up to 4)
+//   kSfaCol + 64 + 8 x stage     W4A4: activation scales, 8 columns per stage (up to 16)
 constexpr int kMaxStages = 16;
 constexpr int kMaxClusterSplit = 6;   // the planner splits K across a cluster of 2..6 CTAs
 
@@ -126,7 +129,12 @@ struct Cfg {
   static constexpr int kIss = BT <= 64 ? 4 : 1;
   static constexpr int kProd = BT <= 64 ? 4 : (A4 ? 2 : 1);   // TMA producer warps
   static constexpr int kPad = kProd > kIss ? kProd : kIss;    // slot padding of a unit
-  static constexpr int kNumAcc = (kIss * 2 * BT <= 256) ? 2 : 1;
+  // Two accumulators (the epilogue drains one while the MMAs fill the
+  // other) wherever they leave room for the scale columns.
+  static constexpr int kNumAcc = (kIss * 2 * BT <= 256 || (!A4 && kIss * 2 * BT <= 384)) ? 2 : 1;
+  static constexpr uint32_t kAccCols = static_cast<uint32_t>(kIss * kNumAcc * BT);
+  static constexpr uint32_t kSfaCol = kAccCols <= 256 ? 256u : 384u;
+  static constexpr uint32_t kSfbCol = kSfaCol + 64u;
   static constexpr int kThreads = 32 * (kProd + kIss + 4);    // producers, MMA issuers, 4 epilogue
   static constexpr int kEpiWarp0 = kProd + kIss;
   static constexpr uint32_t kWBytes = A4 ? 8192u : kWSmem;      // weight tile in shared memory
@@ -142,7 +150,8 @@ struct Cfg {
   static constexpr uint32_t kTxBytes = kWTxBytes + kXSmem + kSfBytes * (1 + kXAtoms);
   static constexpr uint32_t kMiscBytes = 1024;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kMiscBytes + kOutBytes + 1024;  // + align slack
-  static_assert(kIss * kNumAcc * BT <= 256, "accumulators overlap the scale columns");
+  static_assert(kAccCols <= kSfaCol, "accumulators overlap the scale columns");
+  static_assert(kSfbCol + (A4 ? 8u * kMaxStages : 16u * kIss) <= kTmemCols, "scale columns past tensor memory");
   static_assert(kStages >= kPad && kStages % kPad == 0, "stage count");
 };
 
@@ -430,7 +439,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
     // ------------------------------------------------------------ MMA issuers (warps PROD..PROD+ISS-1)
     const int mw = warp - PROD;
     if (lane == 0) {
-      const uint32_t sfb = tmem + kSfbCol + 16u * static_cast<uint32_t>(mw);
+      const uint32_t sfb = tmem + C::kSfbCol + 16u * static_cast<uint32_t>(mw);
       if constexpr (!A4) {
         const uint64_t sfb_desc = sdesc_sf_32x16(smem_u32(sfb_const));
 #pragma unroll
@@ -458,14 +467,14 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
           if (i < nkb) {
             tc_fence_after();
             uint8_t *st = smem + stage * C::kStageBytes;
-            const uint32_t sfa = tmem + kSfaCol + 4u * static_cast<uint32_t>(stage);
+            const uint32_t sfa = tmem + C::kSfaCol + 4u * static_cast<uint32_t>(stage);
             tc_cp_32x128b_warpx4(sfa, sdesc_sf_32x16(smem_u32(st + C::kSfOff)));
             const uint32_t a_base = smem_u32(st);
             const uint32_t b_base = smem_u32(st + C::kWBytes);
             if constexpr (A4) {
               // activation scales: column 4a + (token / 32) of this stage's slot holds
               // tokens 128a .. 128a + 127 of the tile, one byte per 32 K
-              const uint32_t sfbs = tmem + kSfbColA4 + 8u * static_cast<uint32_t>(stage);
+              const uint32_t sfbs = tmem + C::kSfbCol + 8u * static_cast<uint32_t>(stage);
 #pragma unroll
               for (int a = 0; a < C::kXAtoms; ++a)
                 tc_cp_32x128b_warpx4(sfbs + 4u * a, sdesc_sf_32x16(smem_u32(st + C::kSfOff + kSfBytes * (1 + a))));
@@ -944,6 +953,7 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *xsf, const uint8_
                     : BT == 32  ? "w4a8_mxf8f6f4_kernel<32>"
                     : BT == 64  ? "w4a8_mxf8f6f4_kernel<64>"
                     : BT == 128 ? "w4a8_mxf8f6f4_kernel<128>"
+                    : BT == 192 ? "w4a8_mxf8f6f4_kernel<192>"
                                 : "w4a8_mxf8f6f4_kernel<256>");
   return cudaGetLastError() == cudaSuccess ? R4_OK : R4_ERR_CUDA;
 }
@@ -983,6 +993,7 @@ int max_clusters(int bt, int s, bool a4) {
     case 32: return a4 ? max_clusters_bt<32, true>(s) : max_clusters_bt<32, false>(s);
     case 64: return a4 ? max_clusters_bt<64, true>(s) : max_clusters_bt<64, false>(s);
     case 128: return a4 ? max_clusters_bt<128, true>(s) : max_clusters_bt<128, false>(s);
+    case 192: return a4 ? 0 : max_clusters_bt<192, false>(s);
     case 256: return a4 ? max_clusters_bt<256, true>(s) : max_clusters_bt<256, false>(s);
     default: return 0;
   }
@@ -1008,16 +1019,14 @@ int max_clusters(int bt, int s, bool a4) {
 // atom (tiles of 128 or 256 tokens, or a single tile of up to 64 tokens
 // starting at token 0), so that every activation scale of a tile sits at the
 // start of the atom copied into tensor memory.
-static GemmPlan plan_mx(int64_t M, int64_t N, int64_t K, int sms, bool a4) {
+//
+// Over 128 tokens W4A8 chooses between 256-token tiles (one accumulator: the
+// tensor pipe waits while the epilogue drains it, ~2.5 us per unit) and
+// 192-token tiles (two accumulators: the drain overlaps the next unit's
+// MMAs, at a quarter less work per unit and up to 191 padding tokens) by
+// the modeled time of each.
+static GemmPlan plan_mx_bt(int64_t M, int64_t N, int64_t K, int sms, bool a4, int bt, double *t_model) {
   GemmPlan pl;
-  int bt = options().w4a8_token_tile;
-  if (a4 && bt != 0 && bt < 128 && M > bt) bt = 0;   // a forced small tile must hold every token
-  // 33..64 tokens against a narrow weight (few 128-row tiles) run as two
-  // 32-token tiles: twice the tiles to spread over the SMs (measured: M=64,
-  // 2048x5120 9.2 vs 10.2 us; at 5120x17408 the 64-token tile wins, 19.4 vs
-  // 25.3 us).
-  if (bt == 0)
-    bt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? ((!a4 && ceil_div(N, 128) <= 24) ? 32 : 64) : M <= 128 ? 128 : 256;
   pl.BT = bt;
   pl.n_tiles = static_cast<int>(ceil_div(N, 128));
   pl.t_tiles = static_cast<int>(ceil_div(M, bt));
@@ -1033,6 +1042,11 @@ static GemmPlan plan_mx(int64_t M, int64_t N, int64_t K, int sms, bool a4) {
   const double kb_flops = 2.0 * 128 * bt * 128;
   const double part_bytes = 128.0 * bt * 4;
   const double xchg_s = (bt <= 64 ? 2.5e-6 : 1.0e-6) * ((bt + 31) / 32);   // one cluster exchange per 32 tokens
+  // Epilogue drain of a prefill unit, on the critical path once per unit
+  // with one accumulator, else once per CTA (measured ~5,000 cycles at 256
+  // tokens).
+  const bool one_acc = bt == 256;
+  const double drain = bt >= 128 ? 1.0e-8 * bt : 0.0;
   const int forced = options().w4a8_splits;
   // Prefill tiles (BT >= 128) split through the workspace only while the
   // tile count is under a quarter of the SM count, and through a cluster
@@ -1073,14 +1087,14 @@ static GemmPlan plan_mx(int64_t M, int64_t N, int64_t K, int sms, bool a4) {
       const double t_unit =
           std::max(kbps * kb_bytes / std::min(hbm / active, sm_bw), kbps * kb_flops / sm_flops);
       const double xchg = waves == 1 ? 3.0e-6 : xchg_s;   // one whole-tile round, or a round per 32 tokens
-      t = waves * t_unit + xchg + 0.5e-6 * s;
+      t = waves * t_unit + xchg + 0.5e-6 * s + (one_acc ? waves : 1.0) * drain;
       grid = active;
     } else {
       const int64_t active = std::min<int64_t>(units, sms);
       const double waves = std::ceil(static_cast<double>(units) / sms);
       const double t_unit =
           std::max(kbps * kb_bytes / std::min(hbm / active, sm_bw), kbps * kb_flops / sm_flops);
-      t = waves * t_unit;
+      t = waves * t_unit + (one_acc ? waves : 1.0) * drain;
       if (s > 1) t += (waves + s) * part_bytes / red_bw;
       grid = active;
     }
@@ -1102,7 +1116,28 @@ static GemmPlan plan_mx(int64_t M, int64_t N, int64_t K, int sms, bool a4) {
     pl.counters_bytes = round_up(static_cast<size_t>(tiles) * 4, 256);
     pl.ws_bytes = pl.counters_bytes + static_cast<size_t>(pl.units) * 128 * bt * 4;
   }
+  if (t_model) *t_model = best_t;
   return pl;
+}
+
+static GemmPlan plan_mx(int64_t M, int64_t N, int64_t K, int sms, bool a4) {
+  int bt = options().w4a8_token_tile;
+  if (a4 && bt != 0 && bt < 128 && M > bt) bt = 0;   // a forced small tile must hold every token
+  if (a4 && bt == 192) bt = 0;                        // W4A4 tiles start on 128-token scale atoms
+  if (bt != 0) return plan_mx_bt(M, N, K, sms, a4, bt, nullptr);
+  // 33..64 tokens against a narrow weight (few 128-row tiles) run as two
+  // 32-token tiles: twice the tiles to spread over the SMs (measured: M=64,
+  // 2048x5120 9.2 vs 10.2 us; at 5120x17408 the 64-token tile wins, 19.4 vs
+  // 25.3 us).
+  if (M <= 128) {
+    bt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? ((!a4 && ceil_div(N, 128) <= 24) ? 32 : 64) : 128;
+    return plan_mx_bt(M, N, K, sms, a4, bt, nullptr);
+  }
+  double t256 = 0.0, t192 = 0.0;
+  const GemmPlan p256 = plan_mx_bt(M, N, K, sms, a4, 256, &t256);
+  if (a4) return p256;
+  const GemmPlan p192 = plan_mx_bt(M, N, K, sms, a4, 192, &t192);
+  return t192 < t256 ? p192 : p256;
 }
 
 GemmPlan plan_w4a8(int64_t M, int64_t N, int64_t K, int sms) { return plan_mx(M, N, K, sms, false); }
@@ -1115,6 +1150,7 @@ int launch_gemm_w4a8(const uint8_t *q, const float *s, const uint8_t *packed, in
     case 32: return w4a8::launch_bt<32, false>(q, s, nullptr, packed, M, N, K, c, ldc, ws, pl, st);
     case 64: return w4a8::launch_bt<64, false>(q, s, nullptr, packed, M, N, K, c, ldc, ws, pl, st);
     case 128: return w4a8::launch_bt<128, false>(q, s, nullptr, packed, M, N, K, c, ldc, ws, pl, st);
+    case 192: return w4a8::launch_bt<192, false>(q, s, nullptr, packed, M, N, K, c, ldc, ws, pl, st);
     case 256: return w4a8::launch_bt<256, false>(q, s, nullptr, packed, M, N, K, c, ldc, ws, pl, st);
     default: return R4_ERR_INVALID_ARG;
   }

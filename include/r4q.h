@@ -358,8 +358,9 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
 /*
  * r4_set_option -- benchmarking overrides of the host-side schedule choice
  * (process-wide, not thread-safe). key 1: force the W4A8 split-K factor
- * (0 = automatic); key 2: force the W4A8 token tile (0 = automatic, else
- * 16/32/64/128/256); key 3: force the block-FP8 split-K factor; key 4:
+ * (0 = automatic); key 2: force the W4A8/W4A4 token tile (0 = automatic,
+ * else 16/32/64/128/192/256; 192 is a W4A8 tile, W4A4 then chooses its
+ * own); key 3: force the block-FP8 split-K factor; key 4:
  * programmatic dependent launch on (1, default) or off (0); key 5: L2
  * prefetch of the weight stream of the W4A8/W4A4 GEMMs: 2 (default) a
  * rolling window of 8 K blocks beyond each decode CTA's pipeline ring, 1

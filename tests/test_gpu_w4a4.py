@@ -186,7 +186,7 @@ def test_ragged_shapes_and_guard_band(r4q):
     assert np.all(full.float().cpu().numpy()[:, N:] == 7.0), "kernel wrote outside columns [0, N)"
 
 
-@pytest.mark.parametrize("bt", [0, 64, 128, 256])
+@pytest.mark.parametrize("bt", [0, 64, 128, 192, 256])   # 192: W4A4 falls back to its own choice
 @pytest.mark.parametrize("splits,cluster", [(1, 1), (3, 1), (3, 0), (8, 0)])
 def test_forced_tiles_and_splits(r4q, bt, splits, cluster):
     M, N, K = 40, 384, 1024

@@ -85,7 +85,7 @@ def test_ragged_shapes_and_guard_band(r4q):
     assert np.all(g == 7.0), "kernel wrote outside columns [0, N)"
 
 
-@pytest.mark.parametrize("bt", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("bt", [16, 32, 64, 128, 192, 256])
 @pytest.mark.parametrize("splits", [1, 3, 8])
 def test_forced_tiles_and_splits(r4q, bt, splits):
     M, N, K = 40, 384, 1024
@@ -125,6 +125,33 @@ def test_split_k_paths(r4q, cluster, M, N, K, splits):
     c64, _ = G.gemm_w4a8(q, s, p, sc, rows=rows)
     got = c if rows is None else c[:, torch.from_numpy(rows).cuda()]
     assert_gemm_matches(got, c64, f"M={M} N={N} K={K} splits={splits} cluster={cluster}")
+    assert torch.equal(c, c2), "not deterministic across calls"
+    assert np.all(full.float().cpu().numpy()[:, N:] == 7.0), "kernel wrote outside columns [0, N)"
+
+
+@pytest.mark.parametrize("bt", [128, 192, 256])
+@pytest.mark.parametrize("M,N", [(1000, 4008), (1000, 4096), (2100, 2056)])
+def test_prefill_tiles_many_units(r4q, bt, M, N):
+    """Prefill tiles with more units than CTAs, so that each CTA drains one
+    accumulator while the next unit's MMAs fill the other (192 and 128
+    tokens) or waits for it (256): ragged last token tile, N ending inside a
+    warp's 32 columns (4008 = 31 x 128 + 40: one partial and two empty
+    per-warp stores in the last weight tile), a guard band right of N,
+    deterministic across calls."""
+    K = 512
+    q, s, p, sc = _dense_inputs(M, N, K, synth.CFG_PREFILL)
+    ldc = N + 40
+    r4q.r4_set_option(2, bt)
+    r4q.r4_set_option(1, 1)
+    try:
+        c, full = _run(r4q, q, s, p, sc, N, K, ldc=ldc)
+        c2, _ = _run(r4q, q, s, p, sc, N, K)
+    finally:
+        r4q.r4_set_option(1, 0)
+        r4q.r4_set_option(2, 0)
+    rows = np.unique(np.concatenate([synth.sample_indices(N, 256, M).numpy(), [0, 127, 128, N - 1]]))
+    c64, _ = G.gemm_w4a8(q, s, p, sc, rows=rows)
+    assert_gemm_matches(c[:, torch.from_numpy(rows).cuda()], c64, f"bt={bt} M={M} N={N}")
     assert torch.equal(c, c2), "not deterministic across calls"
     assert np.all(full.float().cpu().numpy()[:, N:] == 7.0), "kernel wrote outside columns [0, N)"
 
