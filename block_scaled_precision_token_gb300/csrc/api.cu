@@ -187,6 +187,10 @@ int r4_set_option(int key, int64_t value) {
       if (value < 0 || value > 4) return R4_ERR_INVALID_ARG;
       options().skinny_groups = static_cast<int>(value);
       return R4_OK;
+    case 16:
+      if (value < 0 || value > 2) return R4_ERR_INVALID_ARG;
+      options().stream_k = static_cast<int>(value);
+      return R4_OK;
     case 5:
       if (value < 0 || value > 2) return R4_ERR_INVALID_ARG;
       options().l2_prefetch = static_cast<int>(value);

@@ -85,6 +85,9 @@ struct Params {
   const uint8_t *xsf;    // W4A4: activation scale atoms [KB][xatoms][512] (K-block-major)
   int xatoms;            // W4A4: 128-token scale atoms per K block
   int t_tiles, splits, kb_per_split, units;
+  int sk;                // 1: stream-K -- CTA c of sk_grid owns the K blocks [c*T/G, (c+1)*T/G) of the
+                         // tile-major sequence of all T = tiles x KB blocks; unit c + j*G is its j-th tile piece
+  int sk_grid, sk_total; // G and T of the stream-K schedule
   int ldc;
   int tma_store;         // 1: bf16 output tiles leave through smem + TMA tensor stores
   int l2_prefetch;       // 1: producer 0 prefetches the CTA's whole weight range into L2 at start;
@@ -155,13 +158,47 @@ struct Cfg {
   static_assert(kStages >= kPad && kStages % kPad == 0, "stage count");
 };
 
+// Stream-K: first K block (tile-major) of CTA c, and the CTA that owns
+// block x (the largest c with c*T/G <= x).
+// (The planner keeps sk_total x sk_grid below 2^31: 32-bit arithmetic.)
+__device__ __forceinline__ int sk_begin(const Params &p, int c) {
+  return static_cast<int>(static_cast<uint32_t>(c * p.sk_total) / static_cast<uint32_t>(p.sk_grid));
+}
+__device__ __forceinline__ int sk_cta(const Params &p, int x) {
+  return static_cast<int>(static_cast<uint32_t>((x + 1) * p.sk_grid - 1) / static_cast<uint32_t>(p.sk_total));
+}
+// CTAs whose K ranges share `tile` (1: the tile is one CTA's alone).
+__device__ __forceinline__ int sk_segments(const Params &p, int tile) {
+  return sk_cta(p, tile * p.KB + p.KB - 1) - sk_cta(p, tile * p.KB) + 1;
+}
+
+// Unit u -> weight tile nt, token tile tt, piece sp and K blocks [kb0, kb1)
+// of the tile. Under stream-K a unit past its CTA's range is empty
+// (kb0 == kb1): every role skips it.
 __device__ __forceinline__ void decode_unit(const Params &p, int u, int &nt, int &tt, int &sp, int &kb0, int &kb1) {
-  const int tile = u / p.splits;
-  sp = u - tile * p.splits;
+  int tile;
+  if (p.sk) {
+    const int c = u % p.sk_grid, j = u / p.sk_grid;
+    const int a = sk_begin(p, c), b = sk_begin(p, c + 1);
+    const int ntiles = p.sk_total / p.KB;
+    tile = a / p.KB + j;
+    const int lo = max(a, tile * p.KB), hi = min(b, (tile + 1) * p.KB);
+    sp = j;
+    if (hi <= lo || tile >= ntiles) {
+      tile = min(tile, ntiles - 1);
+      kb0 = kb1 = 0;
+    } else {
+      kb0 = lo - tile * p.KB;
+      kb1 = hi - tile * p.KB;
+    }
+  } else {
+    tile = u / p.splits;
+    sp = u - tile * p.splits;
+    kb0 = sp * p.kb_per_split;
+    kb1 = min(p.KB, kb0 + p.kb_per_split);
+  }
   nt = tile / p.t_tiles;
   tt = tile - nt * p.t_tiles;
-  kb0 = sp * p.kb_per_split;
-  kb1 = min(p.KB, kb0 + p.kb_per_split);
 }
 
 // Rolling L2 prefetch of the decode weight stream: one CTA keeps only its
@@ -179,25 +216,35 @@ constexpr int kPfAhead = 8;
 // (relative to the unit's first block).
 struct PfCursor {
   int u, kb;
+  int nkb = 0;      // K blocks of unit u
+  size_t blk = 0;   // tile-major index of unit u's first K block
 };
+
+// Decode the cursor's unit once (the rolling prefetch runs every slot).
+__device__ __forceinline__ void pf_load(const Params &p, PfCursor &c) {
+  if (c.u >= p.units) return;
+  int nt, tt, sp, kb0, kb1;
+  decode_unit(p, c.u, nt, tt, sp, kb0, kb1);
+  c.nkb = kb1 - kb0;
+  c.blk = static_cast<size_t>(nt) * p.KB + kb0;
+}
 
 // Bulk L2 prefetch of `count` K blocks (weight codes and scale atoms, both
 // contiguous within a unit) from the cursor on, across unit boundaries.
 __device__ __forceinline__ void prefetch_blocks_l2(const Params &p, PfCursor &c, int count) {
   while (count > 0 && c.u < p.units) {
-    int nt, tt, sp, kb0, kb1;
-    decode_unit(p, c.u, nt, tt, sp, kb0, kb1);
-    const int n = min(count, kb1 - kb0 - c.kb);
+    const int n = min(count, c.nkb - c.kb);
     if (n > 0) {
-      const size_t blk = static_cast<size_t>(nt) * p.KB + kb0 + c.kb;
+      const size_t blk = c.blk + c.kb;
       bulk_prefetch_l2(p.w + blk * 8192, static_cast<uint32_t>(n) * 8192u);
       bulk_prefetch_l2(p.sf + blk * kSfBytes, static_cast<uint32_t>(n) * kSfBytes);
       c.kb += n;
       count -= n;
     }
-    if (c.kb >= kb1 - kb0) {
+    if (c.kb >= c.nkb) {
       c.u += gridDim.x;
       c.kb = 0;
+      pf_load(p, c);
     }
   }
 }
@@ -209,6 +256,7 @@ __device__ __forceinline__ void prefetch_unit_l2(const Params &p, int u) {
   decode_unit(p, u, nt, tt, sp, kb0, kb1);
   const size_t blk = static_cast<size_t>(nt) * p.KB + kb0;
   const uint32_t nkb = static_cast<uint32_t>(kb1 - kb0);
+  if (nkb == 0) return;
   bulk_prefetch_l2(p.w + blk * 8192, nkb * 8192u);
   bulk_prefetch_l2(p.sf + blk * kSfBytes, nkb * kSfBytes);
 }
@@ -348,6 +396,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
           left -= nslots;
           pf.u += gridDim.x;
         }
+        pf_load(p, pf);
         prefetch_blocks_l2(p, pf, kPfAhead);
       }
       {
@@ -454,6 +503,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
         int nt, tt, sp, kb0, kb1;
         decode_unit(p, u, nt, tt, sp, kb0, kb1);
         const int nkb = kb1 - kb0;
+        if (nkb <= 0) continue;   // empty stream-K unit
         const int nslots = (nkb + PAD - 1) / PAD * PAD;
         if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_ACC_EMPTY)) break;
         tc_fence_after();
@@ -539,6 +589,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
       int nt, tt, sp, kb0, kb1;
       decode_unit(p, u, nt, tt, sp, kb0, kb1);
+      if (kb1 <= kb0) continue;                   // empty stream-K unit
       const int ncontrib = min(ISS, kb1 - kb0);   // MMA warps that accumulated something
       // The decision to stop must be the same in all 128 epilogue threads
       // (they meet at named barriers below): a failed wait is published
@@ -554,10 +605,14 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
       const int t0 = tt * BT;
       const int tile = nt * p.t_tiles + tt;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      float *part = (p.splits > 1 && !p.cluster) ? p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (128 * BT) : nullptr;
+      // CTAs that share this tile's K range, and this unit's workspace slot
+      const int nseg = p.sk ? sk_segments(p, tile) : p.splits;
+      const size_t slot = p.sk ? static_cast<size_t>(u) : static_cast<size_t>(tile) * p.splits + sp;
+      const bool ws_split = nseg > 1 && !p.cluster;
+      float *part = ws_split ? p.partials + slot * (128 * BT) : nullptr;
       bool drained = false;
       if constexpr (ISS == 1 && CH == 32 && BT % 64 == 0) {
-        if (p.splits == 1 && p.tma_store) {
+        if (nseg == 1 && p.tma_store) {
           // Prefill tile on one accumulator (the MMA waits for it: a second
           // 256-column accumulator would not leave room for the scale
           // columns). Every cycle spent here is tensor-pipe idle time, so
@@ -680,7 +735,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce_bar[acc]);
         }
-        if (BT < 128 && p.splits == 1 && p.tma_store) {
+        if (BT < 128 && nseg == 1 && p.tma_store) {
           // Stage [CH tokens][128 n] bf16 in smem, then one TMA tensor store;
           // the store clips rows >= M and columns >= N. (Prefill tiles with a
           // TMA-storable C took the per-warp drain above: their tensor map
@@ -701,7 +756,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
             bulk_commit();
           }
           ++out_chunk;
-        } else if (p.splits == 1) {
+        } else if (nseg == 1) {
           if (n < p.N) {
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
@@ -808,20 +863,33 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
         }
       }
       if (stop) break;
-      if (p.splits > 1 && !p.cluster) {
+      if (ws_split) {
         __threadfence();
         named_bar_sync(1, 128);
         if (ew == 0 && lane == 0) {
           const int prev = atomicAdd(p.counters + tile, 1);
           // 1: last arrival, sum; 2: last arrival after a poisoned one, no sum
-          *is_last = ((prev & kArrivalMask) == p.splits - 1) ? ((prev >> kPoisonShift) ? 2 : 1) : 0;
+          *is_last = ((prev & kArrivalMask) == nseg - 1) ? ((prev >> kPoisonShift) ? 2 : 1) : 0;
         }
         named_bar_sync(1, 128);
         if (*is_last == 1) {
           __threadfence();
-          const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (128 * BT);
-          reduce_partials_store<BT>(base, p.splits, min(BT, p.M - t0), nt * 128, p.N, A4 ? nullptr : p.s, t0, p.c,
-                                    p.ldc, ew * 32 + lane, 128);
+          if (p.sk) {
+            // the tile's pieces in K order: CTAs c0 .. c0 + nseg - 1, each
+            // its piece j = tile - (first tile of the CTA)
+            const int c0 = sk_cta(p, tile * p.KB);
+            auto slot_ptr = [&](int s2) -> const float * {
+              const int c = c0 + s2;
+              const int j = tile - sk_begin(p, c) / p.KB;
+              return p.partials + (static_cast<size_t>(c) + static_cast<size_t>(j) * p.sk_grid) * (128 * BT);
+            };
+            reduce_slots_store(slot_ptr, nseg, min(BT, p.M - t0), nt * 128, p.N, A4 ? nullptr : p.s, t0, p.c,
+                               p.ldc, ew * 32 + lane, 128);
+          } else {
+            const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (128 * BT);
+            reduce_partials_store<BT>(base, p.splits, min(BT, p.M - t0), nt * 128, p.N, A4 ? nullptr : p.s, t0,
+                                      p.c, p.ldc, ew * 32 + lane, 128);
+          }
         }
         if (*is_last && ew == 0 && lane == 0) p.counters[tile] = 0;
         named_bar_sync(1, 128);
@@ -834,11 +902,16 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
     // An expired wait stopped this CTA: it still arrives, poisoned, at the
     // counter of every workspace split-K tile it owed (the one it stopped in
     // and all later ones), so that every counter ends the launch at zero.
-    if (abort_u >= 0 && p.splits > 1 && !p.cluster && leader) {
+    if (abort_u >= 0 && (p.splits > 1 || p.sk) && !p.cluster && leader) {
       for (int u2 = abort_u; u2 < p.units; u2 += gridDim.x) {
-        const int tile2 = u2 / p.splits;
+        int nt2, tt2, sp2, kb02, kb12;
+        decode_unit(p, u2, nt2, tt2, sp2, kb02, kb12);
+        if (kb12 <= kb02) continue;   // empty stream-K unit: owed nothing
+        const int tile2 = nt2 * p.t_tiles + tt2;
+        const int nseg2 = p.sk ? sk_segments(p, tile2) : p.splits;
+        if (nseg2 <= 1) continue;     // stored directly, no counter
         const int prev = atomicAdd(p.counters + tile2, 1 + kPoisonArrival);
-        if ((prev & kArrivalMask) == p.splits - 1) atomicExch(p.counters + tile2, 0);
+        if ((prev & kArrivalMask) == nseg2 - 1) atomicExch(p.counters + tile2, 0);
       }
     }
     if (lane == 0) bulk_wait_all();   // output stores complete before the CTA's smem goes away
@@ -920,6 +993,9 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *xsf, const uint8_
   p.t_tiles = pl.t_tiles;
   p.splits = pl.splits;
   p.kb_per_split = pl.kb_per_split;
+  p.sk = pl.sk;
+  p.sk_grid = pl.grid;
+  p.sk_total = pl.sk_total;
   p.units = pl.units;
   p.ldc = static_cast<int>(ldc);
   p.tma_store = use_tma_store;
@@ -1115,6 +1191,55 @@ static GemmPlan plan_mx_bt(int64_t M, int64_t N, int64_t K, int sms, bool a4, in
   if (pl.splits > 1 && !pl.cluster) {
     pl.counters_bytes = round_up(static_cast<size_t>(tiles) * 4, 256);
     pl.ws_bytes = pl.counters_bytes + static_cast<size_t>(pl.units) * 128 * bt * 4;
+  }
+  // Stream-K for decode tiles. A decode CTA streams its weights at ~35 GB/s
+  // whatever its share of HBM (latency-bound, measured on GB300), so what
+  // counts is the longest K range one CTA streams: a uniform split leaves
+  // SMs idle when tiles x splits is not a multiple of the SM count (5120 x
+  // 17408: 40 tiles x 3 splits on 120 of 152 SMs) or runs a second partial
+  // wave (34816 x 5120: 272 tiles, 80 K blocks on the busiest CTA against
+  // 72 on average). Stream-K gives every CTA the same number of K blocks of
+  // the tile-major sequence; a tile shared by several CTAs is summed through
+  // the workspace by its last arrival, in K order.
+  // Measured on GB300 (graph-timed, cold weights) it loses to the uniform
+  // schedule on every decode shape -- 6x34816x5120 22.2 vs 19.1 us,
+  // 6x5120x17408 15.9 vs 14.5 us, 64x5120x17408 26.9 vs 19.4 us: a shared
+  // tile's partial write, fence and counter, and the last arrival's sum at
+  // the end of its CTA's range, cost more than the balance gains. So it is
+  // off by default (option 16 = 0) and kept as a tested option.
+  const int sk_opt = options().stream_k;
+  if (bt <= 64 && sk_opt != 0 && !forced_s && tiles * pl.KB * std::min<int64_t>(sms, tiles * pl.KB) < (int64_t(1) << 31)) {
+    const int64_t T = tiles * pl.KB;   // (T x G < 2^31: the kernel's stream-K arithmetic is 32-bit)
+    const int G = static_cast<int>(std::min<int64_t>(sms, T));
+    auto sk_cta = [&](int64_t x) { return static_cast<int>(((x + 1) * G - 1) / T); };
+    int segs_cta = 1, segs_tile = 1;
+    for (int c = 0; c < G; ++c) {
+      const int64_t a = static_cast<int64_t>(c) * T / G, b = static_cast<int64_t>(c + 1) * T / G;
+      if (b > a) segs_cta = std::max(segs_cta, static_cast<int>((b - 1) / pl.KB - a / pl.KB + 1));
+    }
+    for (int64_t t = 0; t < tiles; ++t)
+      segs_tile = std::max(segs_tile, sk_cta(t * pl.KB + pl.KB - 1) - sk_cta(t * pl.KB) + 1);
+    const double cta_bw = 35e9, hbm_eff = 6.0e12;
+    auto rate = [&](int64_t active) { return std::min(cta_bw, hbm_eff / static_cast<double>(active)); };
+    // the uniform plan in the same terms: the busiest CTA's K blocks, plus its exchange or sum
+    const int64_t u_waves = pl.cluster ? ceil_div(tiles, std::max<int64_t>(1, pl.grid / pl.splits))
+                                       : ceil_div(static_cast<int64_t>(pl.units), pl.grid);
+    double t_u = u_waves * pl.kb_per_split * kb_bytes / rate(pl.grid);
+    if (pl.splits > 1) t_u += pl.cluster ? 1.5e-6 : pl.splits * part_bytes / red_bw;
+    double t_sk = static_cast<double>(ceil_div(T, G)) * kb_bytes / rate(G);
+    if (segs_tile > 1) t_sk += 1.0e-6 + segs_tile * part_bytes / red_bw;
+    if (sk_opt == 2 || t_sk < 0.95 * t_u) {
+      pl.sk = 1;
+      pl.sk_total = static_cast<int>(T);
+      pl.splits = 1;
+      pl.kb_per_split = pl.KB;
+      pl.cluster = 0;
+      pl.grid = G;
+      pl.units = G * segs_cta;
+      pl.counters_bytes = segs_tile > 1 ? round_up(static_cast<size_t>(tiles) * 4, 256) : 0;
+      pl.ws_bytes = segs_tile > 1 ? pl.counters_bytes + static_cast<size_t>(pl.units) * 128 * bt * 4 : 0;
+      best_t = t_sk;
+    }
   }
   if (t_model) *t_model = best_t;
   return pl;

@@ -512,11 +512,71 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
   return *reinterpret_cast<uint16_t *>(&h);
 }
 
-// Split-K epilogue of the last-arriving CTA: sum `splits` fp32 partial tiles
-// (each [BT tokens][128 n], n contiguous) in split order -- deterministic --
-// and store bf16(scale[t] * sum) (scale == nullptr: 1) into C[t0 + t][n0 + n]
-// for t < tmax, n0 + n < N. The loads are independent L2 reads (.cg: the
-// partials were written by other SMs), four n per thread.
+// Split-K epilogue of the last-arriving CTA: sum `nslots` fp32 partial tiles
+// (each [tokens][128 n], n contiguous; slot(s) is the s-th) in s order --
+// deterministic -- and store bf16(scale[t] * sum) (scale == nullptr: 1) into
+// C[t0 + t][n0 + n] for t < tmax, n0 + n < N. The loads are independent L2
+// reads (.cg: the partials were written by other SMs), four n per thread.
+template <class SlotFn>
+__device__ __forceinline__ void reduce_slots_store(SlotFn slot, int nslots, int tmax, int n0, int N,
+                                                   const float *scale, int t0, uint16_t *c, int ldc, int tid,
+                                                   int nthreads) {
+  // Each pass covers four float4 groups per thread and keeps up to 16 loads
+  // in flight (four slots at a time), so the pass costs about one L2 round
+  // trip per four slots instead of one per slot and group.
+  constexpr int U = 4, S = 4;
+  const int total = tmax * 32;
+  for (int base = tid; base < total; base += nthreads * U) {
+    float4 acc[U];
+    const float *s0 = slot(0);
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int idx = base + k * nthreads;
+      acc[k] = idx < total ? __ldcg(reinterpret_cast<const float4 *>(s0 + (idx >> 5) * 128 + (idx & 31) * 4))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int s2 = 1; s2 < nslots; s2 += S) {
+      float4 v[S][U];
+#pragma unroll
+      for (int ss = 0; ss < S; ++ss) {
+        const float *sp = s2 + ss < nslots ? slot(s2 + ss) : nullptr;
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          const int idx = base + k * nthreads;
+          v[ss][k] = (sp != nullptr && idx < total)
+                         ? __ldcg(reinterpret_cast<const float4 *>(sp + (idx >> 5) * 128 + (idx & 31) * 4))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int ss = 0; ss < S; ++ss)   // in slot order (deterministic)
+        if (s2 + ss < nslots) {
+#pragma unroll
+          for (int k = 0; k < U; ++k) {
+            acc[k].x += v[ss][k].x;
+            acc[k].y += v[ss][k].y;
+            acc[k].z += v[ss][k].z;
+            acc[k].w += v[ss][k].w;
+          }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int idx = base + k * nthreads;
+      if (idx >= total) continue;
+      const int tl = idx >> 5, n4 = (idx & 31) * 4;
+      const float sc = scale ? __ldg(scale + t0 + tl) : 1.f;
+      const int n = n0 + n4;
+      uint16_t *dst = c + static_cast<size_t>(t0 + tl) * ldc + n;
+      const float vals[4] = {acc[k].x * sc, acc[k].y * sc, acc[k].z * sc, acc[k].w * sc};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (n + j < N) dst[j] = f32_to_bf16_rn(vals[j]);
+    }
+  }
+}
+
+// The same for `splits` partial tiles [BT][128] stored one after another.
 template <int BT>
 __device__ __forceinline__ void reduce_partials_store(const float *base, int splits, int tmax, int n0, int N,
                                                       const float *scale, int t0, uint16_t *c, int ldc, int tid,

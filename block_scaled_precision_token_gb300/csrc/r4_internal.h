@@ -41,6 +41,7 @@ struct Options {
   int row_split = 0;        // row-wise quantizers: CTAs per row (0 = automatic, else 1/2/4/8)
   int row_threads = 0;      // row-wise quantizers: threads per CTA at most (0 = automatic, else 64/128/256)
   int skinny_groups = 0;    // skinny GEMM: 16-token groups per CTA (0 = automatic, else 1..4)
+  int stream_k = 0;         // W4A8/W4A4 decode tiles: stream-K schedule 0 never (default), 1 when the model gains, 2 always
 };
 Options &options();
 
@@ -101,6 +102,8 @@ struct GemmPlan {
   int splits = 1, kb_per_split = 0;
   int units = 0, grid = 0;
   int cluster = 0;       // 1: split-K across a cluster of `splits` CTAs (partials in DSMEM, no workspace)
+  int sk = 0;            // 1: stream-K (grid CTAs share the tile-major K blocks equally; units = grid x sk_segs)
+  int sk_total = 0;      // stream-K: tiles x KB
   size_t counters_bytes = 0;  // arrival counters (one int per tile), 256-B rounded
   size_t ws_bytes = 0;        // total workspace (0 when splits == 1)
 };

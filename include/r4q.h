@@ -391,7 +391,16 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * rule at the top of this header;
  * key 15: skinny bf16 GEMM, 16-token groups per CTA: 0 (default) chooses,
  * 1..4 force it (the tokens are split over that many more CTAs); other
- * values return R4_ERR_INVALID_ARG.
+ * values return R4_ERR_INVALID_ARG;
+ * key 16: stream-K schedule of the W4A8/W4A4 decode tiles (M <= 64): every
+ * CTA streams an equal share of all tiles' K blocks, and a tile shared by
+ * several CTAs is summed through the workspace by its last arrival, in K
+ * order: 0 (default) never, 1 when the schedule model expects a gain, 2
+ * always (unless key 1 forces a split factor); other values return
+ * R4_ERR_INVALID_ARG. It changes r4_gemm_workspace_bytes: query it after
+ * setting the option. (Measured on GB300 it is slower than the default
+ * schedule on the decode shapes; it is an option for other shapes and
+ * GPUs.)
  */
 int r4_set_option(int key, int64_t value);
 

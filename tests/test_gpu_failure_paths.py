@@ -84,18 +84,22 @@ def _blockfp8_inputs(r4q, M, N, K):
     return torch.from_numpy(q).cuda(), torch.from_numpy(As).cuda(), pk, (q, As, wq, Ws)
 
 
-@pytest.mark.parametrize("op", ["w4a8", "blockfp8"])
+@pytest.mark.parametrize("op", ["w4a8", "w4a8_stream_k", "blockfp8"])
 def test_expired_wait_leaves_the_workspace_reusable(r4q, op):
     """Split-K through the caller's workspace (forced: 4 splits, no cluster
-    exchange). The first CTA's stalled unit never writes its partial; the
-    launch must still end with every arrival counter at zero, and the next
-    call on the same workspace must match the oracle."""
+    exchange; or the stream-K schedule, where every tile is shared by eight
+    CTAs of one K block each). The first CTA's stalled unit never writes its
+    partial; the launch must still end with every arrival counter at zero,
+    and the next call on the same workspace must match the oracle."""
     M, N, K = 8, 512, 1024
     tiles = (N // 128) * 1                       # 16-token tiles: one token tile
-    if op == "w4a8":
+    if op.startswith("w4a8"):
         q, s, pk, ref = _w4a8_inputs(r4q, M, N, K)
-        r4q.r4_set_option(1, 4)
-        r4q.r4_set_option(6, 0)
+        if op == "w4a8":
+            r4q.r4_set_option(1, 4)
+            r4q.r4_set_option(6, 0)
+        else:
+            r4q.r4_set_option(16, 2)
         opid = r4q.R4_OP_W4A8_MXFP4
         call = lambda ws: r4q.gemm_w4a8(q, s, pk, N, K, ws=ws)
         exact = lambda: G.gemm_w4a8(*ref)[0]
@@ -126,6 +130,7 @@ def test_expired_wait_leaves_the_workspace_reusable(r4q, op):
         r4q.r4_set_option(1, 0)
         r4q.r4_set_option(3, 0)
         r4q.r4_set_option(6, 1)
+        r4q.r4_set_option(16, 0)
     assert_gemm_matches(c, exact(), f"{op} after the stalled launch, reused workspace")
 
 

@@ -20,6 +20,7 @@ def r4q():
     m.r4_set_option(1, 0)
     m.r4_set_option(2, 0)
     m.r4_set_option(6, 1)
+    m.r4_set_option(16, 0)
 
 
 def _run(r4q, q_np, s_np, packed_np, scale_np, N, K, ldc=None):
@@ -154,6 +155,39 @@ def test_prefill_tiles_many_units(r4q, bt, M, N):
     assert_gemm_matches(c[:, torch.from_numpy(rows).cuda()], c64, f"bt={bt} M={M} N={N}")
     assert torch.equal(c, c2), "not deterministic across calls"
     assert np.all(full.float().cpu().numpy()[:, N:] == 7.0), "kernel wrote outside columns [0, N)"
+
+
+@pytest.mark.parametrize("M,N,K", [(6, 640, 2048), (16, 2000, 1152), (33, 1280, 4096), (64, 384, 5120),
+                                   (1, 8192, 640), (40, 300, 416)])
+def test_stream_k(r4q, M, N, K):
+    """Stream-K forced (option 16 = 2): the SMs share the tile-major K blocks
+    equally, so CTAs cover pieces of several tiles and tiles are shared by
+    several CTAs (summed through the workspace in K order) or owned by one
+    (stored directly). Ragged N with a guard band, tiles of one K block,
+    deterministic across calls."""
+    q, s, p, sc = _dense_inputs(M, N, K, synth.CFG_DECODE)
+    ldc = N + 24
+    r4q.r4_set_option(16, 2)
+    try:
+        ws_bytes = r4q.r4_gemm_workspace_bytes(r4q.R4_OP_W4A8_MXFP4, M, N, K)
+        c, full = _run(r4q, q, s, p, sc, N, K, ldc=ldc)
+        c2, _ = _run(r4q, q, s, p, sc, N, K)
+    finally:
+        r4q.r4_set_option(16, 0)
+    c64, _ = G.gemm_w4a8(q, s, p, sc)
+    assert_gemm_matches(c, c64, f"stream-K M={M} N={N} K={K} (workspace {ws_bytes} B)")
+    assert torch.equal(c, c2), "not deterministic across calls"
+    assert np.all(full.float().cpu().numpy()[:, N:] == 7.0), "kernel wrote outside columns [0, N)"
+
+
+@pytest.mark.parametrize("M", [6, 64])
+@pytest.mark.parametrize("N,K", synth.DECODE_NK)
+def test_stream_k_full_size_sampled(r4q, M, N, K):
+    r4q.r4_set_option(16, 2)
+    try:
+        _sampled_full_size(r4q, M, N, K, seed=300 + M)
+    finally:
+        r4q.r4_set_option(16, 0)
 
 
 def _sampled_full_size(r4q, M, N, K, seed, nsample=384):
