@@ -582,26 +582,8 @@ __device__ __forceinline__ void reduce_partials_store(const float *base, int spl
                                                       const float *scale, int t0, uint16_t *c, int ldc, int tid,
                                                       int nthreads) {
   constexpr size_t kTile = 128 * BT;
-  for (int idx = tid; idx < tmax * 32; idx += nthreads) {
-    const int tl = idx >> 5, n4 = (idx & 31) * 4;
-    const float *src = base + tl * 128 + n4;
-    float4 acc = __ldcg(reinterpret_cast<const float4 *>(src));
-#pragma unroll 4
-    for (int s2 = 1; s2 < splits; ++s2) {
-      const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + s2 * kTile));
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    const float sc = scale ? __ldg(scale + t0 + tl) : 1.f;
-    const int n = n0 + n4;
-    uint16_t *dst = c + static_cast<size_t>(t0 + tl) * ldc + n;
-    const float vals[4] = {acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc};
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (n + j < N) dst[j] = f32_to_bf16_rn(vals[j]);
-  }
+  reduce_slots_store([&](int s2) { return base + s2 * kTile; }, splits, tmax, n0, N, scale, t0, c, ldc, tid,
+                     nthreads);
 }
 
 }  // namespace r4
