@@ -65,8 +65,9 @@ struct Params {
 template <int BT>
 struct Cfg {
   static constexpr int kProd = BT <= 64 ? 2 : 1;           // TMA producer warps
-  static constexpr int kMmaWarp = kProd;
-  static constexpr int kEpiWarp0 = kProd + 1;
+  static constexpr int kMmaWarp = kProd;                   // first MMA-issuing warp
+  static constexpr int kMma = 2;                           // MMA-issuing warps (slot g: warp g % kMma)
+  static constexpr int kEpiWarp0 = kProd + kMma;
   static constexpr int kCW = BT < 32 ? BT : 32;            // token columns per epilogue warp
   static constexpr int kH = BT / kCW;                      // column groups
   static constexpr int kEpiWarps = 4 * kH;
@@ -174,7 +175,7 @@ __device__ __forceinline__ void copy_scale_chunk(const Params &p, const ChunkCur
 }
 
 template <int BT>
-__global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kThreads > 576 ? 96 : 128)
     blockfp8_f8f6f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                            const Params p) {
   using C = Cfg<BT>;
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
   uint64_t *accf_bar = empty_bar + kMaxStages;               // [kMaxBuf]
   uint64_t *acce_bar = accf_bar + kMaxBuf;                   // [kMaxBuf]
   uint64_t *drain_bar = acce_bar + kMaxBuf;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain_bar + 1);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain_bar + C::kMma);   // drain_bar: one per MMA warp
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *is_last = abort_flag + 1;
 
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
       mbar_init(&accf_bar[b], 1);
       mbar_init(&acce_bar[b], C::kEpiWarps);
     }
-    mbar_init(drain_bar, 1);
+    for (int m = 0; m < C::kMma; ++m) mbar_init(&drain_bar[m], 1);
     *abort_flag = 0;
     *is_last = 0;
     fence_mbar_init();
@@ -274,13 +275,20 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
         }
     }
     __syncwarp();
-  } else if (warp == C::kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp < C::kMmaWarp + C::kMma) {
+    // ------------------------------------------------------------ MMA issuers
+    // Every slot writes a fresh accumulator buffer, so the slots can be
+    // issued by two threads independently (slot g by warp g % kMma): one
+    // thread's barrier waits and commits overlap the other's MMAs in the
+    // tensor pipe. (With one issuer, four N = 128 MMAs of ~80 cycles each
+    // left the pipe idle during ~400-700 cycles of per-slot handshake.)
+    const int mw = warp - C::kMmaWarp;
     if (lane == 0) {
       const uint32_t idesc = idesc_f8f6f4_e4m3(BT);
       SlotCursor cu;
       cu.start(p);
       for (int g = 0; cu.valid(p); ++g, cu.next(p)) {
+        if (g % C::kMma != mw) continue;
         const int stage = g % C::kStages;
         const uint32_t phase = static_cast<uint32_t>(g / C::kStages) & 1u;
         const int buf = g % C::kNumBuf;
@@ -299,9 +307,9 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1)
         tc_commit(&accf_bar[buf]);
       }
       // All MMAs this thread issued must be complete before tensor memory is freed.
-      tc_commit(drain_bar);
+      tc_commit(&drain_bar[mw]);
       volatile int dummy = 0;
-      mbar_wait(drain_bar, 0, &dummy, p.err, DEV_ERR_WAIT_DRAIN);
+      mbar_wait(&drain_bar[mw], 0, &dummy, p.err, DEV_ERR_WAIT_DRAIN);
     }
     __syncwarp();
   } else {
