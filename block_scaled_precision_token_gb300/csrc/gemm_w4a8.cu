@@ -61,6 +61,7 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *s
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 constexpr int kBK = 128;
@@ -138,8 +139,16 @@ struct Cfg {
   static constexpr uint32_t kAccCols = static_cast<uint32_t>(kIss * kNumAcc * BT);
   static constexpr uint32_t kSfaCol = kAccCols <= 256 ? 256u : 384u;
   static constexpr uint32_t kSfbCol = kSfaCol + 64u;
-  static constexpr int kThreads = 32 * (kProd + kIss + 4);    // producers, MMA issuers, 4 epilogue
+  // 256-token tiles (one accumulator) drain it into registers with 8
+  // epilogue warps, two per tensor-memory lane quarter, 128 columns each
+  // (see the epilogue); other tiles use 4.
+  static constexpr bool kRegDrain = BT == 256;
+  static constexpr int kEpiWarps = kRegDrain ? 8 : 4;
+  static constexpr int kThreads = 32 * (kProd + kIss + kEpiWarps);   // producers, MMA issuers, epilogue
   static constexpr int kEpiWarp0 = kProd + kIss;
+  // Registers per thread: with more than 8 warps three share one SMSP, whose
+  // 16K registers then allow 170 each.
+  static constexpr int kMaxReg = kThreads > 256 ? 168 : 255;
   static constexpr uint32_t kWBytes = A4 ? 8192u : kWSmem;      // weight tile in shared memory
   static constexpr uint32_t kXSmem = A4 ? BT * 64 : BT * 128;   // activation tile
   static constexpr int kXAtoms = A4 ? (BT > 128 ? 2 : 1) : 0;   // activation scale atoms per stage
@@ -281,8 +290,69 @@ __host__ __device__ constexpr uint32_t idesc_mxf4_e2m1(int n, int a_sf_id, int b
          (1u << 23) | (static_cast<uint32_t>(128 >> 4) << 24) | (static_cast<uint32_t>(a_sf_id & 3) << 29);
 }
 
+// Register drain of one warp's half of a 256-token accumulator (one
+// tensor-memory lane quarter q, 128 token columns from abase): all four
+// 32-token chunks leave tensor memory in the 16x256b shape at once (128
+// registers), the accumulator is released (one arrival on `acce`), and only
+// then are the chunks scaled, rounded, written by stmatrix.trans into the
+// warp's own 2 KB region ([32 token][32 n], 64-byte rows, 64-byte swizzle)
+// and stored with one TMA store each -- while the next unit's MMAs already
+// run. t0 is the first token of the half; tokens >= M get scale 0 and the
+// TMA store clips them.
+template <bool A4>
+__device__ __forceinline__ void drain_half_to_regs(const Params &p, const CUtensorMap *tm_c, uint32_t abase,
+                                                   uint16_t *region, int t0, int nt, int q, int lane,
+                                                   uint64_t *acce) {
+  uint32_t r[4][32];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    tc_ld_16x256b_x4(abase + static_cast<uint32_t>(32 * c), r[c]);
+    tc_ld_16x256b_x4(abase + (16u << 16) + static_cast<uint32_t>(32 * c), r[c] + 16);
+  }
+  tc_wait_ld();
+  tc_fence_before();   // every chunk is in registers: the accumulator is free
+  __syncwarp();
+  if (lane == 0) mbar_arrive(acce);
+  const int tq = 2 * (lane & 3);
+  const int mrow = lane & 7, mmat = lane >> 3;
+  const uint32_t sbase = smem_u32(region) + static_cast<uint32_t>(mrow * 64 + ((mmat ^ ((mrow >> 1) & 3)) << 4));
+  const bool q_store = nt * 128 + q * 32 < p.N;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float sc[8];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int t = t0 + 32 * c + 8 * g + tq;
+      if constexpr (A4) {
+        sc[2 * g] = sc[2 * g + 1] = 1.f;
+      } else {
+        sc[2 * g] = (t < p.M) ? __ldg(p.s + t) : 0.f;
+        sc[2 * g + 1] = (t + 1 < p.M) ? __ldg(p.s + t + 1) : 0.f;
+      }
+    }
+    if (lane == 0) bulk_wait_read0();   // the previous chunk's store has read the region
+    __syncwarp();
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t w[4];   // matrix m: n = 8m + lane/4 of the quarter, tokens 8g + tq, +1
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int b = 16 * (m >> 1) + 4 * g + 2 * (m & 1);
+        w[m] = pack_bf16x2(__uint_as_float(r[c][b]) * sc[2 * g], __uint_as_float(r[c][b + 1]) * sc[2 * g + 1]);
+      }
+      stmatrix_x4_trans(sbase + static_cast<uint32_t>(g * 8 * 64), w[0], w[1], w[2], w[3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (q_store) tma_store_2d(tm_c, region, nt * 128 + q * 32, t0 + 32 * c);
+      bulk_commit();
+    }
+  }
+}
+
 template <int BT, bool A4>
-__global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT, A4>::kMaxReg))
     w4a8_mxf8f6f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                          const __grid_constant__ CUtensorMap tm_c, const Params p) {
   using C = Cfg<BT, A4>;
@@ -326,7 +396,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&accf_bar[a], ISS);   // one arrival per MMA warp per unit
-      mbar_init(&acce_bar[a], 4);     // one per epilogue warp
+      mbar_init(&acce_bar[a], C::kEpiWarps);   // one per epilogue warp
     }
     for (int w = 0; w < 4; ++w) mbar_init(&drain_bar[w], 1);
     mbar_init(red_full, p.splits);    // one arrival per CTA of the cluster
@@ -573,6 +643,42 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
       mbar_wait(&drain_bar[mw], 0, &dummy, p.err, DEV_ERR_WAIT_DRAIN);
     }
     __syncwarp();
+  } else if (C::kRegDrain && warp >= C::kEpiWarp0 + 4) {
+    // ------------------------------------------------------------ epilogue helpers (256-token tiles)
+    // Columns 128-255 of the accumulator, lane quarter q: drained into
+    // registers with the first four epilogue warps' halves, when the tile
+    // is stored directly through TMA. On every other path (split-K, a C
+    // that TMA cannot store) the first four warps read the whole tile, and
+    // a helper only adds its arrival to the accumulator's release (the
+    // release counts all eight warps, so it cannot complete before those
+    // four have read it).
+    pdl_wait();
+    const int q = warp & 3;
+    const int ew = warp - C::kEpiWarp0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      int nt, tt, sp, kb0, kb1;
+      decode_unit(p, u, nt, tt, sp, kb0, kb1);
+      if (kb1 <= kb0) continue;   // empty stream-K unit
+      const int tile = nt * p.t_tiles + tt;
+      const int nseg = p.sk ? sk_segments(p, tile) : p.splits;
+      if (!warp_wait(&accf_bar[acc], acc_phase, abort_flag, p.err, DEV_ERR_WAIT_ACC_FULL)) break;
+      tc_fence_after();
+      if (nseg == 1 && p.tma_store) {
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        drain_half_to_regs<A4>(p, &tm_c, lane_base + static_cast<uint32_t>(acc * BT + 128), staging + ew * 1024,
+                               tt * BT + 128, nt, q, lane, &acce_bar[acc]);
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce_bar[acc]);
+      }
+      if (++acc == C::kNumAcc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_all();   // output stores complete before the CTA's smem goes away
   } else {
     // ------------------------------------------------------------ epilogue (4 warps)
     pdl_wait();                     // s, C and the workspace belong to the kernel stream order
@@ -641,75 +747,82 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1)
           // split-K prefill of the same kernel lost 12 %); draining every
           // chunk into registers first (255 registers, spills); plain
           // coalesced global stores (M=2048, 34816x5120: 260 -> 345 us).
-          uint32_t ra[32], rb[32];   // [0,16): lanes 0-15 of the quarter; [16,32): lanes 16-31
-          const uint32_t abase = lane_base + static_cast<uint32_t>(acc * BT);
-          auto load_chunk = [&](uint32_t (&r)[32], int c0) {
-            tc_ld_16x256b_x4(abase + static_cast<uint32_t>(c0), r);
-            tc_ld_16x256b_x4(abase + (16u << 16) + static_cast<uint32_t>(c0), r + 16);
-          };
-          const int tq = 2 * (lane & 3);                 // first of this thread's token pair in an 8-token group
-          const int mrow = lane & 7, mmat = lane >> 3;   // stmatrix row (token) and matrix (8-n group) addressed
-          const uint32_t st_off =
-              static_cast<uint32_t>(q * 2048 + mrow * 64 + ((mmat ^ ((mrow >> 1) & 3)) << 4));
-          const bool q_store = nt * 128 + q * 32 < p.N;  // this warp's 32 n hold at least one column
-          float sc_cur[8], sc_nxt[8];                    // per-token scales of the token pairs, 4 groups
-          auto load_scales = [&](float (&sc)[8], int c0) {
-            if constexpr (!A4) {
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                const int t = t0 + c0 + 8 * g + tq;
-                sc[2 * g] = (t < p.M) ? __ldg(p.s + t) : 0.f;
-                sc[2 * g + 1] = (t + 1 < p.M) ? __ldg(p.s + t + 1) : 0.f;
-              }
-            }
-          };
-          auto stage_and_store = [&](const uint32_t (&r)[32], int c0) {
-            if (c0 + 32 < BT) load_scales(sc_nxt, c0 + 32);
-            uint16_t *stg = staging + (out_chunk & 1u) * (CH * 128);
-            const uint32_t sbase = smem_u32(stg) + st_off;
-            if (lane == 0) bulk_wait_read1();   // this warp's store from two chunks ago has read its region
-            __syncwarp();
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              uint32_t w[4];   // matrix m: n = 8m + lane/4 of the quarter, tokens 8g + tq, +1
-#pragma unroll
-              for (int m = 0; m < 4; ++m) {
-                const int b = 16 * (m >> 1) + 4 * g + 2 * (m & 1);
-                float v0 = __uint_as_float(r[b]), v1 = __uint_as_float(r[b + 1]);
-                if constexpr (!A4) {
-                  v0 *= sc_cur[2 * g];
-                  v1 *= sc_cur[2 * g + 1];
+          if constexpr (C::kRegDrain) {
+            // 256-token tile: this warp drains columns 0-127 of its quarter,
+            // the matching helper warp (ew + 4) columns 128-255.
+            drain_half_to_regs<A4>(p, &tm_c, lane_base + static_cast<uint32_t>(acc * BT), staging + ew * 1024, t0,
+                                   nt, q, lane, &acce_bar[acc]);
+          } else {
+            uint32_t ra[32], rb[32];   // [0,16): lanes 0-15 of the quarter; [16,32): lanes 16-31
+            const uint32_t abase = lane_base + static_cast<uint32_t>(acc * BT);
+            auto load_chunk = [&](uint32_t (&r)[32], int c0) {
+              tc_ld_16x256b_x4(abase + static_cast<uint32_t>(c0), r);
+              tc_ld_16x256b_x4(abase + (16u << 16) + static_cast<uint32_t>(c0), r + 16);
+            };
+            const int tq = 2 * (lane & 3);                 // first of this thread's token pair in an 8-token group
+            const int mrow = lane & 7, mmat = lane >> 3;   // stmatrix row (token) and matrix (8-n group) addressed
+            const uint32_t st_off =
+                static_cast<uint32_t>(q * 2048 + mrow * 64 + ((mmat ^ ((mrow >> 1) & 3)) << 4));
+            const bool q_store = nt * 128 + q * 32 < p.N;  // this warp's 32 n hold at least one column
+            float sc_cur[8], sc_nxt[8];                    // per-token scales of the token pairs, 4 groups
+            auto load_scales = [&](float (&sc)[8], int c0) {
+              if constexpr (!A4) {
+  #pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                  const int t = t0 + c0 + 8 * g + tq;
+                  sc[2 * g] = (t < p.M) ? __ldg(p.s + t) : 0.f;
+                  sc[2 * g + 1] = (t + 1 < p.M) ? __ldg(p.s + t + 1) : 0.f;
                 }
-                w[m] = pack_bf16x2(v0, v1);
               }
-              stmatrix_x4_trans(sbase + static_cast<uint32_t>(g * 8 * 64), w[0], w[1], w[2], w[3]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              if (q_store) tma_store_2d(&tm_c, stg + q * 1024, nt * 128 + q * 32, t0 + c0);
-              bulk_commit();   // (an empty group when nothing was stored keeps the count per chunk)
-            }
-            ++out_chunk;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) sc_cur[i] = sc_nxt[i];
-          };
-          load_scales(sc_cur, 0);
-          load_chunk(ra, 0);
-#pragma unroll 1
-          for (int c0 = 0; c0 < BT; c0 += 64) {
-            tc_wait_ld();              // chunk c0 in ra
-            load_chunk(rb, c0 + 32);   // chunk c0 + 32 in flight
-            stage_and_store(ra, c0);
-            tc_wait_ld();              // chunk c0 + 32 in rb
-            if (c0 + 64 < BT) {
-              load_chunk(ra, c0 + 64);
-            } else {
-              tc_fence_before();   // every chunk is in registers: the accumulator is free
+            };
+            auto stage_and_store = [&](const uint32_t (&r)[32], int c0) {
+              if (c0 + 32 < BT) load_scales(sc_nxt, c0 + 32);
+              uint16_t *stg = staging + (out_chunk & 1u) * (CH * 128);
+              const uint32_t sbase = smem_u32(stg) + st_off;
+              if (lane == 0) bulk_wait_read1();   // this warp's store from two chunks ago has read its region
               __syncwarp();
-              if (lane == 0) mbar_arrive(&acce_bar[acc]);
+  #pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                uint32_t w[4];   // matrix m: n = 8m + lane/4 of the quarter, tokens 8g + tq, +1
+  #pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                  const int b = 16 * (m >> 1) + 4 * g + 2 * (m & 1);
+                  float v0 = __uint_as_float(r[b]), v1 = __uint_as_float(r[b + 1]);
+                  if constexpr (!A4) {
+                    v0 *= sc_cur[2 * g];
+                    v1 *= sc_cur[2 * g + 1];
+                  }
+                  w[m] = pack_bf16x2(v0, v1);
+                }
+                stmatrix_x4_trans(sbase + static_cast<uint32_t>(g * 8 * 64), w[0], w[1], w[2], w[3]);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                if (q_store) tma_store_2d(&tm_c, stg + q * 1024, nt * 128 + q * 32, t0 + c0);
+                bulk_commit();   // (an empty group when nothing was stored keeps the count per chunk)
+              }
+              ++out_chunk;
+  #pragma unroll
+              for (int i = 0; i < 8; ++i) sc_cur[i] = sc_nxt[i];
+            };
+            load_scales(sc_cur, 0);
+            load_chunk(ra, 0);
+  #pragma unroll 1
+            for (int c0 = 0; c0 < BT; c0 += 64) {
+              tc_wait_ld();              // chunk c0 in ra
+              load_chunk(rb, c0 + 32);   // chunk c0 + 32 in flight
+              stage_and_store(ra, c0);
+              tc_wait_ld();              // chunk c0 + 32 in rb
+              if (c0 + 64 < BT) {
+                load_chunk(ra, c0 + 64);
+              } else {
+                tc_fence_before();   // every chunk is in registers: the accumulator is free
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acce_bar[acc]);
+              }
+              stage_and_store(rb, c0 + 32);
             }
-            stage_and_store(rb, c0 + 32);
           }
           drained = true;
         }
