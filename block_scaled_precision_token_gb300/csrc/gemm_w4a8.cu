@@ -829,19 +829,34 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
       }
 #pragma unroll 1
       for (int c0 = 0; c0 < (drained ? 0 : BT); c0 += CH) {
-        uint32_t r[32];
+        uint32_t r[32], r2[32];
         float v[32];
-#pragma unroll 1
-        for (int w = 0; w < ncontrib; ++w) {
+        // The MMA warps' accumulators are summed in warp order; the load of
+        // accumulator w + 1 is in flight while accumulator w is added.
+        auto ld_acc = [&](int w, uint32_t (&dst)[32]) {
           const uint32_t taddr = lane_base + static_cast<uint32_t>((w * C::kNumAcc + acc) * BT + c0);
           if constexpr (CH == 32) {
-            tc_ld_32x32b_x32(taddr, r);
+            tc_ld_32x32b_x32(taddr, dst);
           } else {
-            tc_ld_32x32b_x16(taddr, r);
+            tc_ld_32x32b_x16(taddr, dst);
           }
-          tc_wait_ld();
+        };
+        ld_acc(0, r);
+        tc_wait_ld();
 #pragma unroll
-          for (int j = 0; j < CH; ++j) v[j] = (w == 0) ? __uint_as_float(r[j]) : v[j] + __uint_as_float(r[j]);
+        for (int j = 0; j < CH; ++j) v[j] = __uint_as_float(r[j]);
+#pragma unroll 1
+        for (int w = 1; w < ncontrib; w += 2) {
+          ld_acc(w, r2);
+          tc_wait_ld();
+          if (w + 1 < ncontrib) ld_acc(w + 1, r);
+#pragma unroll
+          for (int j = 0; j < CH; ++j) v[j] += __uint_as_float(r2[j]);
+          if (w + 1 < ncontrib) {
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < CH; ++j) v[j] += __uint_as_float(r[j]);
+          }
         }
         if (c0 + CH >= BT) {
           tc_fence_before();
