@@ -190,6 +190,27 @@ def test_stream_k_full_size_sampled(r4q, M, N, K):
         r4q.r4_set_option(16, 0)
 
 
+@pytest.mark.parametrize("bt", [128, 192, 256])
+def test_prefill_tiles_unaligned_rows(r4q, bt):
+    """C rows not 16-byte aligned (ldc = N + 1): no TMA store, so the first
+    four epilogue warps read and store the whole tile and, at 256 tokens,
+    the four helper warps only add their arrival to the accumulator's
+    release. More units than CTAs, a ragged last token tile."""
+    M, N, K = 1100, 5200, 512
+    q, s, p, sc = _dense_inputs(M, N, K, synth.CFG_PREFILL)
+    r4q.r4_set_option(2, bt)
+    r4q.r4_set_option(1, 1)
+    try:
+        c, full = _run(r4q, q, s, p, sc, N, K, ldc=N + 1)
+    finally:
+        r4q.r4_set_option(1, 0)
+        r4q.r4_set_option(2, 0)
+    rows = np.unique(np.concatenate([synth.sample_indices(N, 256, M + 1).numpy(), [0, 127, 128, N - 1]]))
+    c64, _ = G.gemm_w4a8(q, s, p, sc, rows=rows)
+    assert_gemm_matches(c[:, torch.from_numpy(rows).cuda()], c64, f"bt={bt} unaligned rows")
+    assert np.all(full.float().cpu().numpy()[:, N:] == 7.0), "kernel wrote outside columns [0, N)"
+
+
 def _sampled_full_size(r4q, M, N, K, seed, nsample=384):
     q = random_e4m3_codes((M, K), seed=seed)
     s = (np.random.default_rng(seed).uniform(1e-3, 5e-2, M)).astype(np.float32)
