@@ -239,9 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int NG2, int NB>
 cudaError_t launch_ng(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N, int64_t K, uint16_t *c,
-                      int64_t ldc, int slices, cudaStream_t st) {
+                      int64_t ldc, int slices, int ks, cudaStream_t st) {
   const int chunks = static_cast<int>(K / 256);
-  const int ks = chunks < kMaxKS ? chunks : kMaxKS;
   const int cpc = (chunks + ks - 1) / ks;
   auto kern = skinny_bf16_kernel<NG2, NB>;
   constexpr size_t kSmemBytes = Smem<NG2, NB>::kBytes;
@@ -277,18 +276,28 @@ cudaError_t launch_gemm_skinny(const uint16_t *x, const uint16_t *w, int64_t M, 
   // 64 tokens, where the larger footprint spreads the CTAs over more SMs
   // (measured, [256, 2048], one chunk per CTA: M <= 16 3.0 vs 3.2 us and
   // M = 32 4.3 vs 4.6 us with one buffer; M = 64 5.9 vs 6.6 us with two).
-  // Token groups of 16 per CTA: above 32 tokens one group per CTA, the tokens
-  // split over more CTAs (measured on GB300, graph-timed, M = 64: [256,2048]
-  // 6.05 -> 5.45 us, [96,5120] 6.38 -> 5.53 us; at M = 32 neither way wins
-  // clearly: 4.51 / 4.58 and 4.73 / 4.19 us); option 15 forces a count.
+  // Token groups of 16 per CTA: from 32 tokens on one group per CTA, the
+  // tokens split over more CTAs (measured on GB300, graph-timed, M = 64:
+  // [256,2048] 6.05 -> 5.45 us, [96,5120] 6.38 -> 5.53 us; M = 32 with the
+  // split of 8: 4.17 -> 4.00 and 4.50 -> 4.06 us); option 15 forces a count.
   const int64_t groups = ceil_div(M, 16);
-  int64_t ng2 = groups > 2 ? 1 : groups;
+  int64_t ng2 = groups >= 2 ? 1 : groups;
   if (options().skinny_groups > 0) ng2 = std::min<int64_t>(groups, options().skinny_groups);
   const int slices = static_cast<int>(ceil_div(groups, ng2));
-  const bool multi = ceil_div(K / 256, static_cast<int64_t>(skinny::kMaxKS)) > 1 || ng2 == 4;
+  // K split (cluster size): the largest power of two up to 8 (and up to the
+  // 256-wide K chunks) that keeps the grid within one CTA per SM. Measured
+  // on GB300 (graph-timed, µs), against a fixed split of 8: [256,2048]
+  // M=32 4.12 -> 3.60 (split 4), M=64 5.24 -> 4.43 (split 2); [96,5120] M=64
+  // 5.16 -> 5.09 (split 4; a split of 2 took 7.3); the other shapes keep 8.
+  const int64_t chunks = K / 256;
+  const int64_t per_split = ceil_div(N, static_cast<int64_t>(skinny::kRows)) * slices;
+  const int64_t fit = std::max<int64_t>(1, device_sm_count() / std::max<int64_t>(1, per_split));
+  int ks = 1;
+  while (ks * 2 <= skinny::kMaxKS && ks * 2 <= chunks && ks * 2 <= fit) ks *= 2;
+  const bool multi = ceil_div(chunks, static_cast<int64_t>(ks)) > 1 || ng2 == 4;
 #define R4_SK(G)                                                                               \
-  return multi ? skinny::launch_ng<G, 2>(x, w, M, N, K, c, ldc, slices, st)                   \
-               : skinny::launch_ng<G, 1>(x, w, M, N, K, c, ldc, slices, st);
+  return multi ? skinny::launch_ng<G, 2>(x, w, M, N, K, c, ldc, slices, ks, st)               \
+               : skinny::launch_ng<G, 1>(x, w, M, N, K, c, ldc, slices, ks, st);
   switch (ng2) {
     case 1: R4_SK(1)
     case 2: R4_SK(2)
