@@ -1314,12 +1314,26 @@ static GemmPlan plan_mx_bt(int64_t M, int64_t N, int64_t K, int sms, bool a4, in
                              : 128.0 * 128 * 0.5 + 512 + 128.0 * bt;
   const double kb_flops = 2.0 * 128 * bt * 128;
   const double part_bytes = 128.0 * bt * 4;
+  // Prefill tiles (BT >= 128): the activation tile is read from L2 (every
+  // weight tile re-reads it), so only the weight bytes share HBM, and every
+  // K block's bytes pass through the CTA's shared-memory feed at ~110 GB/s
+  // per SM. Fitted to GB300 timings of forced 192- and 256-token tiles
+  // (interleaved, cold weights): 1024x34816x5120 predicted 121 / 133 us,
+  // measured 122 / 133; 4096x10240x5120 136 / 145 vs 137 / 145;
+  // 512x5120x17408 picks the 192-token tile (42.0 vs 48.1 us).
+  const double w_bytes = 128.0 * 128 * 0.5 + 512, feed_bw = 110e9;
+  auto unit_time = [&](int64_t kbps_, int64_t active) {
+    if (bt < 128)
+      return std::max(kbps_ * kb_bytes / std::min(hbm / active, sm_bw), kbps_ * kb_flops / sm_flops);
+    return std::max({kbps_ * w_bytes / std::min(hbm / active, sm_bw), kbps_ * kb_flops / sm_flops,
+                     kbps_ * kb_bytes / feed_bw});
+  };
   const double xchg_s = (bt <= 64 ? 2.5e-6 : 1.0e-6) * ((bt + 31) / 32);   // one cluster exchange per 32 tokens
-  // Epilogue drain of a prefill unit, on the critical path once per unit
-  // with one accumulator, else once per CTA (measured ~5,000 cycles at 256
-  // tokens).
+  // Epilogue drain of a prefill unit: at 256 tokens (one accumulator) the
+  // tensor pipe waits ~0.3 us per unit while eight warps pull it into
+  // registers; with two accumulators it costs once per CTA.
   const bool one_acc = bt == 256;
-  const double drain = bt >= 128 ? 1.0e-8 * bt : 0.0;
+  const double drain = bt == 256 ? 0.3e-6 : bt >= 128 ? 1.0e-8 * bt : 0.0;
   const int forced = options().w4a8_splits;
   // Prefill tiles (BT >= 128) split through the workspace only while the
   // tile count is under a quarter of the SM count, and through a cluster
@@ -1357,16 +1371,14 @@ static GemmPlan plan_mx_bt(int64_t M, int64_t N, int64_t K, int sms, bool a4, in
       const int64_t nclust = std::min<int64_t>(tiles, ncl);
       const int64_t active = nclust * s;
       const double waves = std::ceil(static_cast<double>(tiles) / nclust);
-      const double t_unit =
-          std::max(kbps * kb_bytes / std::min(hbm / active, sm_bw), kbps * kb_flops / sm_flops);
+      const double t_unit = unit_time(kbps, active);
       const double xchg = waves == 1 ? 3.0e-6 : xchg_s;   // one whole-tile round, or a round per 32 tokens
       t = waves * t_unit + xchg + 0.5e-6 * s + (one_acc ? waves : 1.0) * drain;
       grid = active;
     } else {
       const int64_t active = std::min<int64_t>(units, sms);
       const double waves = std::ceil(static_cast<double>(units) / sms);
-      const double t_unit =
-          std::max(kbps * kb_bytes / std::min(hbm / active, sm_bw), kbps * kb_flops / sm_flops);
+      const double t_unit = unit_time(kbps, active);
       t = waves * t_unit + (one_acc ? waves : 1.0) * drain;
       if (s > 1) t += (waves + s) * part_bytes / red_bw;
       grid = active;
