@@ -39,6 +39,7 @@ def r4q():
     yield m
     m.r4_set_option(10, 0)
     m.r4_set_option(1, 0)
+    m.r4_set_option(2, 0)
     m.r4_set_option(3, 0)
     m.r4_set_option(6, 1)
 
@@ -73,6 +74,55 @@ def test_bounded_wait_expires_and_reports(r4q):
     assert r4q.r4_device_error(clear=True) == 0
     c64, _ = G.gemm_w4a8(*ref)
     assert_gemm_matches(c, c64, "after the stalled launch")
+
+
+@pytest.mark.parametrize("mode,bt", [("w4a8", 256), ("w4a8", 192), ("w4a4", 256)])
+def test_prefill_stall_reports_and_recovers(r4q, mode, bt):
+    """The same on prefill tiles, whose roles differ from the decode ones:
+    the 256-token tile's four helper warps (they wait on the accumulator and
+    drain half of it), the 192-token tile's two accumulators, and the W4A4
+    scale warp (it waits on every stage's full barrier and the MMA thread
+    waits on its commits). CTA 0 withholds its first activation copy: every
+    role's wait must expire and return, the error must be reported, and the
+    next call must give the oracle's result."""
+    M, N, K = 600, 1024, 1024
+    x = synth.activations(M, K, synth.CFG_PREFILL)
+    w = synth.weights_fp32(N, K, synth.CFG_PREFILL)
+    p, sc = Q.quant_mxfp4_ocp(w.numpy())
+    pk = r4q.prepack_mxfp4(torch.from_numpy(p).cuda(), torch.from_numpy(sc).cuda(), N, K)
+    rows = np.unique(np.concatenate([synth.sample_indices(N, 128, 7).numpy(), [0, N - 1]]))
+    if mode == "w4a8":
+        q, s = Q.quant_act(x.float().numpy())
+        qd, sd = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+        call = lambda: r4q.gemm_w4a8(qd, sd, pk, N, K)
+        exact = lambda: G.gemm_w4a8(q, s, p, sc, rows=rows)[0]
+    else:
+        xq, xsc = Q.quant_act_mxfp4(x.float().numpy())
+        qd, qsd = r4q.quant_mxfp4(x.cuda())     # the GPU quantizer (bit-exact: test_gpu_w4a4.py)
+        call = lambda: r4q.gemm_w4a4(qd, qsd, pk, N, K)
+        exact = lambda: G.gemm_w4a4(xq, xsc, p, sc, rows=rows)[0]
+    r4q.r4_set_option(2, bt)
+    r4q.r4_set_option(1, 1)
+    try:
+        r4q.r4_device_error(clear=True)
+        r4q.r4_set_option(10, 1)
+        try:
+            t0 = time.time()
+            call()
+            torch.cuda.synchronize()
+            elapsed = time.time() - t0
+        finally:
+            r4q.r4_set_option(10, 0)
+        code = r4q.r4_device_error(clear=True)
+        assert code in (WAIT_FULL, WAIT_ACC_FULL, WAIT_DRAIN), f"device error word {code}"
+        assert 1.0 < elapsed < 30.0, f"the stalled launch took {elapsed:.1f} s"
+        c = call()
+        torch.cuda.synchronize()
+        assert r4q.r4_device_error(clear=True) == 0
+    finally:
+        r4q.r4_set_option(1, 0)
+        r4q.r4_set_option(2, 0)
+    assert_gemm_matches(c[:, torch.from_numpy(rows).cuda()], exact(), f"{mode} bt={bt} after the stalled launch")
 
 
 def _blockfp8_inputs(r4q, M, N, K):
