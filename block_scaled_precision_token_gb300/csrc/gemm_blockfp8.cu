@@ -52,6 +52,7 @@ struct Params {
   int M, KB;           // KB = K / 128 (blocks per row of As / Ws)
   int t_tiles, splits, kb_per_split, units;
   int ldc;
+  int tma_store;       // 1: unsplit tiles leave through shared memory and TMA tensor stores
   int inject_stall;    // test of the bounded waits: CTA 0 withholds its first activation copy
   int early_w;         // 1: weight tiles are requested before waiting for the preceding kernel
   const float *As;     // [M, KB]
@@ -83,11 +84,18 @@ struct Cfg {
   static constexpr uint32_t kScBytes = 2 * kScFloats * 4;
   static constexpr int kScPer = (BT * kChunk + kEpiThreads - 1) / kEpiThreads;   // As values per thread
   static constexpr uint32_t kMiscBytes = 1024;             // barriers and flags
-  static constexpr int kStagesRaw = static_cast<int>((227u * 1024u - 1024u - kMiscBytes - kScBytes) / kStageBytes);
+  // Unsplit tiles of 32-token warps store their output through shared
+  // memory: one [32 tokens][32 n] bf16 buffer per epilogue warp, written by
+  // the warp and handed to a TMA tensor store, so the next unit's promotion
+  // starts without waiting for global stores.
+  static constexpr bool kTmaOut = kCW == 32;
+  static constexpr uint32_t kOutBytes = kTmaOut ? static_cast<uint32_t>(kEpiWarps) * 2048u : 0u;
+  static constexpr int kStagesRaw =
+      static_cast<int>((227u * 1024u - 1024u - kMiscBytes - kScBytes - kOutBytes) / kStageBytes);
   static constexpr int kStagesCap = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
   static constexpr int kStages = (kStagesCap / kProd) * kProd;   // each producer owns fixed stages
   static constexpr uint32_t kTxBytes = kWSmem + kXSmem;
-  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kScBytes + kMiscBytes + 1024;
+  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kOutBytes + kScBytes + kMiscBytes + 1024;
   static_assert(kTmemCols >= 32 && (kTmemCols & (kTmemCols - 1)) == 0, "tensor-memory allocation");
   static_assert(kThreads <= 1024, "block size");
   static_assert(kStages >= kProd, "stage count");
@@ -177,11 +185,12 @@ __device__ __forceinline__ void copy_scale_chunk(const Params &p, const ChunkCur
 template <int BT>
 __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kThreads > 576 ? 96 : 128)
     blockfp8_f8f6f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                           const Params p) {
+                           const __grid_constant__ CUtensorMap tm_c, const Params p) {
   using C = Cfg<BT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float *scbuf = reinterpret_cast<float *>(smem + C::kStages * C::kStageBytes);   // [2][kScFloats]
+  uint8_t *outbuf = smem + C::kStages * C::kStageBytes;                         // [kEpiWarps][32][32] bf16
+  float *scbuf = reinterpret_cast<float *>(outbuf + C::kOutBytes);              // [2][kScFloats]
   uint8_t *misc = reinterpret_cast<uint8_t *>(scbuf) + C::kScBytes;
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(misc);   // [kMaxStages]
   uint64_t *empty_bar = full_bar + kMaxStages;               // [kMaxStages]
@@ -410,7 +419,20 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kTh
         break;
       }
       const int tcol = t0 + col0;
-      if (p.splits == 1) {
+      if (C::kTmaOut && p.splits == 1 && p.tma_store) {
+        // [token][n] rows of 64 bytes; the store clips tokens past M.
+        uint16_t *ob = reinterpret_cast<uint16_t *>(outbuf + ew * 2048);
+        if (lane == 0) bulk_wait_read0();   // this warp's previous store has read the buffer
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < C::kCW; ++j) ob[j * 32 + lane] = f32_to_bf16_rn(acc[j]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_c, ob, nt * 128 + q * 32, tcol);
+          bulk_commit();
+        }
+      } else if (p.splits == 1) {
 #pragma unroll
         for (int j = 0; j < C::kCW; ++j)
           if (tcol + j < p.M) p.c[static_cast<size_t>(tcol + j) * p.ldc + n] = f32_to_bf16_rn(acc[j]);
@@ -436,6 +458,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kTh
         named_bar_sync(2, C::kEpiThreads);
       }
     }
+    if (C::kTmaOut && lane == 0) bulk_wait_all();   // output stores complete before the CTA's smem goes away
     // An expired wait stopped this CTA: it still arrives, poisoned, at the
     // counter of every split-K tile it owed, so every counter ends at zero.
     if (abort_u >= 0 && p.splits > 1 && e == 0) {
@@ -476,9 +499,24 @@ int launch_bt(const uint8_t *q, const float *As, const uint8_t *packed, int64_t 
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return R4_ERR_CUDA;
   }
+  // Output through TMA tensor stores when C's base, row stride and row
+  // length are 16-byte multiples (N is a multiple of 128 here).
+  CUtensorMap tm_c;
+  int use_tma_store = 0;
+  if (C::kTmaOut && pl.splits == 1 && (reinterpret_cast<uintptr_t>(c) % 16) == 0 && (ldc * 2) % 16 == 0 &&
+      (N * 2) % 16 == 0) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(ldc) * 2};
+    const uint32_t box[2] = {32, 32};
+    use_tma_store =
+        encode_tiled(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) ==
+        CUDA_SUCCESS;
+  }
+  if (!use_tma_store) tm_c = tm_x;   // not read by the kernel in that case
   Params p;
   p.M = static_cast<int>(M);
   p.KB = pl.KB;
+  p.tma_store = use_tma_store;
   p.inject_stall = options().inject_stall;
   p.early_w = options().early_weights;
   p.t_tiles = pl.t_tiles;
@@ -494,7 +532,7 @@ int launch_bt(const uint8_t *q, const float *As, const uint8_t *packed, int64_t 
   p.err = device_error_word();
   auto kern = blockfp8_f8f6f4_kernel<BT>;
   if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::kSmemBytes) != cudaSuccess) return R4_ERR_CUDA;
-  if (launch_pdl(kern, dim3(pl.grid), dim3(C::kThreads), C::kSmemBytes, st, tm_w, tm_x, p) != cudaSuccess)
+  if (launch_pdl(kern, dim3(pl.grid), dim3(C::kThreads), C::kSmemBytes, st, tm_w, tm_x, tm_c, p) != cudaSuccess)
     return R4_ERR_CUDA;
   set_last_kernel(BT == 16   ? "blockfp8_f8f6f4_kernel<16>"
                   : BT == 32 ? "blockfp8_f8f6f4_kernel<32>"

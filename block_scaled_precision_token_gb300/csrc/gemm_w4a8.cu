@@ -53,17 +53,6 @@
 namespace r4 {
 namespace w4a8 {
 
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(x), "r"(y), "r"(smem_u32(src))
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 constexpr int kBK = 128;
 constexpr uint32_t kWSmem = 128 * 128;  // expanded e2m1 tile: 128 rows x 128 one-byte slots
 // The 16U4_ALIGN16B tile load completes the mbarrier transaction with the

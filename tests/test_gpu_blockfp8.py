@@ -110,3 +110,35 @@ def test_token_tiles_ragged(r4q, M, N, K):
     c64, _ = G.gemm_blockfp8(q, As, w, Ws, rows=rows)
     got = c if rows is None else c[:, torch.from_numpy(rows).cuda()]
     assert_gemm_matches(got, c64, f"M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,N,K,pad", [(300, 1024, 1024, 8), (300, 1024, 1024, 1), (64, 6144, 2048, 24),
+                                       (45, 384, 2048, 3), (200, 768, 512, 0)])
+def test_output_row_stride_guard_band(r4q, M, N, K, pad):
+    """C inside a larger buffer: a row stride that is a 16-byte multiple
+    (the tiles leave through TMA tensor stores) and one that is not (plain
+    stores), ragged token tiles (the tensor store clips rows past M), more
+    than one unit per CTA. The K split is forced to 1 (the unsplit tiles
+    are the ones stored from shared memory). Only the M x N block changes."""
+    q = random_e4m3_codes((M, K), seed=M + pad)
+    As = np.random.default_rng(M + 11).uniform(1e-3, 1e-2, (M, K // 128)).astype(np.float32)
+    w = random_e4m3_codes((N, K), seed=N + pad)
+    Ws = np.random.default_rng(N + 13).uniform(1e-4, 1e-3, (N // 128, K // 128)).astype(np.float32)
+    pk = r4q.prepack_blockfp8(torch.from_numpy(w).cuda(), torch.from_numpy(Ws).cuda(), N, K)
+    ldc = N + pad
+    full = torch.full((M + 3, ldc), 7.0, dtype=torch.bfloat16, device="cuda")
+    r4q.r4_set_option(3, 1)
+    try:
+        ws = r4q.workspace(r4q.R4_OP_BLOCKFP8, M, N, K)
+        r4q.r4_gemm_blockfp8(torch.from_numpy(q).cuda(), torch.from_numpy(As).cuda(), pk, M, N, K, full, ldc, ws)
+        check_device_error(r4q)
+    finally:
+        r4q.r4_set_option(3, 0)
+    rows = None if N <= 2048 else synth.sample_indices(N, 384, M).numpy()
+    c64, _ = G.gemm_blockfp8(q, As, w, Ws, rows=rows)
+    c = full[:M, :N]
+    got = c if rows is None else c[:, torch.from_numpy(rows).cuda()]
+    assert_gemm_matches(got, c64, f"M={M} N={N} K={K} ldc={ldc}")
+    g = full.float().cpu().numpy()
+    assert np.all(g[:M, N:] == 7.0), "kernel wrote outside columns [0, N)"
+    assert np.all(g[M:, :] == 7.0), "kernel wrote rows past M"
