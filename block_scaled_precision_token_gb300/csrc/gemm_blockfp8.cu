@@ -89,6 +89,13 @@ struct Cfg {
   // the warp and handed to a TMA tensor store, so the next unit's promotion
   // starts without waiting for global stores.
   static constexpr bool kTmaOut = kCW == 32;
+  // 128-token tiles accumulate token-major: the activation tile is the MMA's
+  // A operand (tensor-memory lane = token) and the weight tile its B operand
+  // (column = n), so each thread's scale for a K block is the single product
+  // As[t,kb] * Ws[nt,kb] -- one FMA per element -- and its 32 outputs are
+  // contiguous in a row of C. Narrower tiles keep the weights on the lanes
+  // (the MMA needs 128 rows).
+  static constexpr bool kTokMajor = BT == 128;
   static constexpr uint32_t kOutBytes = kTmaOut ? static_cast<uint32_t>(kEpiWarps) * 2048u : 0u;
   static constexpr int kStagesRaw =
       static_cast<int>((227u * 1024u - 1024u - kMiscBytes - kScBytes - kOutBytes) / kStageBytes);
@@ -306,7 +313,8 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kTh
         if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.err, DEV_ERR_WAIT_FULL)) break;
         tc_fence_after();
         uint8_t *st = smem + stage * C::kStageBytes;
-        const uint32_t a_base = smem_u32(st), b_base = smem_u32(st + kWSmem);
+        const uint32_t w_base = smem_u32(st), x_base = smem_u32(st + kWSmem);
+        const uint32_t a_base = C::kTokMajor ? x_base : w_base, b_base = C::kTokMajor ? w_base : x_base;
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * BT);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -389,6 +397,14 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kTh
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce_bar[buf]);
           const float ws = sc[kChunk * BT + i];
+          if constexpr (C::kTokMajor) {
+            // acc[n] += (As[t,kb] * Ws[kb]) * D[t,n]
+            const float sa = sc[i * BT + q * 32 + lane] * ws;
+#pragma unroll
+            for (int j = 0; j < C::kCW; j += 2)
+              fma_f32x2(acc[j], acc[j + 1], sa, sa, __uint_as_float(d[j]), __uint_as_float(d[j + 1]));
+            continue;
+          }
           const float4 *a4 = reinterpret_cast<const float4 *>(sc + i * BT + col0);
           // acc[t] += As[t,kb] * (Ws[kb] * D[n,t]): the weight scale is applied
           // to the block result in place (no extra registers), then the
@@ -419,7 +435,46 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kTh
         break;
       }
       const int tcol = t0 + col0;
-      if (C::kTmaOut && p.splits == 1 && p.tma_store) {
+      if constexpr (C::kTokMajor) {
+        // Thread = token t0 + 32q + lane, its 32 values = n nt*128 + col0 + j.
+        const int t = t0 + q * 32 + lane;
+        const int nc = nt * 128 + col0;
+        if (p.splits == 1 && p.tma_store) {
+          // [32 tokens][32 n] in the 64-byte swizzle (row r's 16-byte unit u at
+          // u ^ ((r >> 1) & 3): conflict-free rows); the store clips tokens past M.
+          uint8_t *ob = outbuf + ew * 2048;
+          if (lane == 0) bulk_wait_read0();   // this warp's previous store has read the buffer
+          __syncwarp();
+#pragma unroll
+          for (int u4 = 0; u4 < 4; ++u4) {
+            uint4 v;
+            v.x = pack_bf16x2(acc[8 * u4 + 0], acc[8 * u4 + 1]);
+            v.y = pack_bf16x2(acc[8 * u4 + 2], acc[8 * u4 + 3]);
+            v.z = pack_bf16x2(acc[8 * u4 + 4], acc[8 * u4 + 5]);
+            v.w = pack_bf16x2(acc[8 * u4 + 6], acc[8 * u4 + 7]);
+            *reinterpret_cast<uint4 *>(ob + lane * 64 + ((u4 ^ ((lane >> 1) & 3)) << 4)) = v;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_c, ob, nc, t0 + q * 32);
+            bulk_commit();
+          }
+        } else if (p.splits == 1) {
+          if (t < p.M) {
+            uint16_t *dst = p.c + static_cast<size_t>(t) * p.ldc + nc;
+#pragma unroll
+            for (int j = 0; j < C::kCW; ++j) dst[j] = f32_to_bf16_rn(acc[j]);
+          }
+        } else {
+          // partial tile [token][128 n], as the reduction reads it
+          float4 *part = reinterpret_cast<float4 *>(p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (128 * BT) +
+                                                    (q * 32 + lane) * 128 + col0);
+#pragma unroll
+          for (int j4 = 0; j4 < C::kCW / 4; ++j4)
+            part[j4] = make_float4(acc[4 * j4], acc[4 * j4 + 1], acc[4 * j4 + 2], acc[4 * j4 + 3]);
+        }
+      } else if (C::kTmaOut && p.splits == 1 && p.tma_store) {
         // [token][n] rows of 64 bytes; the store clips tokens past M.
         uint16_t *ob = reinterpret_cast<uint16_t *>(outbuf + ew * 2048);
         if (lane == 0) bulk_wait_read0();   // this warp's previous store has read the buffer
@@ -440,6 +495,8 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kTh
         float *part = p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (128 * BT);
 #pragma unroll
         for (int j = 0; j < C::kCW; ++j) part[(col0 + j) * 128 + q * 32 + lane] = acc[j];
+      }
+      if (p.splits > 1) {
         __threadfence();
         named_bar_sync(2, C::kEpiThreads);
         if (e == 0) {
@@ -508,9 +565,8 @@ int launch_bt(const uint8_t *q, const float *As, const uint8_t *packed, int64_t 
     const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
     const uint64_t strides[1] = {static_cast<uint64_t>(ldc) * 2};
     const uint32_t box[2] = {32, 32};
-    use_tma_store =
-        encode_tiled(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) ==
-        CUDA_SUCCESS;
+    use_tma_store = encode_tiled(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims, strides, box,
+                                 C::kTokMajor ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE) == CUDA_SUCCESS;
   }
   if (!use_tma_store) tm_c = tm_x;   // not read by the kernel in that case
   Params p;

@@ -63,9 +63,12 @@ def test_workload_shapes(r4q, M, N, K):
     assert_gemm_matches(got, c64, f"M={M} N={N} K={K}")
 
 
+@pytest.mark.parametrize("M", [45, 200])
 @pytest.mark.parametrize("splits", [1, 2, 5, 16])
-def test_forced_splits_ragged_m(r4q, splits):
-    M, N, K = 45, 384, 2048
+def test_forced_splits_ragged_m(r4q, splits, M):
+    """32-token tiles (M=45) and 128-token tiles (M=200, token-major
+    accumulator), each with a ragged last tile, at forced K splits."""
+    N, K = 384, 2048
     q = random_e4m3_codes((M, K), seed=3)
     As = np.random.default_rng(4).uniform(1e-3, 1e-2, (M, K // 128)).astype(np.float32)
     w = random_e4m3_codes((N, K), seed=5)
