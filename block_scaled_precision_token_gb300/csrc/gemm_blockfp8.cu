@@ -96,6 +96,7 @@ struct Cfg {
   // contiguous in a row of C. Narrower tiles keep the weights on the lanes
   // (the MMA needs 128 rows).
   static constexpr bool kTokMajor = BT == 128;
+  static constexpr int kRedU = BT == 128 ? 2 : 4;          // split-K reduction unroll (registers)
   static constexpr uint32_t kOutBytes = kTmaOut ? static_cast<uint32_t>(kEpiWarps) * 2048u : 0u;
   static constexpr int kStagesRaw =
       static_cast<int>((227u * 1024u - 1024u - kMiscBytes - kScBytes - kOutBytes) / kStageBytes);
@@ -508,8 +509,10 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kTh
         if (*is_last == 1) {
           __threadfence();
           const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (128 * BT);
-          reduce_partials_store<BT>(base, p.splits, min(BT, p.M - t0), nt * 128, nt * 128 + 128, nullptr, t0, p.c,
-                                    p.ldc, e, C::kEpiThreads);
+          // (the 128-token tile runs 19 warps at 96 registers: a lighter
+          // reduction keeps the whole kernel free of spills)
+          reduce_partials_store<BT, C::kRedU, C::kRedU>(base, p.splits, min(BT, p.M - t0), nt * 128, nt * 128 + 128,
+                                                        nullptr, t0, p.c, p.ldc, e, C::kEpiThreads);
         }
         if (*is_last && e == 0) p.counters[tile] = 0;
         named_bar_sync(2, C::kEpiThreads);

@@ -530,14 +530,14 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
 // deterministic -- and store bf16(scale[t] * sum) (scale == nullptr: 1) into
 // C[t0 + t][n0 + n] for t < tmax, n0 + n < N. The loads are independent L2
 // reads (.cg: the partials were written by other SMs), four n per thread.
-template <class SlotFn>
+template <int U = 4, int S = 4, class SlotFn>
 __device__ __forceinline__ void reduce_slots_store(SlotFn slot, int nslots, int tmax, int n0, int N,
                                                    const float *scale, int t0, uint16_t *c, int ldc, int tid,
                                                    int nthreads) {
-  // Each pass covers four float4 groups per thread and keeps up to 16 loads
-  // in flight (four slots at a time), so the pass costs about one L2 round
-  // trip per four slots instead of one per slot and group.
-  constexpr int U = 4, S = 4;
+  // Each pass covers U float4 groups per thread and keeps up to U x S loads
+  // in flight (S slots at a time), so the pass costs about one L2 round trip
+  // per S slots instead of one per slot and group. (Kernels under a tight
+  // register cap take smaller U and S.)
   const int total = tmax * 32;
   for (int base = tid; base < total; base += nthreads * U) {
     float4 acc[U];
@@ -590,13 +590,13 @@ __device__ __forceinline__ void reduce_slots_store(SlotFn slot, int nslots, int 
 }
 
 // The same for `splits` partial tiles [BT][128] stored one after another.
-template <int BT>
+template <int BT, int U = 4, int S = 4>
 __device__ __forceinline__ void reduce_partials_store(const float *base, int splits, int tmax, int n0, int N,
                                                       const float *scale, int t0, uint16_t *c, int ldc, int tid,
                                                       int nthreads) {
   constexpr size_t kTile = 128 * BT;
-  reduce_slots_store([&](int s2) { return base + s2 * kTile; }, splits, tmax, n0, N, scale, t0, c, ldc, tid,
-                     nthreads);
+  reduce_slots_store<U, S>([&](int s2) { return base + s2 * kTile; }, splits, tmax, n0, N, scale, t0, c, ldc, tid,
+                           nthreads);
 }
 
 }  // namespace r4
