@@ -14,9 +14,12 @@
 //    g % kNumBuf; with 512 columns there are 4 (BT = 128) to 16 buffers, so
 //    the MMAs run several K blocks ahead of the promotion epilogue;
 //  * 4 x kH epilogue warps (one per tensor-memory lane quarter and column
-//    group of 32 tokens) load each block result and fold it into fp32
-//    registers: acc[t] += As[t,kb] * (Ws[nt,kb] * D_kb[n,t]), the scaling
-//    and the accumulation each one packed f32x2 instruction per two columns;
+//    group) load each block result and fold it into fp32 registers. Tiles of
+//    up to 64 tokens keep the weights on the lanes, 32 (or 16) token columns
+//    per warp: acc[t] += As[t,kb] * (Ws[nt,kb] * D_kb[n,t]), the scaling and
+//    the accumulation each one packed f32x2 instruction per two columns. The
+//    128-token tile puts the tokens on the lanes (see Cfg::kTokMajor), eight
+//    warps of 64 n columns: acc[n] += (As[t,kb] * Ws[nt,kb]) * D_kb[t,n];
 //  * the scales reach the epilogue without a handshake per K block: the
 //    epilogue threads themselves copy As and Ws for a chunk of 16 K blocks
 //    of their tile into shared memory (As transposed, [kb][token], so a
@@ -69,11 +72,14 @@ struct Cfg {
   static constexpr int kMmaWarp = kProd;                   // first MMA-issuing warp
   static constexpr int kMma = 2;                           // MMA-issuing warps (slot g: warp g % kMma)
   static constexpr int kEpiWarp0 = kProd + kMma;
-  static constexpr int kCW = BT < 32 ? BT : 32;            // token columns per epilogue warp
+  // accumulator columns per epilogue warp: 64 n for the token-major 128-token
+  // tile (eight warps), else 32 (or BT) tokens
+  static constexpr int kCW = BT == 128 ? 64 : (BT < 32 ? BT : 32);
   static constexpr int kH = BT / kCW;                      // column groups
   static constexpr int kEpiWarps = 4 * kH;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+  static constexpr int kMaxReg = BT == 128 ? 168 : (kThreads > 576 ? 96 : 128);
   static constexpr int kNumBufRaw = 512 / BT;
   static constexpr int kNumBuf = kNumBufRaw > kMaxBuf ? kMaxBuf : kNumBufRaw;
   static constexpr uint32_t kTmemCols = static_cast<uint32_t>(kNumBuf * BT);
@@ -88,7 +94,7 @@ struct Cfg {
   // memory: one [32 tokens][32 n] bf16 buffer per epilogue warp, written by
   // the warp and handed to a TMA tensor store, so the next unit's promotion
   // starts without waiting for global stores.
-  static constexpr bool kTmaOut = kCW == 32;
+  static constexpr bool kTmaOut = kCW >= 32;
   // 128-token tiles accumulate token-major: the activation tile is the MMA's
   // A operand (tensor-memory lane = token) and the weight tile its B operand
   // (column = n), so each thread's scale for a K block is the single product
@@ -96,8 +102,8 @@ struct Cfg {
   // contiguous in a row of C. Narrower tiles keep the weights on the lanes
   // (the MMA needs 128 rows).
   static constexpr bool kTokMajor = BT == 128;
-  static constexpr int kRedU = BT == 128 ? 2 : 4;          // split-K reduction unroll (registers)
-  static constexpr uint32_t kOutBytes = kTmaOut ? static_cast<uint32_t>(kEpiWarps) * 2048u : 0u;
+  static constexpr int kRedU = BT == 128 ? 1 : 4;          // split-K reduction unroll (registers)
+  static constexpr uint32_t kOutBytes = kTmaOut ? static_cast<uint32_t>(kEpiWarps * kCW) * 64u : 0u;
   static constexpr int kStagesRaw =
       static_cast<int>((227u * 1024u - 1024u - kMiscBytes - kScBytes - kOutBytes) / kStageBytes);
   static constexpr int kStagesCap = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
@@ -191,7 +197,7 @@ __device__ __forceinline__ void copy_scale_chunk(const Params &p, const ChunkCur
 }
 
 template <int BT>
-__global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kThreads > 576 ? 96 : 128)
+__global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kMaxReg))
     blockfp8_f8f6f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                            const __grid_constant__ CUtensorMap tm_c, const Params p) {
   using C = Cfg<BT>;
@@ -387,11 +393,15 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kTh
             continue;
           }
           tc_fence_after();
-          uint32_t d[32];
-          if constexpr (C::kCW == 32) {
-            tc_ld_32x32b_x32(lane_base + static_cast<uint32_t>(buf * BT), d);
+          uint32_t d[C::kCW > 32 ? C::kCW : 32];
+          if constexpr (C::kCW == 64) {
+            tc_ld_32x32b_x32(lane_base + static_cast<uint32_t>(buf * BT), *reinterpret_cast<uint32_t(*)[32]>(&d[0]));
+            tc_ld_32x32b_x32(lane_base + static_cast<uint32_t>(buf * BT) + 32u,
+                             *reinterpret_cast<uint32_t(*)[32]>(&d[32]));
+          } else if constexpr (C::kCW == 32) {
+            tc_ld_32x32b_x32(lane_base + static_cast<uint32_t>(buf * BT), *reinterpret_cast<uint32_t(*)[32]>(&d[0]));
           } else {
-            tc_ld_32x32b_x16(lane_base + static_cast<uint32_t>(buf * BT), d);
+            tc_ld_32x32b_x16(lane_base + static_cast<uint32_t>(buf * BT), *reinterpret_cast<uint32_t(*)[32]>(&d[0]));
           }
           tc_wait_ld();
           tc_fence_before();
@@ -443,22 +453,27 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kTh
         if (p.splits == 1 && p.tma_store) {
           // [32 tokens][32 n] in the 64-byte swizzle (row r's 16-byte unit u at
           // u ^ ((r >> 1) & 3): conflict-free rows); the store clips tokens past M.
-          uint8_t *ob = outbuf + ew * 2048;
-          if (lane == 0) bulk_wait_read0();   // this warp's previous store has read the buffer
+          // one [32 tokens][32 n] box per 32 columns
+          uint8_t *ob = outbuf + ew * (C::kCW * 64);
+          if (lane == 0) bulk_wait_read0();   // this warp's previous stores have read the buffer
           __syncwarp();
 #pragma unroll
-          for (int u4 = 0; u4 < 4; ++u4) {
-            uint4 v;
-            v.x = pack_bf16x2(acc[8 * u4 + 0], acc[8 * u4 + 1]);
-            v.y = pack_bf16x2(acc[8 * u4 + 2], acc[8 * u4 + 3]);
-            v.z = pack_bf16x2(acc[8 * u4 + 4], acc[8 * u4 + 5]);
-            v.w = pack_bf16x2(acc[8 * u4 + 6], acc[8 * u4 + 7]);
-            *reinterpret_cast<uint4 *>(ob + lane * 64 + ((u4 ^ ((lane >> 1) & 3)) << 4)) = v;
-          }
+          for (int hh = 0; hh < C::kCW / 32; ++hh)
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+              const float *a = acc + 32 * hh + 8 * u4;
+              uint4 v;
+              v.x = pack_bf16x2(a[0], a[1]);
+              v.y = pack_bf16x2(a[2], a[3]);
+              v.z = pack_bf16x2(a[4], a[5]);
+              v.w = pack_bf16x2(a[6], a[7]);
+              *reinterpret_cast<uint4 *>(ob + hh * 2048 + lane * 64 + ((u4 ^ ((lane >> 1) & 3)) << 4)) = v;
+            }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tm_c, ob, nc, t0 + q * 32);
+#pragma unroll
+            for (int hh = 0; hh < C::kCW / 32; ++hh) tma_store_2d(&tm_c, ob + hh * 2048, nc + 32 * hh, t0 + q * 32);
             bulk_commit();
           }
         } else if (p.splits == 1) {
@@ -477,7 +492,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__(Cfg<BT>::kTh
         }
       } else if (C::kTmaOut && p.splits == 1 && p.tma_store) {
         // [token][n] rows of 64 bytes; the store clips tokens past M.
-        uint16_t *ob = reinterpret_cast<uint16_t *>(outbuf + ew * 2048);
+        uint16_t *ob = reinterpret_cast<uint16_t *>(outbuf + ew * (C::kCW * 64));
         if (lane == 0) bulk_wait_read0();   // this warp's previous store has read the buffer
         __syncwarp();
 #pragma unroll
