@@ -108,6 +108,13 @@ struct Cfg {
       static_cast<int>((227u * 1024u - 1024u - kMiscBytes - kScBytes - kOutBytes) / kStageBytes);
   static constexpr int kStagesCap = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
   static constexpr int kStages = (kStagesCap / kProd) * kProd;   // each producer owns fixed stages
+  // With at least as many stages as accumulator buffers, the stage's empty
+  // barrier (the MMA commit after slot g) also tells the epilogue that slot
+  // g's accumulator is complete, and the MMA thread commits once per slot:
+  // the MMAs of slot g + kStages (the stage's next phase) need the buffer of
+  // slot g + kStages - kNumBuf >= g back from the epilogue, so that barrier
+  // cannot run a phase ahead of the epilogue's wait.
+  static constexpr bool kFullIsEmpty = kStages >= kNumBuf;
   static constexpr uint32_t kTxBytes = kWSmem + kXSmem;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kOutBytes + kScBytes + kMiscBytes + 1024;
   static_assert(kTmemCols >= 32 && (kTmemCols & (kTmemCols - 1)) == 0, "tensor-memory allocation");
@@ -316,8 +323,8 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
         const uint32_t phase = static_cast<uint32_t>(g / C::kStages) & 1u;
         const int buf = g % C::kNumBuf;
         const uint32_t bphase = static_cast<uint32_t>(g / C::kNumBuf) & 1u;
-        if (!mbar_wait(&acce_bar[buf], bphase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_ACC_EMPTY)) break;
-        if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.err, DEV_ERR_WAIT_FULL)) break;
+        if (!mbar_spin_wait(&acce_bar[buf], bphase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_ACC_EMPTY)) break;
+        if (!mbar_spin_wait(&full_bar[stage], phase, abort_flag, p.err, DEV_ERR_WAIT_FULL)) break;
         tc_fence_after();
         uint8_t *st = smem + stage * C::kStageBytes;
         const uint32_t w_base = smem_u32(st), x_base = smem_u32(st + kWSmem);
@@ -328,7 +335,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
           tc_mma_f8f6f4(d_tmem, sdesc_sw128_kmajor(a_base + 32u * kk), sdesc_sw128_kmajor(b_base + 32u * kk), idesc,
                         kk > 0 ? 1u : 0u);
         tc_commit(&empty_bar[stage]);
-        tc_commit(&accf_bar[buf]);
+        if constexpr (!C::kFullIsEmpty) tc_commit(&accf_bar[buf]);
       }
       // All MMAs this thread issued must be complete before tensor memory is freed.
       tc_commit(&drain_bar[mw]);
@@ -386,9 +393,10 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
         for (int i = 0; i < nblk; ++i, ++g, cu.next(p)) {
           if (!ok) continue;           // stopped: skip to the chunk barrier
           const int buf = g % C::kNumBuf;
-          const uint32_t bphase = static_cast<uint32_t>(g / C::kNumBuf) & 1u;
+          uint64_t *fbar = C::kFullIsEmpty ? &empty_bar[g % C::kStages] : &accf_bar[buf];
+          const uint32_t fpar = static_cast<uint32_t>(C::kFullIsEmpty ? g / C::kStages : g / C::kNumBuf) & 1u;
           // Warp-uniform wait (tcgen05.ld needs the whole warp).
-          if (!warp_wait(&accf_bar[buf], bphase, abort_flag, p.err, DEV_ERR_WAIT_ACC_FULL)) {
+          if (!warp_spin_wait(fbar, fpar, abort_flag, p.err, DEV_ERR_WAIT_ACC_FULL)) {
             ok = false;
             continue;
           }

@@ -97,6 +97,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (no suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete. Returns false
 // (and raises *abort, records `code` in *err) on timeout, or false at once if
 // another role of the CTA has already aborted.
@@ -111,6 +124,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
       if (globaltimer_ns() - t0 > R4_WAIT_TIMEOUT_NS) {
         *abort = 1;
         atomicCAS(err, 0, code);   // keep the first error recorded
+        return false;
+      }
+    }
+  }
+}
+
+// mbar_wait by spinning on test_wait instead of a suspending try_wait, same
+// bounds and error contract. For handshakes on the critical path of every
+// K block, where waking a suspended thread costs more than the spin (block-
+// FP8 promotion on GB300: 3-4 % faster).
+__device__ __forceinline__ bool mbar_spin_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *err,
+                                               int code) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > R4_WAIT_TIMEOUT_NS) {
+        *abort = 1;
+        atomicCAS(err, 0, code);
         return false;
       }
     }
@@ -210,6 +244,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
                                           int code) {
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, err, code);
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// warp_wait with lane 0 spinning (mbar_spin_wait).
+__device__ __forceinline__ bool warp_spin_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *err,
+                                               int code) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_spin_wait(bar, parity, abort, err, code);
   __syncwarp();
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
