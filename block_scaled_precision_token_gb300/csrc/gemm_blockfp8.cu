@@ -669,12 +669,13 @@ GemmPlan plan_blockfp8(int64_t M, int64_t N, int64_t K, int sms) {
   }
   const int forced = options().fp8_splits;
   if (forced && forced <= pl.KB) best_s = forced;
+  if (tiles > kMaxCounterTiles) best_s = 1;   // the counter region holds at most this many tiles
   pl.kb_per_split = static_cast<int>(ceil_div(pl.KB, best_s));
   pl.splits = static_cast<int>(ceil_div(pl.KB, pl.kb_per_split));
   pl.units = static_cast<int>(tiles * pl.splits);
   pl.grid = std::min(pl.units, sms);
   if (pl.splits > 1) {
-    pl.counters_bytes = round_up(static_cast<size_t>(tiles) * 4, 256);
+    pl.counters_bytes = kCounterBytes;
     pl.ws_bytes = pl.counters_bytes + static_cast<size_t>(pl.units) * 128 * bt * 4;
   }
   return pl;

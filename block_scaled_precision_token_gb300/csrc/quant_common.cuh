@@ -52,19 +52,25 @@ __device__ __forceinline__ float div_by_scale(float x, float s, float rc) {
   return copysignf(__fmaf_rn(e, rc, q), x);
 }
 
+// Two fp32 -> two e4m3 codes in one instruction (round to nearest even,
+// saturating to +-448): lo in bits 0-7, hi in bits 8-15.
+__device__ __forceinline__ uint32_t e4m3x2_of(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // 8 bf16 -> 8 e4m3 codes (element i in byte i), each x/s correctly rounded;
 // rc = __frcp_rn(sc).
 __device__ __forceinline__ uint2 quant8(const uint4 &v, float sc, float rc) {
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t b[8];
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t b[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    b[2 * i] = e4m3_of(div_by_scale(bf16lo(w[i]), sc, rc));
-    b[2 * i + 1] = e4m3_of(div_by_scale(bf16hi(w[i]), sc, rc));
-  }
+  for (int i = 0; i < 4; ++i)
+    b[i] = e4m3x2_of(div_by_scale(bf16lo(w[i]), sc, rc), div_by_scale(bf16hi(w[i]), sc, rc));
   uint2 r;
-  r.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-  r.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+  r.x = b[0] | (b[1] << 16);
+  r.y = b[2] | (b[3] << 16);
   return r;
 }
 

@@ -22,7 +22,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "r4q.h")
 
 R4_OK, R4_ERR_INVALID_ARG, R4_ERR_UNSUPPORTED_SHAPE, R4_ERR_MISALIGNED = 0, 1, 2, 3
 R4_ERR_WORKSPACE, R4_ERR_CUDA, R4_ERR_DEVICE_TIMEOUT = 4, 5, 6
-R4_OP_W4A8_MXFP4, R4_OP_BLOCKFP8, R4_OP_BF16_SKINNY, R4_OP_W4A4_MXFP4 = 1, 2, 3, 4
+R4_OP_W4A8_MXFP4, R4_OP_BLOCKFP8, R4_OP_BF16_SKINNY, R4_OP_W4A4_MXFP4, R4_OP_LINEAR_W4A8_MXFP4 = 1, 2, 3, 4, 5
 
 
 class R4Error(RuntimeError):
@@ -49,6 +49,7 @@ _SIGS = {
     "r4_prepack_blockfp8": ([_P, _P, _I64, _I64, _P, _SZ, _P], _I),
     "r4_gemm_workspace_bytes": ([_I, _I64, _I64, _I64], _SZ),
     "r4_gemm_w4a8_mxfp4": ([_P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
+    "r4_linear_w4a8_mxfp4": ([_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
     "r4_gemm_blockfp8": ([_P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
     "r4_gemm_bf16_nt_skinny": ([_P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
     "r4_gemm_w4a8_mxfp4_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P, _I64, _P], _I),
@@ -206,6 +207,13 @@ def r4_gemm_w4a8_mxfp4(q, s, packed, M, N, K, c, ldc, workspace=None, stream=Non
            "r4_gemm_w4a8_mxfp4")
 
 
+def r4_linear_w4a8_mxfp4(x, ldx, packed, M, N, K, c, ldc, workspace, stream=None):
+    _need(x, torch.bfloat16, "x"); _need(c, torch.bfloat16, "c")
+    wp, wb = _ws(workspace)
+    _check(lib().r4_linear_w4a8_mxfp4(_ptr(x), ldx, _ptr(packed), M, N, K, _ptr(c), ldc, wp, wb, _stream(stream)),
+           "r4_linear_w4a8_mxfp4")
+
+
 def r4_gemm_w4a8_mxfp4_noalloc(q, s, packed, M, N, K, c, ldc, stream=None):
     """W4A8 GEMM without a caller workspace (split-K scratch is the library's
     static device buffer); for callers that cannot allocate device memory."""
@@ -339,6 +347,18 @@ def workspace(op, M, N, K, device="cuda"):
     if n == 0:
         return None
     return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def linear_w4a8(x, packed, N, K, ws=None, out=None, stream=None):
+    """bf16 activations x [M, K] (row stride x.stride(0)) -> bf16 [M, N]:
+    per-token quantization and the W4A8 GEMM in one call (one kernel for
+    M <= 16 with option 17 = 1)."""
+    M = x.shape[0]
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if out is None else out
+    if ws is None:
+        ws = workspace(R4_OP_LINEAR_W4A8_MXFP4, M, N, K, x.device)
+    r4_linear_w4a8_mxfp4(x, x.stride(0), packed, M, N, K, c, c.stride(0), ws, stream)
+    return c
 
 
 def gemm_w4a8(q, s, packed, N, K, ws=None, out=None, stream=None):

@@ -70,7 +70,13 @@ enum r4_status {
 };
 
 /* GEMM identifiers for r4_gemm_workspace_bytes(). */
-enum r4_gemm_op { R4_OP_W4A8_MXFP4 = 1, R4_OP_BLOCKFP8 = 2, R4_OP_BF16_SKINNY = 3, R4_OP_W4A4_MXFP4 = 4 };
+enum r4_gemm_op {
+  R4_OP_W4A8_MXFP4 = 1,
+  R4_OP_BLOCKFP8 = 2,
+  R4_OP_BF16_SKINNY = 3,
+  R4_OP_W4A4_MXFP4 = 4,
+  R4_OP_LINEAR_W4A8_MXFP4 = 5 /* r4_linear_w4a8_mxfp4 */
+};
 
 int r4_version(void);                 /* (major << 16) | minor */
 const char *r4_status_string(int status);
@@ -255,8 +261,12 @@ int r4_prepack_blockfp8(const uint8_t *w, const float *w_scale, int64_t N, int64
 
 /*
  * r4_gemm_workspace_bytes -- device workspace a GEMM call needs for (M, N, K):
- * split-K fp32 partials plus one int32 arrival counter per output tile. 0 when
- * the chosen schedule needs none. The counters must be zero when the
+ * a fixed 16 KiB region of int32 arrival counters (one per output tile) at
+ * the start, then the split-K fp32 partials. 0 when the chosen schedule needs
+ * none (schedules with more than 4096 output tiles never split). Because the
+ * counters are always at the start and no call writes anything else there,
+ * one workspace may serve calls of different ops and shapes one after
+ * another (sized for the largest). The counters must be zero when the
  * workspace is first used (e.g. cudaMemsetAsync once after allocation); every
  * call leaves them zero again, including a call whose kernel stopped early
  * because a bounded device wait expired (r4_device_error reports it): such a
@@ -284,6 +294,34 @@ size_t r4_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
 int r4_gemm_w4a8_mxfp4(const uint8_t *q, const float *s, const void *packed, int64_t M,
                        int64_t N, int64_t K, uint16_t *c, int64_t ldc, void *workspace,
                        size_t workspace_bytes, r4_stream_t stream);
+
+/*
+ * r4_linear_w4a8_mxfp4 -- the W4A8 linear layer from bf16 activations:
+ * r4_quant_fp8_per_token(x, group = K) followed by r4_gemm_w4a8_mxfp4, with
+ * the same result bit for bit.
+ * Source: "radiance_mxfp4.py", module docstring (per-token FP8 activations
+ * feeding the W4A8 GEMM) and _traced_quant (the quantization rule).
+ * By default it runs the quantization kernel into the workspace and then the
+ * GEMM (two launches). With option 17 = 1 and M <= 16 (one 16-token tile,
+ * x 16-byte aligned) the quantization runs inside the GEMM kernel instead
+ * (one launch): each CTA computes the token scales over the whole rows and
+ * quantizes the bf16 block of every pipeline stage itself. Measured on GB300
+ * in CUDA graphs that one launch is slower than the two (each CTA redoes the
+ * row maxima and the quantization of the blocks it streams), so it is off.
+ *   x        bf16 [M, ldx] row-major, ldx >= K, ldx % 8 == 0; 16-B aligned
+ *            for the fused path (else the two-launch path runs).
+ *   packed   prepacked weight from r4_prepack_mxfp4(N, K).
+ *   c        bf16 [M, ldc] row-major; columns [0, N) are written, nothing else.
+ *   workspace  r4_gemm_workspace_bytes(R4_OP_LINEAR_W4A8_MXFP4, M, N, K)
+ *            bytes, 256-byte aligned, counters zeroed once: the GEMM's
+ *            workspace (counter region always reserved), then room for the
+ *            quantized activations of the two-launch path.
+ * Requirements: M >= 1, N >= 1, K % 32 == 0, K >= 128, ldc >= N. Errors as
+ * r4_gemm_w4a8_mxfp4 (R4_ERR_WORKSPACE for a missing or short workspace).
+ */
+int r4_linear_w4a8_mxfp4(const uint16_t *x, int64_t ldx, const void *packed, int64_t M, int64_t N,
+                         int64_t K, uint16_t *c, int64_t ldc, void *workspace, size_t workspace_bytes,
+                         r4_stream_t stream);
 
 /*
  * r4_gemm_w4a4_mxfp4 -- the W4A4 variant, MXFP4 activations x MXFP4 weights:
@@ -401,6 +439,8 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * setting the option. (Measured on GB300 it is slower than the default
  * schedule on the decode shapes; it is an option for other shapes and
  * GPUs.)
+ * key 17: r4_linear_w4a8_mxfp4 quantizes inside the GEMM kernel when it can
+ * (1) or always runs the quantization kernel first (0, default).
  */
 int r4_set_option(int key, int64_t value);
 

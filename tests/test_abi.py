@@ -52,6 +52,8 @@ def test_options(r4q):
     assert lib.r4_set_option(2, 160) == r4q.R4_ERR_INVALID_ARG
     assert lib.r4_set_option(16, 3) == r4q.R4_ERR_INVALID_ARG and lib.r4_set_option(16, -1) == r4q.R4_ERR_INVALID_ARG
     assert lib.r4_set_option(16, 2) == 0 and lib.r4_set_option(16, 1) == 0 and lib.r4_set_option(16, 0) == 0
+    assert lib.r4_set_option(17, 2) == r4q.R4_ERR_INVALID_ARG and lib.r4_set_option(17, -1) == r4q.R4_ERR_INVALID_ARG
+    assert lib.r4_set_option(17, 0) == 0 and lib.r4_set_option(17, 1) == 0
     assert lib.r4_set_option(1, 0) == 0 and lib.r4_set_option(3, 0) == 0
 
 
@@ -117,6 +119,14 @@ def test_validation_of_the_later_entry_points(r4q):
     assert na(good, good, good, 8, 256, 2000, good, 256, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
     assert na(good, good, odd8, 8, 256, 2048, good, 256, S) == r4q.R4_ERR_MISALIGNED
     assert na(odd8, good, good, 8, 256, 2048, good, 256, S) == r4q.R4_ERR_MISALIGNED
+    ln = lib.r4_linear_w4a8_mxfp4
+    assert ln(None, 2048, good, 8, 256, 2048, good, 256, good, 1 << 20, S) == r4q.R4_ERR_INVALID_ARG
+    assert ln(good, 2048, good, 8, 256, 2048, good, 100, good, 1 << 20, S) == r4q.R4_ERR_INVALID_ARG
+    assert ln(good, 1024, good, 8, 256, 2048, good, 256, good, 1 << 20, S) == r4q.R4_ERR_INVALID_ARG
+    assert ln(good, 0, good, 0, 256, 2048, good, 256, good, 1 << 20, S) == r4q.R4_ERR_INVALID_ARG
+    assert ln(good, 2000, good, 8, 256, 2000, good, 256, good, 1 << 20, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert ln(good, 2052, good, 8, 256, 2048, good, 256, good, 1 << 20, S) == r4q.R4_ERR_UNSUPPORTED_SHAPE
+    assert ln(good, 2048, odd8, 8, 256, 2048, good, 256, good, 1 << 20, S) == r4q.R4_ERR_MISALIGNED
     assert lib.r4_check_quotients(None, good, S) == r4q.R4_ERR_INVALID_ARG
     assert lib.r4_check_quotients(odd4, good, S) == r4q.R4_ERR_MISALIGNED
 
