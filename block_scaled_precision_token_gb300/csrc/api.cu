@@ -191,10 +191,6 @@ int r4_set_option(int key, int64_t value) {
       if (value < 0 || value > 2) return R4_ERR_INVALID_ARG;
       options().stream_k = static_cast<int>(value);
       return R4_OK;
-    case 17:
-      if (value < 0 || value > 1) return R4_ERR_INVALID_ARG;
-      options().fuse_quant = static_cast<int>(value);
-      return R4_OK;
     case 5:
       if (value < 0 || value > 2) return R4_ERR_INVALID_ARG;
       options().l2_prefetch = static_cast<int>(value);
@@ -380,7 +376,7 @@ int r4_linear_w4a8_mxfp4(const uint16_t *x, int64_t ldx, const void *packed, int
   if (!x || !packed || !c) return R4_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1 || ldc < N || ldx < K || M > (1 << 30) || N > (1 << 30)) return R4_ERR_INVALID_ARG;
   if (K % 32 || K < 128 || ldx % 8) return R4_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(packed, 256) || !aligned(c, 2) || !aligned(x, 2)) return R4_ERR_MISALIGNED;
+  if (!aligned(packed, 256) || !aligned(c, 2) || !aligned(x, 16)) return R4_ERR_MISALIGNED;
   const GemmPlan pl = plan_w4a8(M, N, K, device_sm_count());
   // [the GEMM's workspace, counters first, at least the counter region][q][s]
   const size_t gpart = linear_gemm_part_bytes(pl.ws_bytes);
@@ -389,9 +385,6 @@ int r4_linear_w4a8_mxfp4(const uint16_t *x, int64_t ldx, const void *packed, int
   if (device_error_word() == nullptr) return R4_ERR_CUDA;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   void *gws = pl.ws_bytes ? workspace : nullptr;
-  if (options().fuse_quant && pl.BT == 16 && !pl.cluster && !pl.sk && aligned(x, 16))
-    return launch_linear_w4a8_fused(x, ldx, static_cast<const uint8_t *>(packed), M, N, K, c, ldc, gws, pl, st);
-  if (!aligned(x, 16)) return R4_ERR_MISALIGNED;   // the quantization kernel reads 16-byte vectors
   uint8_t *q = static_cast<uint8_t *>(workspace) + gpart;
   float *s = reinterpret_cast<float *>(q + round_up(static_cast<size_t>(M) * K, 256));
   if (launch_quant_act(x, M, K, ldx, K, q, s, st) != cudaSuccess) return R4_ERR_CUDA;

@@ -47,7 +47,6 @@
 #include <algorithm>
 #include <cmath>
 
-#include "quant_common.cuh"
 #include "r4_device.cuh"
 #include "r4_internal.h"
 
@@ -73,7 +72,6 @@ constexpr int kMaxClusterSplit = 6;   // the planner splits K across a cluster o
 
 struct Params {
   int M, N, KB;
-  int K;                 // columns of x (fused quantization)
   const uint8_t *xsf;    // W4A4: activation scale atoms [KB][xatoms][512] (K-block-major)
   int xatoms;            // W4A4: 128-token scale atoms per K block
   int t_tiles, splits, kb_per_split, units;
@@ -90,12 +88,6 @@ struct Params {
   int early_w;           // 1: weight tiles are requested before waiting for the preceding kernel
   const uint8_t *w;      // packed weight codes [NT][KB][128][64]
   const float *s;
-  // Fused per-token quantization (16-token W4A8 tiles): the producers read
-  // bf16 activations x [M][ldx], compute each token's scale and write the
-  // e4m3 activation tile of every stage themselves (fuse_q = 1; q and s unused).
-  const uint16_t *x;
-  long long ldx;
-  int fuse_q;
   const uint8_t *sf;     // scale atoms of the prepacked weight
   uint16_t *c;
   float *partials;
@@ -159,22 +151,14 @@ struct Cfg {
   static constexpr uint32_t kXSmem = A4 ? BT * 64 : BT * 128;   // activation tile
   static constexpr int kXAtoms = A4 ? (BT > 128 ? 2 : 1) : 0;   // activation scale atoms per stage
   static constexpr uint32_t kSfOff = kWBytes + kXSmem;          // weight scale atom, then activation atoms
-  // 16-token W4A8 tiles can quantize their own activations (Params::fuse_q):
-  // the stage then also holds the bf16 activation block (16 x 128) the
-  // producer copies in, from which the MMA warp writes the e4m3 tile.
-  static constexpr bool kFuseQ = BT == 16 && !A4;
-  static constexpr uint32_t kXrawOff = kSfOff + kSfBytes * (1 + kXAtoms);
-  static constexpr uint32_t kXrawBytes = kFuseQ ? 16u * 128u * 2u : 0u;
-  static constexpr uint32_t kStageBytes = ((kXrawOff + kXrawBytes + 1023) / 1024) * 1024;
+  static constexpr uint32_t kStageBytes = ((kSfOff + kSfBytes * (1 + kXAtoms) + 1023) / 1024) * 1024;
   static constexpr int kOutChunk = BT < 32 ? BT : 32;                // tokens per output chunk
   static constexpr uint32_t kOutBytes = 2u * kOutChunk * 128u * 2u;  // two bf16 [chunk][128] buffers
   static constexpr int kStagesRaw = static_cast<int>((208u * 1024u) / kStageBytes);
   static constexpr int kStagesCap = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
   static constexpr int kStages = (kStagesCap / kPad) * kPad;        // every warp owns fixed stages
   static constexpr uint32_t kTxBytes = kWTxBytes + kXSmem + kSfBytes * (1 + kXAtoms);
-  static constexpr uint32_t kTxFused = kWTxBytes + kSfBytes + kXrawBytes;   // weights, atom, bf16 block
-  // fused quantization: the token scales and the row maxima live behind the barriers
-  static constexpr uint32_t kMiscBytes = kFuseQ ? 2048 : 1024;
+  static constexpr uint32_t kMiscBytes = 1024;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kMiscBytes + kOutBytes + 1024;  // + align slack
   static_assert(kAccCols <= kSfaCol, "accumulators overlap the scale columns");
   static_assert(kSfbCol + (A4 ? 8u * kMaxStages : 16u * kIss) <= kTmemCols, "scale columns past tensor memory");
@@ -250,32 +234,6 @@ __device__ __forceinline__ void pf_load(const Params &p, PfCursor &c) {
   decode_unit(p, c.u, nt, tt, sp, kb0, kb1);
   c.nkb = kb1 - kb0;
   c.blk = static_cast<size_t>(nt) * p.KB + kb0;
-}
-
-// The rolling prefetch's first position: the first K block that the ring's
-// initial fill (the first `stages` slots, padding slots included) leaves out.
-template <int PAD>
-__device__ __forceinline__ PfCursor rolling_start(const Params &p, int stages) {
-  PfCursor pf{p.units, 0};
-  int left = stages;
-  pf.u = blockIdx.x;
-  while (pf.u < p.units) {
-    int nt, tt, sp, kb0, kb1;
-    decode_unit(p, pf.u, nt, tt, sp, kb0, kb1);
-    const int nkb = kb1 - kb0, nslots = (nkb + PAD - 1) / PAD * PAD;
-    if (left < nslots) {
-      pf.kb = min(left, nkb);
-      if (pf.kb == nkb) {
-        pf.u += gridDim.x;
-        pf.kb = 0;
-      }
-      break;
-    }
-    left -= nslots;
-    pf.u += gridDim.x;
-  }
-  pf_load(p, pf);
-  return pf;
 }
 
 // Bulk L2 prefetch of `count` K blocks (weight codes and scale atoms, both
@@ -391,105 +349,6 @@ __device__ __forceinline__ void drain_half_to_regs(const Params &p, const CUtens
   }
 }
 
-// Fused per-token quantization (16-token W4A8 tiles, Params::fuse_q). Each
-// token's scale is computed over its whole row exactly as the quantization
-// kernel computes it (same row maximum, s = max(RN(amax/448), 1/(448*512)),
-// correctly rounded quotients, the same conversion), so the codes -- and
-// the GEMM -- are identical to quantizing first. The producers copy each
-// block's bf16 activations (16 x 128, rows >= M and columns >= K zero-filled
-// by the TMA) into the stage; the MMA warp that owns the slot quantizes them
-// into the e4m3 tile just before its MMAs.
-
-// The 4 MMA warps and the 4 epilogue warps (256 threads, w8 = their index
-// 0..7): the token scales s_buf[0..16) (rows >= M get the floor scale), and
-// token rows M..15 of every stage's e4m3 tile zeroed once (nothing writes
-// them again). Loads of all 16 rows are in flight together.
-template <class C>
-__device__ __forceinline__ void fused_scales(const Params &p, uint8_t *smem, float *s_buf, float *rowmax, int w8,
-                                             int lane) {
-  constexpr int NT = 256;
-  pdl_wait();   // x comes from the preceding kernel
-  const int tid = w8 * 32 + lane;
-  for (int s_ = 0; s_ < C::kStages; ++s_) {
-    uint8_t *xs = smem + s_ * C::kStageBytes + C::kWBytes;
-    for (int o = p.M * 128 + tid * 16; o < 16 * 128; o += NT * 16)
-      *reinterpret_cast<uint4 *>(xs + o) = make_uint4(0, 0, 0, 0);
-  }
-  fence_proxy_async_smem();   // the tensor core reads these rows through the async proxy
-  const int nvec = p.K / 8;
-  float a[16];
-#pragma unroll
-  for (int t = 0; t < 16; ++t) a[t] = 0.f;
-  for (int v = tid; v < nvec; v += NT) {
-    uint4 r[16];
-#pragma unroll
-    for (int t = 0; t < 16; ++t)
-      r[t] = t < p.M ? __ldg(reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(t) * p.ldx + 8 * v))
-                     : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int t = 0; t < 16; ++t) a[t] = fmaxf(a[t], qc::absmax8(r[t]));
-  }
-#pragma unroll
-  for (int t = 0; t < 16; ++t) {
-    const float m = qc::warp_max(a[t]);
-    if (lane == 0) rowmax[w8 * 16 + t] = m;
-  }
-  named_bar_sync(2, NT);
-  if (tid < 16) {
-    float m = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) m = fmaxf(m, rowmax[w * 16 + tid]);
-    s_buf[tid] = fmaxf(__fdiv_rn(m, qc::kFp8Max), qc::kMinScale);
-  }
-  named_bar_sync(2, NT);
-}
-
-// Epilogue warp ew (all 32 lanes) of a 16-token W4A8 tile with fused
-// quantization: the slots of one unit that belong to it (i = ew, ew + 4, ...,
-// the MMA warps' slot order), before it waits for that unit's accumulator.
-// Per slot: wait for the stage (weights, scale atom and the bf16 block),
-// quantize the M x 128 values -- 16 items of 8 per token row, item k = (t, h)
-// = (k / 16, k % 16), items lane, lane + 32, ... -- into the e4m3 tile in the
-// 128-byte swizzle the TMA would have produced (row t's 16-byte chunk c at
-// c ^ (t & 7)), make it visible to the tensor core and arrive on the stage's
-// "ready" barrier, which the MMA thread waits on instead of the full one (a
-// padding slot gets a plain arrival). Returns false after an expired wait.
-template <class C>
-__device__ __forceinline__ bool quantize_unit_slots(const Params &p, uint8_t *smem, uint64_t *full_bar,
-                                                    uint64_t *ready_bar, const float *sc, const float *rc,
-                                                    int nkb, int nslots, int ew, int lane, int &stage,
-                                                    uint32_t &phase, volatile int *abort_flag) {
-  const int items = p.M * 16;   // (M <= 16: at most 8 per lane)
-  for (int i = ew; i < nslots; i += C::kIss) {
-    // every lane observes the stage's completion before reading the block
-    if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[stage], phase, abort_flag, p.err, DEV_ERR_WAIT_FULL)))
-      return false;
-    if (i < nkb) {
-      uint8_t *st = smem + stage * C::kStageBytes;
-      const uint8_t *raw = st + C::kXrawOff;
-      uint8_t *xs = st + C::kWBytes;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int kk = lane + 32 * r;
-        if (kk < items) {
-          const int t = kk >> 4, h = kk & 15;
-          const uint2 q8 = qc::quant8(*reinterpret_cast<const uint4 *>(raw + kk * 16), sc[r], rc[r]);
-          *reinterpret_cast<uint2 *>(xs + t * 128 + (((h >> 1) ^ (t & 7)) << 4) + (h & 1) * 8) = q8;
-        }
-      }
-      fence_proxy_async_smem();   // the tensor core reads the tile through the async proxy
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ready_bar[stage]);
-    stage += C::kIss;
-    if (stage >= C::kStages) {
-      stage -= C::kStages;
-      phase ^= 1u;
-    }
-  }
-  return true;
-}
-
 template <int BT, bool A4>
 __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT, A4>::kMaxReg))
     w4a8_mxf8f6f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
@@ -497,23 +356,19 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
   using C = Cfg<BT, A4>;
   constexpr int kXStep = A4 ? 64 : kBK;   // activation tile x coordinate per 128-K block (bytes)
   // per-token output scale: s[t] for W4A8; none for W4A4 (both scales are in the MMA)
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *misc = smem + C::kStages * C::kStageBytes;
-  // fused quantization: token scales [16], per-warp row maxima [8][16]
-  float *s_buf = reinterpret_cast<float *>(misc + 1024);
-  float *rowmax = s_buf + 32;
-  const bool fused = C::kFuseQ && p.fuse_q;
   auto out_scale = [&](int t) -> float {
     if constexpr (A4) {
       return 1.f;
     } else {
-      return fused ? s_buf[t] : __ldg(p.s + t);
+      return __ldg(p.s + t);
     }
   };
   constexpr int ISS = C::kIss;    // MMA-issuing warps
   constexpr int PROD = C::kProd;  // TMA producer warps
   constexpr int PAD = C::kPad;    // a unit's slots are padded to a multiple of this
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *misc = smem + C::kStages * C::kStageBytes;
   uint8_t *sfb_const = misc;                                         // 512 B of 0x7F
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(misc + 512);     // [16]
   uint64_t *empty_bar = full_bar + kMaxStages;                       // [16]
@@ -575,9 +430,6 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
     // Slot sequence: every unit's k-blocks, padded to a multiple of PAD. A
     // padding slot carries no data: its full barrier gets a plain arrival.
     const int pw = warp;
-    // (fused quantization: the stage's transaction is the weights, the scale
-    // atom and the bf16 activation block, which lands behind the scale atom)
-    const uint32_t tx = fused ? C::kTxFused : C::kTxBytes;
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
@@ -599,7 +451,24 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
       PfCursor pf{p.units, 0};
       const bool rolling = p.l2_prefetch == 2 && pw == 0 && BT <= 64;
       if (rolling) {
-        pf = rolling_start<PAD>(p, C::kStages);
+        int left = C::kStages;
+        pf.u = blockIdx.x;
+        while (pf.u < p.units) {
+          int nt, tt, sp, kb0, kb1;
+          decode_unit(p, pf.u, nt, tt, sp, kb0, kb1);
+          const int nkb = kb1 - kb0, nslots = (nkb + PAD - 1) / PAD * PAD;
+          if (left < nslots) {
+            pf.kb = min(left, nkb);
+            if (pf.kb == nkb) {
+              pf.u += gridDim.x;
+              pf.kb = 0;
+            }
+            break;
+          }
+          left -= nslots;
+          pf.u += gridDim.x;
+        }
+        pf_load(p, pf);
         prefetch_blocks_l2(p, pf, kPfAhead);
       }
       {
@@ -614,7 +483,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
             if (i < nkb) {
               uint8_t *st = smem + s_ * C::kStageBytes;
               const int kb = kb0 + i;
-              mbar_arrive_expect_tx(&full_bar[s_], tx);
+              mbar_arrive_expect_tx(&full_bar[s_], C::kTxBytes);
               tma_load_3d(st, &tm_w, &full_bar[s_], 0, 0, nt * p.KB + kb, pol_w);
               bulk_load(st + C::kSfOff, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
                         &full_bar[s_], pol_w);
@@ -644,7 +513,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
               break;
             }
             if (i < nkb) {
-              mbar_arrive_expect_tx(&full_bar[stage], tx);
+              mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
               tma_load_3d(st, &tm_w, &full_bar[stage], 0, 0, nt * p.KB + kb, pol_w);
               bulk_load(st + C::kSfOff, p.sf + static_cast<size_t>(nt * p.KB + kb) * kSfBytes, kSfBytes,
                         &full_bar[stage], pol_w);
@@ -656,12 +525,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
           // first activation copy, so that stage's transaction never completes
           // and the consumer's bounded wait must expire and report.)
           const bool withhold = p.inject_stall && blockIdx.x == 0 && gbase + i == 0;
-          if (i < nkb && !withhold) {
-            if (fused)   // the bf16 block: 128 columns from kb * 128, token rows from 0 (M <= 16)
-              tma_load_2d(st + C::kXrawOff, &tm_x, &full_bar[stage], kb * kBK, 0, pol_x);
-            else
-              tma_load_2d(st + C::kWBytes, &tm_x, &full_bar[stage], kb * kXStep, tt * BT, pol_x);
-          }
+          if (i < nkb && !withhold) tma_load_2d(st + C::kWBytes, &tm_x, &full_bar[stage], kb * kXStep, tt * BT, pol_x);
           if constexpr (A4) {
             // the activation scale atom(s) of this token tile and K block:
             // adjacent in the K-block-major layout, one copy
@@ -695,8 +559,6 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
   } else if (warp < PROD + ISS) {
     // ------------------------------------------------------------ MMA issuers (warps PROD..PROD+ISS-1)
     const int mw = warp - PROD;
-    if constexpr (C::kFuseQ)
-      if (fused) fused_scales<C>(p, smem, s_buf, rowmax, mw, lane);
     if (lane == 0) {
       const uint32_t sfb = tmem + C::kSfbCol + 16u * static_cast<uint32_t>(mw);
       if constexpr (!A4) {
@@ -720,10 +582,9 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
         const uint32_t d_tmem = tmem + static_cast<uint32_t>((mw * C::kNumAcc + acc) * BT);
         bool first = true;
         for (int i = mw; i < nslots; i += ISS) {
-          // with a scale warp (or the epilogue warps quantizing the
-          // activations), its "ready" barrier -- which follows the stage's
-          // full barrier -- also stands for the stage's data
-          if (!mbar_wait((C::kScaleWarp || fused) ? &sready_bar[stage] : &full_bar[stage], phase, abort_flag, p.err,
+          // with a scale warp, its "scales ready" barrier (which follows the
+          // stage's full barrier) also stands for the stage's data
+          if (!mbar_wait(C::kScaleWarp ? &sready_bar[stage] : &full_bar[stage], phase, abort_flag, p.err,
                          DEV_ERR_WAIT_FULL)) {
             ok = false;
             break;
@@ -878,11 +739,7 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
     if (lane == 0) bulk_wait_all();   // output stores complete before the CTA's smem goes away
   } else {
     // ------------------------------------------------------------ epilogue (4 warps)
-    if (fused) {                    // (fused quantization: the token scales, with the MMA warps)
-      if constexpr (C::kFuseQ) fused_scales<C>(p, smem, s_buf, rowmax, warp - PROD, lane);
-    } else {
-      pdl_wait();                   // s, C and the workspace belong to the kernel stream order
-    }
+    pdl_wait();                     // s, C and the workspace belong to the kernel stream order
     const int q = warp & 3;         // tensor-memory lane quarter this warp may access
     const int ew = warp - C::kEpiWarp0;
     int acc = 0;
@@ -893,30 +750,10 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
     uint32_t xchg = 0;        // running count of cluster split-K exchanges
     bool stop = false;
     int abort_u = -1;         // unit at which an expired wait stopped the epilogue
-    // fused quantization: this warp's slots (the MMA warps' order) and its token scales
-    int qstage = ew;
-    uint32_t qphase = 0;
-    float qsc[8], qrc[8];
-    if constexpr (C::kFuseQ) {
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int k = lane + 32 * r;
-        qsc[r] = fused ? s_buf[(k < p.M * 16 ? k : 0) >> 4] : 1.f;
-        qrc[r] = __frcp_rn(qsc[r]);
-      }
-    }
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
       int nt, tt, sp, kb0, kb1;
       decode_unit(p, u, nt, tt, sp, kb0, kb1);
       if (kb1 <= kb0) continue;                   // empty stream-K unit
-      if constexpr (C::kFuseQ) {
-        if (fused) {
-          const int nkb_u = kb1 - kb0, nslots_u = (nkb_u + PAD - 1) / PAD * PAD;
-          if (!quantize_unit_slots<C>(p, smem, full_bar, sready_bar, qsc, qrc, nkb_u, nslots_u, ew, lane, qstage,
-                                      qphase, abort_flag))
-            *epi_abort = 1;   // (the accumulator wait below then fails at once and the unit stops)
-        }
-      }
       const int ncontrib = min(ISS, kb1 - kb0);   // MMA warps that accumulated something
       // The decision to stop must be the same in all 128 epilogue threads
       // (they meet at named barriers below): a failed wait is published
@@ -1232,11 +1069,11 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
               const int j = tile - sk_begin(p, c) / p.KB;
               return p.partials + (static_cast<size_t>(c) + static_cast<size_t>(j) * p.sk_grid) * (128 * BT);
             };
-            reduce_slots_store(slot_ptr, nseg, min(BT, p.M - t0), nt * 128, p.N, A4 ? nullptr : (fused ? s_buf : p.s), t0, p.c,
+            reduce_slots_store(slot_ptr, nseg, min(BT, p.M - t0), nt * 128, p.N, A4 ? nullptr : p.s, t0, p.c,
                                p.ldc, ew * 32 + lane, 128);
           } else {
             const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (128 * BT);
-            reduce_partials_store<BT>(base, p.splits, min(BT, p.M - t0), nt * 128, p.N, A4 ? nullptr : (fused ? s_buf : p.s), t0,
+            reduce_partials_store<BT>(base, p.splits, min(BT, p.M - t0), nt * 128, p.N, A4 ? nullptr : p.s, t0,
                                       p.c, p.ldc, ew * 32 + lane, 128);
           }
         }
@@ -1277,14 +1114,10 @@ __global__ void __launch_bounds__(Cfg<BT, A4>::kThreads, 1) __maxnreg__((Cfg<BT,
   if (p.cluster) cluster_sync_all();
 }
 
-// x != nullptr (16-token W4A8 tiles only): fused per-token quantization of
-// the bf16 activations x [M][ldx]; q and s are then unused.
 template <int BT, bool A4>
 int launch_bt(const uint8_t *q, const float *s, const uint8_t *xsf, const uint8_t *packed, int64_t M, int64_t N,
-              int64_t K, uint16_t *c, int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st,
-              const uint16_t *x = nullptr, int64_t ldx = 0) {
+              int64_t K, uint16_t *c, int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st) {
   using C = Cfg<BT, A4>;
-  if (x && !C::kFuseQ) return R4_ERR_INVALID_ARG;
   const int64_t NT = ceil_div(N, 128);
   CUtensorMap tm_w, tm_x, tm_c;
   if constexpr (A4) {
@@ -1314,16 +1147,7 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *xsf, const uint8_
                        box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return R4_ERR_CUDA;
     }
-    if (x) {
-      // bf16 activation blocks of 16 rows x 128 columns, unswizzled (the
-      // producers quantize them into the stages)
-      const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
-      const uint64_t strides[1] = {static_cast<uint64_t>(ldx) * 2};
-      const uint32_t box[2] = {128, 16};
-      if (encode_tiled(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
-        return R4_ERR_CUDA;
-    } else {
+    {
       const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
       const uint64_t strides[1] = {static_cast<uint64_t>(K)};
       const uint32_t box[2] = {128, static_cast<uint32_t>(BT)};
@@ -1350,10 +1174,6 @@ int launch_bt(const uint8_t *q, const float *s, const uint8_t *xsf, const uint8_
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.KB = pl.KB;
-  p.K = static_cast<int>(K);
-  p.x = x;
-  p.ldx = ldx;
-  p.fuse_q = x ? 1 : 0;
   p.xsf = xsf;
   p.xatoms = static_cast<int>(mx_act_tokens_padded(M) / 128);
   p.t_tiles = pl.t_tiles;
@@ -1664,14 +1484,6 @@ int launch_gemm_w4a8(const uint8_t *q, const float *s, const uint8_t *packed, in
     case 256: return w4a8::launch_bt<256, false>(q, s, nullptr, packed, M, N, K, c, ldc, ws, pl, st);
     default: return R4_ERR_INVALID_ARG;
   }
-}
-
-// Per-token quantization fused into the 16-token W4A8 tile (pl.BT == 16, no
-// cluster or stream-K schedule; the caller checks).
-int launch_linear_w4a8_fused(const uint16_t *x, int64_t ldx, const uint8_t *packed, int64_t M, int64_t N, int64_t K,
-                             uint16_t *c, int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st) {
-  if (pl.BT != 16 || pl.cluster || pl.sk) return R4_ERR_INVALID_ARG;
-  return w4a8::launch_bt<16, false>(nullptr, nullptr, nullptr, packed, M, N, K, c, ldc, ws, pl, st, x, ldx);
 }
 
 int launch_gemm_w4a4(const uint8_t *q, const uint8_t *q_scale, const uint8_t *packed, int64_t M, int64_t N,

@@ -570,8 +570,7 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
 
 // Split-K epilogue of the last-arriving CTA: sum `nslots` fp32 partial tiles
 // (each [tokens][128 n], n contiguous; slot(s) is the s-th) in s order --
-// deterministic -- and store bf16(scale[t] * sum) (scale == nullptr: 1; a
-// global or a shared-memory array) into
+// deterministic -- and store bf16(scale[t] * sum) (scale == nullptr: 1) into
 // C[t0 + t][n0 + n] for t < tmax, n0 + n < N. The loads are independent L2
 // reads (.cg: the partials were written by other SMs), four n per thread.
 template <int U = 4, int S = 4, class SlotFn>
@@ -622,7 +621,7 @@ __device__ __forceinline__ void reduce_slots_store(SlotFn slot, int nslots, int 
       const int idx = base + k * nthreads;
       if (idx >= total) continue;
       const int tl = idx >> 5, n4 = (idx & 31) * 4;
-      const float sc = scale ? scale[t0 + tl] : 1.f;   // global or shared (generic load)
+      const float sc = scale ? __ldg(scale + t0 + tl) : 1.f;
       const int n = n0 + n4;
       uint16_t *dst = c + static_cast<size_t>(t0 + tl) * ldc + n;
       const float vals[4] = {acc[k].x * sc, acc[k].y * sc, acc[k].z * sc, acc[k].w * sc};

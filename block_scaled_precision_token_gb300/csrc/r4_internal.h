@@ -41,7 +41,6 @@ struct Options {
   int row_split = 0;        // row-wise quantizers: CTAs per row (0 = automatic, else 1/2/4/8)
   int row_threads = 0;      // row-wise quantizers: threads per CTA at most (0 = automatic, else 64/128/256)
   int skinny_groups = 0;    // skinny GEMM: 16-token groups per CTA (0 = automatic, else 1..4)
-  int fuse_quant = 0;       // r4_linear_w4a8_mxfp4: quantize inside the 16-token GEMM tile (1) or launch the quantizer (0)
   int stream_k = 0;         // W4A8/W4A4 decode tiles: stream-K schedule 0 never (default), 1 when the model gains, 2 always
 };
 Options &options();
@@ -124,9 +123,9 @@ inline size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
 constexpr size_t kCounterBytes = 16384;
 constexpr int64_t kMaxCounterTiles = static_cast<int64_t>(kCounterBytes / 4);
 // r4_linear_w4a8_mxfp4's own part of its workspace: the e4m3 codes [M][K]
-// and the token scales [M] of its two-launch path. It follows the GEMM's
-// part, which always reserves the counter region (so that this transient
-// scratch never lands on another call's counters).
+// and the token scales [M]. It follows the GEMM's part, which always
+// reserves the counter region (so that this transient scratch never lands
+// on another call's counters).
 inline size_t linear_scratch_bytes(int64_t M, int64_t K) {
   return round_up(static_cast<size_t>(M) * static_cast<size_t>(K), 256) + round_up(static_cast<size_t>(M) * 4, 256);
 }
@@ -175,8 +174,6 @@ cudaError_t launch_prepack_mxfp4(const uint8_t *w, const uint8_t *ws, int64_t N,
 cudaError_t launch_prepack_blockfp8(const uint8_t *w, const float *ws, int64_t N, int64_t K, uint8_t *packed,
                                    cudaStream_t st);
 // Returns an r4_status (tensor-map encoding can fail with R4_ERR_CUDA).
-int launch_linear_w4a8_fused(const uint16_t *x, int64_t ldx, const uint8_t *packed, int64_t M, int64_t N, int64_t K,
-                             uint16_t *c, int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st);
 int launch_gemm_w4a8(const uint8_t *q, const float *s, const uint8_t *packed, int64_t M, int64_t N, int64_t K,
                      uint16_t *c, int64_t ldc, void *ws, const GemmPlan &plan, cudaStream_t st);
 int launch_gemm_w4a4(const uint8_t *q, const uint8_t *q_scale, const uint8_t *packed, int64_t M, int64_t N,

@@ -351,8 +351,7 @@ def workspace(op, M, N, K, device="cuda"):
 
 def linear_w4a8(x, packed, N, K, ws=None, out=None, stream=None):
     """bf16 activations x [M, K] (row stride x.stride(0)) -> bf16 [M, N]:
-    per-token quantization and the W4A8 GEMM in one call (one kernel for
-    M <= 16 with option 17 = 1)."""
+    per-token quantization and the W4A8 GEMM in one call."""
     M = x.shape[0]
     c = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if out is None else out
     if ws is None:

@@ -301,21 +301,15 @@ int r4_gemm_w4a8_mxfp4(const uint8_t *q, const float *s, const void *packed, int
  * the same result bit for bit.
  * Source: "radiance_mxfp4.py", module docstring (per-token FP8 activations
  * feeding the W4A8 GEMM) and _traced_quant (the quantization rule).
- * By default it runs the quantization kernel into the workspace and then the
- * GEMM (two launches). With option 17 = 1 and M <= 16 (one 16-token tile,
- * x 16-byte aligned) the quantization runs inside the GEMM kernel instead
- * (one launch): each CTA computes the token scales over the whole rows and
- * quantizes the bf16 block of every pipeline stage itself. Measured on GB300
- * in CUDA graphs that one launch is slower than the two (each CTA redoes the
- * row maxima and the quantization of the blocks it streams), so it is off.
- *   x        bf16 [M, ldx] row-major, ldx >= K, ldx % 8 == 0; 16-B aligned
- *            for the fused path (else the two-launch path runs).
+ * It runs the quantization kernel into the workspace and then the GEMM (two
+ * launches, the second under programmatic dependent launch).
+ *   x        bf16 [M, ldx] row-major, ldx >= K, ldx % 8 == 0, 16-byte aligned.
  *   packed   prepacked weight from r4_prepack_mxfp4(N, K).
  *   c        bf16 [M, ldc] row-major; columns [0, N) are written, nothing else.
  *   workspace  r4_gemm_workspace_bytes(R4_OP_LINEAR_W4A8_MXFP4, M, N, K)
  *            bytes, 256-byte aligned, counters zeroed once: the GEMM's
  *            workspace (counter region always reserved), then room for the
- *            quantized activations of the two-launch path.
+ *            quantized activations and their scales.
  * Requirements: M >= 1, N >= 1, K % 32 == 0, K >= 128, ldc >= N. Errors as
  * r4_gemm_w4a8_mxfp4 (R4_ERR_WORKSPACE for a missing or short workspace).
  */
@@ -439,8 +433,6 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * setting the option. (Measured on GB300 it is slower than the default
  * schedule on the decode shapes; it is an option for other shapes and
  * GPUs.)
- * key 17: r4_linear_w4a8_mxfp4 quantizes inside the GEMM kernel when it can
- * (1) or always runs the quantization kernel first (0, default).
  */
 int r4_set_option(int key, int64_t value);
 

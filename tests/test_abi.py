@@ -52,8 +52,6 @@ def test_options(r4q):
     assert lib.r4_set_option(2, 160) == r4q.R4_ERR_INVALID_ARG
     assert lib.r4_set_option(16, 3) == r4q.R4_ERR_INVALID_ARG and lib.r4_set_option(16, -1) == r4q.R4_ERR_INVALID_ARG
     assert lib.r4_set_option(16, 2) == 0 and lib.r4_set_option(16, 1) == 0 and lib.r4_set_option(16, 0) == 0
-    assert lib.r4_set_option(17, 2) == r4q.R4_ERR_INVALID_ARG and lib.r4_set_option(17, -1) == r4q.R4_ERR_INVALID_ARG
-    assert lib.r4_set_option(17, 0) == 0 and lib.r4_set_option(17, 1) == 0
     assert lib.r4_set_option(1, 0) == 0 and lib.r4_set_option(3, 0) == 0
 
 

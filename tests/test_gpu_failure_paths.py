@@ -42,7 +42,6 @@ def r4q():
     m.r4_set_option(2, 0)
     m.r4_set_option(3, 0)
     m.r4_set_option(6, 1)
-    m.r4_set_option(17, 0)
 
 
 def _w4a8_inputs(r4q, M, N, K):
@@ -135,18 +134,18 @@ def _blockfp8_inputs(r4q, M, N, K):
     return torch.from_numpy(q).cuda(), torch.from_numpy(As).cuda(), pk, (q, As, wq, Ws)
 
 
-@pytest.mark.parametrize("op", ["w4a8", "w4a8_stream_k", "blockfp8", "linear_fused"])
+@pytest.mark.parametrize("op", ["w4a8", "w4a8_stream_k", "blockfp8", "linear"])
 def test_expired_wait_leaves_the_workspace_reusable(r4q, op):
     """Split-K through the caller's workspace (forced: 4 splits, no cluster
     exchange; or the stream-K schedule, where every tile is shared by eight
     CTAs of one K block each). The first CTA's stalled unit never writes its
     partial; the launch must still end with every arrival counter at zero,
-    and the next call on the same workspace must match the oracle. The
-    fused-quantization linear call stalls in its own producer (CTA 0 never
-    marks its first activation tile written)."""
+    and the next call on the same workspace must match the oracle (for the
+    linear call: its GEMM, whose counters lead the workspace, before the
+    quantized activations)."""
     M, N, K = 8, 512, 1024
     tiles = (N // 128) * 1                       # 16-token tiles: one token tile
-    if op == "linear_fused":
+    if op == "linear":
         x = synth.activations(M, K, synth.CFG_DECODE, outliers=True)
         w = synth.weights_fp32(N, K, synth.CFG_DECODE)
         p, sc = Q.quant_mxfp4_ocp(w.numpy())
@@ -156,7 +155,6 @@ def test_expired_wait_leaves_the_workspace_reusable(r4q, op):
         cd = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         r4q.r4_set_option(1, 4)
         r4q.r4_set_option(6, 0)
-        r4q.r4_set_option(17, 1)                 # the fused path (one launch)
         opid = r4q.R4_OP_LINEAR_W4A8_MXFP4
 
         def call(ws):
@@ -201,7 +199,6 @@ def test_expired_wait_leaves_the_workspace_reusable(r4q, op):
         r4q.r4_set_option(3, 0)
         r4q.r4_set_option(6, 1)
         r4q.r4_set_option(16, 0)
-        r4q.r4_set_option(17, 0)
     assert_gemm_matches(c, exact(), f"{op} after the stalled launch, reused workspace")
 
 
@@ -243,11 +240,7 @@ def test_every_entry_point_captures_in_a_graph(r4q):
         r4q.r4_quant_fp8_per_token(x, M, K, K, 128, qg, sg)
         r4q.r4_gemm_w4a8_mxfp4(q, s, pk, M, N, K, c1, N, ws1)
         r4q.r4_linear_w4a8_mxfp4(x, K, pk, M, N, K, c5, N, ws3)             # quantizer + GEMM
-        r4q.r4_set_option(17, 1)
-        try:
-            r4q.r4_linear_w4a8_mxfp4(x[:M - 1], K, pk, M - 1, N, K, c6, N, ws3)  # one fused launch, 15 tokens
-        finally:
-            r4q.r4_set_option(17, 0)
+        r4q.r4_linear_w4a8_mxfp4(x[:M - 1], K, pk, M - 1, N, K, c6, N, ws3)  # 15 tokens, same workspace
         r4q.r4_gemm_blockfp8(qg, sg, pk8, M, N, K, c2, N, ws2)
         r4q.r4_gemm_bf16_nt_skinny(x, wb, M, 256, K, c3, 256)
         r4q.r4_add_rmsnorm_quant_fp8(x, res, nw, 1e-6, M, K, ro, q2, s2)
