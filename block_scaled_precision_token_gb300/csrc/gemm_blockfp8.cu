@@ -7,8 +7,8 @@
 //
 // The scales are arbitrary fp32, so the tensor core cannot apply them (its
 // block-scale kinds take power-of-two ue8m0 scales only). Instead:
-//  * weight-stationary orientation: a 128-row weight tile is exactly one
-//    scale block along N, so Ws[n/128, kb] is one scalar per tile per K block;
+//  * a 128-row weight tile is exactly one scale block along N, so
+//    Ws[n/128, kb] is one scalar per tile per K block;
 //  * every 128-K block is its own "slot": 4 MMAs (K = 32 each) write a FRESH
 //    fp32 accumulator in tensor memory. Slot g uses accumulator buffer
 //    g % kNumBuf; with 512 columns there are 4 (BT = 128) to 16 buffers, so
@@ -32,7 +32,11 @@
 //    -- at 50 us for M=2048, N=6144, K=2048, 37 us without it.)
 //  * decode tiles (BT <= 64) run two TMA producer warps: one thread issuing
 //    every weight and activation copy caps the weight stream (each TMA issue
-//    holds its thread for a few hundred cycles on GB300).
+//    holds its thread for a few hundred cycles on GB300);
+//  * the per-K-block handshakes (block result ready, accumulator free, stage
+//    full) spin on a non-blocking mbarrier test, bounded like every wait;
+//  * unsplit tiles of 32- and 64-column warps store through shared memory
+//    and TMA tensor stores, so the next unit's promotion starts at once.
 // Split-K and the last-arriving-CTA reduction are as in the W4A8 kernel.
 
 #include <cuda_bf16.h>
