@@ -1354,6 +1354,13 @@ static GemmPlan plan_mx_bt(int64_t M, int64_t N, int64_t K, int sms, bool a4, in
     int ncl = (options().cluster_split && bt >= 32 && s >= 2 && s <= 6) ? w4a8::max_clusters(bt, s, a4) : 0;
     if (bt >= 128 && !forced_s && tiles > ncl) ncl = 0;
     if (bt >= 128 && !forced_s && s > 1 && ncl == 0 && !prefill_ws_ok) continue;
+    // Prefill tiles split only while every CTA holds at most one split unit
+    // (forced factors included; otherwise the schedule stays unsplit). The
+    // split paths with several split units per CTA are not run on prefill
+    // tiles: a timing sweep of forced factors at M=256, 34816x5120 (272
+    // tiles) ended in an illegal-address error whose cause was not found.
+    if (bt >= 128 && s > 1 && units > (ncl > 0 ? std::min<int64_t>(tiles, ncl) * s : static_cast<int64_t>(sms)))
+      continue;
     double t;
     int64_t grid;
     if (ncl > 0) {
