@@ -30,7 +30,7 @@ pytestmark = pytest.mark.gpu
 # producer's end-of-kernel drain of that same stage (this small shape's
 # slots are all issued before the producer's loop, so it reaches its drain
 # at once). The first to record wins the error word.
-WAIT_FULL, WAIT_ACC_FULL, WAIT_DRAIN = 1, 3, 5
+WAIT_FULL, WAIT_EMPTY, WAIT_ACC_FULL, WAIT_ACC_EMPTY, WAIT_DRAIN = 1, 2, 3, 4, 5
 
 
 @pytest.fixture(scope="module")
@@ -123,6 +123,44 @@ def test_prefill_stall_reports_and_recovers(r4q, mode, bt):
         r4q.r4_set_option(1, 0)
         r4q.r4_set_option(2, 0)
     assert_gemm_matches(c[:, torch.from_numpy(rows).cuda()], exact(), f"{mode} bt={bt} after the stalled launch")
+
+
+def test_blockfp8_prefill_stall_reports_and_recovers(r4q):
+    """The block-FP8 128-token tile (token-major accumulator, spinning
+    per-K-block handshakes, TMA-stored output): CTA 0 withholds its first
+    activation copy. The spinning waits are bounded like the others: they
+    must expire and return, the error must be reported, and the next call
+    must give the oracle's result. K = 512 keeps every slot within the ring,
+    so the producer reaches its drain at once."""
+    M, N, K = 300, 768, 512
+    x = synth.activations(M, K, synth.CFG_BLOCKFP8)
+    w = synth.weights_fp32(N, K, synth.CFG_BLOCKFP8)
+    wq, Ws = Q.quant_blockfp8_w(w.numpy())
+    q, As = Q.quant_act(x.float().numpy(), group=128)
+    pk = r4q.prepack_blockfp8(torch.from_numpy(wq).cuda(), torch.from_numpy(Ws).cuda(), N, K)
+    qd, Ad = torch.from_numpy(q).cuda(), torch.from_numpy(As).cuda()
+    r4q.r4_set_option(3, 1)
+    try:
+        r4q.r4_device_error(clear=True)
+        r4q.r4_set_option(10, 1)
+        try:
+            t0 = time.time()
+            r4q.gemm_blockfp8(qd, Ad, pk, N, K)
+            torch.cuda.synchronize()
+            elapsed = time.time() - t0
+        finally:
+            r4q.r4_set_option(10, 0)
+        code = r4q.r4_device_error(clear=True)
+        assert code in (WAIT_FULL, WAIT_EMPTY, WAIT_ACC_FULL, WAIT_ACC_EMPTY, WAIT_DRAIN), f"device error word {code}"
+        assert 1.0 < elapsed < 30.0, f"the stalled launch took {elapsed:.1f} s"
+        c = r4q.gemm_blockfp8(qd, Ad, pk, N, K)
+        torch.cuda.synchronize()
+        assert r4q.r4_device_error(clear=True) == 0
+    finally:
+        r4q.r4_set_option(3, 0)
+    assert r4q.r4_last_kernel_name() == "blockfp8_f8f6f4_kernel<128>"
+    c64, _ = G.gemm_blockfp8(q, As, wq, Ws)
+    assert_gemm_matches(c, c64, "block-FP8 128-token tile after the stalled launch")
 
 
 def _blockfp8_inputs(r4q, M, N, K):
