@@ -181,6 +181,10 @@ int r4_set_option(int key, int64_t value) {
       options().w4a8_token_tile = static_cast<int>(value);
       return R4_OK;
     case 3: options().fp8_splits = static_cast<int>(value); return R4_OK;
+    case 8:
+      if (value != 0 && value != 128 && value != 256) return R4_ERR_INVALID_ARG;
+      options().fp8_n_tile = static_cast<int>(value);
+      return R4_OK;
     case 4: options().pdl = value ? 1 : 0; return R4_OK;
     case 14: options().early_weights = value ? 1 : 0; return R4_OK;
     case 15:
@@ -196,7 +200,6 @@ int r4_set_option(int key, int64_t value) {
       options().l2_prefetch = static_cast<int>(value);
       return R4_OK;
     case 6: options().cluster_split = value ? 1 : 0; return R4_OK;
-    case 9: options().fp8_stage_scales = value ? 1 : 0; return R4_OK;
     case 10: options().inject_stall = value ? 1 : 0; return R4_OK;
     case 13:
       if (value != 0 && value != 64 && value != 128 && value != 256) return R4_ERR_INVALID_ARG;

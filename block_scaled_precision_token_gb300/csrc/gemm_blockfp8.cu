@@ -7,19 +7,21 @@
 //
 // The scales are arbitrary fp32, so the tensor core cannot apply them (its
 // block-scale kinds take power-of-two ue8m0 scales only). Instead:
-//  * a 128-row weight tile is exactly one scale block along N, so
-//    Ws[n/128, kb] is one scalar per tile per K block;
+//  * a 128-row weight block is exactly one scale block along N, so
+//    Ws[n/128, kb] is one scalar per 128 rows per K block (the 128-token
+//    tile takes two such blocks, 256 rows, when N allows);
 //  * every 128-K block is its own "slot": 4 MMAs (K = 32 each) write a FRESH
 //    fp32 accumulator in tensor memory. Slot g uses accumulator buffer
-//    g % kNumBuf; with 512 columns there are 4 (BT = 128) to 16 buffers, so
-//    the MMAs run several K blocks ahead of the promotion epilogue;
+//    g % kNumBuf; with 512 columns there are 2 (256 weight rows) to 16
+//    buffers, so the MMAs run ahead of the promotion epilogue;
 //  * 4 x kH epilogue warps (one per tensor-memory lane quarter and column
 //    group) load each block result and fold it into fp32 registers. Tiles of
 //    up to 64 tokens keep the weights on the lanes, 32 (or 16) token columns
 //    per warp: acc[t] += As[t,kb] * (Ws[nt,kb] * D_kb[n,t]), the scaling and
 //    the accumulation each one packed f32x2 instruction per two columns. The
 //    128-token tile puts the tokens on the lanes (see Cfg::kTokMajor), eight
-//    warps of 64 n columns: acc[n] += (As[t,kb] * Ws[nt,kb]) * D_kb[t,n];
+//    warps of 128 (or 64) n columns: acc[n] += (As[t,kb] * Ws[n/128,kb]) *
+//    D_kb[t,n];
 //  * the scales reach the epilogue without a handshake per K block: the
 //    epilogue threads themselves copy As and Ws for a chunk of 16 K blocks
 //    of their tile into shared memory (As transposed, [kb][token], so a
@@ -70,27 +72,48 @@ struct Params {
   int *err;
 };
 
-template <int BT>
+template <int BT, int BN = 128>
 struct Cfg {
   static constexpr int kProd = BT <= 64 ? 2 : 1;           // TMA producer warps
   static constexpr int kMmaWarp = kProd;                   // first MMA-issuing warp
   static constexpr int kMma = 2;                           // MMA-issuing warps (slot g: warp g % kMma)
   static constexpr int kEpiWarp0 = kProd + kMma;
-  // accumulator columns per epilogue warp: 64 n for the token-major 128-token
-  // tile (eight warps), else 32 (or BT) tokens
-  static constexpr int kCW = BT == 128 ? 64 : (BT < 32 ? BT : 32);
-  static constexpr int kH = BT / kCW;                      // column groups
+  // 128-token tiles accumulate token-major: the activation tile is the MMA's
+  // A operand (tensor-memory lane = token) and the weight tile its B operand
+  // (column = n), so each thread's scale for a K block is the single product
+  // As[t,kb] * Ws[n/128,kb] -- one FMA per element -- and its outputs are
+  // contiguous in a row of C. Narrower tiles keep the weights on the lanes
+  // (the MMA needs 128 rows).
+  static constexpr bool kTokMajor = BT == 128;
+  // Weight rows per tile: 128, or 256 for the token-major tile (two 128-row
+  // scale blocks side by side; one N = 256 MMA per K step).
+  static constexpr int kNB = BN / 128;                     // 128-row weight blocks per tile
+  static constexpr int kAccCols = kTokMajor ? BN : BT;     // accumulator columns (the MMA's N)
+  // accumulator columns per epilogue warp: the token-major tile's n columns
+  // in two groups (eight warps), else 32 (or BT) tokens. (Sixteen warps of
+  // 64 columns for the 256-row tile, at 96 registers: 13 % slower.)
+  static constexpr int kCW = kTokMajor ? kAccCols / 2 : (BT < 32 ? BT : 32);
+  static constexpr int kH = kAccCols / kCW;                // column groups
   static constexpr int kEpiWarps = 4 * kH;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
-  static constexpr int kMaxReg = BT == 128 ? 168 : (kThreads > 576 ? 96 : 128);
-  static constexpr int kNumBufRaw = 512 / BT;
+  // A scheduler's 16384 registers serve every warp placed on it (warps are
+  // spread over the SM's four schedulers), in steps of 8 a thread.
+  static constexpr int kWarpsPerSched = (kThreads / 32 + 3) / 4;
+  static constexpr int kRegLimit = (16384 / (32 * kWarpsPerSched)) / 8 * 8;
+  static constexpr int kMaxReg = kTokMajor ? (kRegLimit > 168 ? 168 : kRegLimit) : (kThreads > 576 ? 96 : 128);
+  // Token-major promotion: all loads of a K block, then one wait, when the
+  // registers hold a second copy of the accumulators; else 16-column loads,
+  // each waited for (the registers hold the accumulators and one load).
+  static constexpr bool kLdAll = kCW * 2 + 40 <= kMaxReg;
+  static constexpr int kNumBufRaw = 512 / kAccCols;
   static constexpr int kNumBuf = kNumBufRaw > kMaxBuf ? kMaxBuf : kNumBufRaw;
-  static constexpr uint32_t kTmemCols = static_cast<uint32_t>(kNumBuf * BT);
+  static constexpr uint32_t kTmemCols = static_cast<uint32_t>(kNumBuf * kAccCols);
+  static constexpr uint32_t kWBytes = kNB * kWSmem;         // weight part of a stage
   static constexpr uint32_t kXSmem = BT * 128;
-  static constexpr uint32_t kStageBytes = ((kWSmem + kXSmem + 1023) / 1024) * 1024;
-  // scale chunks: 2 buffers of As [kChunk][BT] and Ws [kChunk]
-  static constexpr uint32_t kScFloats = kChunk * BT + kChunk;
+  static constexpr uint32_t kStageBytes = ((kWBytes + kXSmem + 1023) / 1024) * 1024;
+  // scale chunks: 2 buffers of As [kChunk][BT] and Ws [kNB][kChunk]
+  static constexpr uint32_t kScFloats = kChunk * BT + kChunk * kNB;
   static constexpr uint32_t kScBytes = 2 * kScFloats * 4;
   static constexpr int kScPer = (BT * kChunk + kEpiThreads - 1) / kEpiThreads;   // As values per thread
   static constexpr uint32_t kMiscBytes = 1024;             // barriers and flags
@@ -99,13 +122,6 @@ struct Cfg {
   // the warp and handed to a TMA tensor store, so the next unit's promotion
   // starts without waiting for global stores.
   static constexpr bool kTmaOut = kCW >= 32;
-  // 128-token tiles accumulate token-major: the activation tile is the MMA's
-  // A operand (tensor-memory lane = token) and the weight tile its B operand
-  // (column = n), so each thread's scale for a K block is the single product
-  // As[t,kb] * Ws[nt,kb] -- one FMA per element -- and its 32 outputs are
-  // contiguous in a row of C. Narrower tiles keep the weights on the lanes
-  // (the MMA needs 128 rows).
-  static constexpr bool kTokMajor = BT == 128;
   static constexpr int kRedU = BT == 128 ? 1 : 4;          // split-K reduction unroll (registers)
   static constexpr uint32_t kOutBytes = kTmaOut ? static_cast<uint32_t>(kEpiWarps * kCW) * 64u : 0u;
   static constexpr int kStagesRaw =
@@ -119,11 +135,14 @@ struct Cfg {
   // slot g + kStages - kNumBuf >= g back from the epilogue, so that barrier
   // cannot run a phase ahead of the epilogue's wait.
   static constexpr bool kFullIsEmpty = kStages >= kNumBuf;
-  static constexpr uint32_t kTxBytes = kWSmem + kXSmem;
+  static constexpr uint32_t kTxBytes = kWBytes + kXSmem;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kOutBytes + kScBytes + kMiscBytes + 1024;
   static_assert(kTmemCols >= 32 && (kTmemCols & (kTmemCols - 1)) == 0, "tensor-memory allocation");
   static_assert(kThreads <= 1024, "block size");
   static_assert(kStages >= kProd, "stage count");
+  static_assert(BN == 128 || (BN == 256 && kTokMajor), "256-row weight tiles only with the token-major tile");
+  static_assert(!kTokMajor || kCW % 16 == 0, "epilogue columns");
+  static_assert(kSmemBytes <= 227u * 1024u, "shared memory");
 };
 
 // Walks the K-block slots of this CTA's units in order.
@@ -176,6 +195,17 @@ struct ChunkCursor {
   }
 };
 
+// tcgen05.wait::ld that also names the loaded registers as its operands, so
+// no use of them can be scheduled before the wait.
+__device__ __forceinline__ void wait_ld_into(uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+        "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+      :
+      : "memory");
+}
+
 // 4-byte asynchronous copy global -> shared; src_bytes = 0 writes zero.
 __device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
@@ -184,12 +214,13 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t s
 
 // Copies one scale chunk into `buf` with cp.async (no registers held while
 // it is in flight): As transposed, buf[i * BT + t] = As[t0 + t, kb + i], then
-// buf[kChunk * BT + i] = Ws[nt, kb + i]; 0 past M or past the chunk. Element
+// buf[kChunk * BT + h * kChunk + i] = Ws[nt * kNB + h, kb + i]; 0 past M or
+// past the chunk. Element
 // r of thread e is (t, i) = divmod(e + kEpiThreads * r, kChunk): consecutive
 // threads walk a token's 16 consecutive K blocks (64 contiguous bytes).
-template <int BT>
+template <int BT, int BN>
 __device__ __forceinline__ void copy_scale_chunk(const Params &p, const ChunkCursor &ch, float *buf, int e) {
-  using C = Cfg<BT>;
+  using C = Cfg<BT, BN>;
   const int n = ch.len();
   const int t0 = ch.tt * BT;
 #pragma unroll
@@ -201,20 +232,22 @@ __device__ __forceinline__ void copy_scale_chunk(const Params &p, const ChunkCur
       cp_async4(buf + i * BT + t, in ? p.As + static_cast<size_t>(t0 + t) * p.KB + ch.kb + i : p.As, in ? 4u : 0u);
     }
   }
-  if (e < kChunk)
-    cp_async4(buf + kChunk * BT + e, e < n ? p.Ws + static_cast<size_t>(ch.nt) * p.KB + ch.kb + e : p.Ws,
-              e < n ? 4u : 0u);
+  if (e < kChunk * C::kNB) {
+    const int h = e / kChunk, i = e - h * kChunk;
+    cp_async4(buf + kChunk * BT + e,
+              i < n ? p.Ws + static_cast<size_t>(ch.nt * C::kNB + h) * p.KB + ch.kb + i : p.Ws, i < n ? 4u : 0u);
+  }
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-template <int BT>
-__global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kMaxReg))
+template <int BT, int BN>
+__global__ void __launch_bounds__(Cfg<BT, BN>::kThreads, 1) __maxnreg__((Cfg<BT, BN>::kMaxReg))
     blockfp8_f8f6f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                            const __grid_constant__ CUtensorMap tm_c, const Params p) {
-  using C = Cfg<BT>;
+  using C = Cfg<BT, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *outbuf = smem + C::kStages * C::kStageBytes;                         // [kEpiWarps][32][32] bf16
+  uint8_t *outbuf = smem + C::kStages * C::kStageBytes;                         // [kEpiWarps][32][kCW] bf16
   float *scbuf = reinterpret_cast<float *>(outbuf + C::kOutBytes);              // [2][kScFloats]
   uint8_t *misc = reinterpret_cast<uint8_t *>(scbuf) + C::kScBytes;
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(misc);   // [kMaxStages]
@@ -274,7 +307,10 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
         for (int g = 0; cu.valid(p) && g < C::kStages; ++g, cu.next(p))
           if (g % C::kProd == pw) {
             mbar_arrive_expect_tx(&full_bar[g], C::kTxBytes);
-            tma_load_3d(smem + g * C::kStageBytes, &tm_w, &full_bar[g], 0, 0, cu.nt * p.KB + cu.kb, pol_w);
+#pragma unroll
+            for (int h = 0; h < C::kNB; ++h)
+              tma_load_3d(smem + g * C::kStageBytes + h * kWSmem, &tm_w, &full_bar[g], 0, 0,
+                          (cu.nt * C::kNB + h) * p.KB + cu.kb, pol_w);
           }
       }
       pdl_wait();
@@ -288,12 +324,14 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
         if (g >= C::kStages) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, DEV_ERR_WAIT_EMPTY)) break;
           mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
-          tma_load_3d(st, &tm_w, &full_bar[stage], 0, 0, cu.nt * p.KB + cu.kb, pol_w);
+#pragma unroll
+          for (int h = 0; h < C::kNB; ++h)
+            tma_load_3d(st + h * kWSmem, &tm_w, &full_bar[stage], 0, 0, (cu.nt * C::kNB + h) * p.KB + cu.kb, pol_w);
         }
         // (Failure-detection test: with inject_stall, CTA 0 never issues its
         // first activation copy, so the stage's transaction never completes.)
         if (!(p.inject_stall && blockIdx.x == 0 && g == 0))
-          tma_load_2d(st + kWSmem, &tm_x, &full_bar[stage], cu.kb * 128, cu.tt * BT, pol_x);
+          tma_load_2d(st + C::kWBytes, &tm_x, &full_bar[stage], cu.kb * 128, cu.tt * BT, pol_x);
         // Record the newest phase of every stage: a parity wait cannot tell
         // phase k from k + 2, and a stage only advances once its earlier
         // phases completed.
@@ -318,7 +356,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
     // left the pipe idle during ~400-700 cycles of per-slot handshake.)
     const int mw = warp - C::kMmaWarp;
     if (lane == 0) {
-      const uint32_t idesc = idesc_f8f6f4_e4m3(BT);
+      const uint32_t idesc = idesc_f8f6f4_e4m3(C::kAccCols);
       SlotCursor cu;
       cu.start(p);
       for (int g = 0; cu.valid(p); ++g, cu.next(p)) {
@@ -331,9 +369,9 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
         if (!mbar_spin_wait(&full_bar[stage], phase, abort_flag, p.err, DEV_ERR_WAIT_FULL)) break;
         tc_fence_after();
         uint8_t *st = smem + stage * C::kStageBytes;
-        const uint32_t w_base = smem_u32(st), x_base = smem_u32(st + kWSmem);
+        const uint32_t w_base = smem_u32(st), x_base = smem_u32(st + C::kWBytes);
         const uint32_t a_base = C::kTokMajor ? x_base : w_base, b_base = C::kTokMajor ? w_base : x_base;
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * BT);
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * C::kAccCols);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_f8f6f4(d_tmem, sdesc_sw128_kmajor(a_base + 32u * kk), sdesc_sw128_kmajor(b_base + 32u * kk), idesc,
@@ -361,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
     {
       ChunkCursor c0;
       c0.start(p);
-      if (c0.valid(p)) copy_scale_chunk<BT>(p, c0, scbuf, e);
+      if (c0.valid(p)) copy_scale_chunk<BT, BN>(p, c0, scbuf, e);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     named_bar_sync(1, C::kEpiThreads);
@@ -373,7 +411,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
     while (cu.valid(p)) {
       const int nt = cu.nt, tt = cu.tt, sp = cu.sp, u = cu.u;
       const int t0 = tt * BT;
-      const int n = nt * 128 + q * 32 + lane;
+      const int n = nt * BN + q * 32 + lane;
       const int tile = nt * p.t_tiles + tt;
       float acc[C::kCW];
 #pragma unroll
@@ -391,7 +429,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
           cn.kb = kbc;
           cn.kb1 = cu.kb1;
           cn.next(p);
-          if (cn.valid(p)) copy_scale_chunk<BT>(p, cn, scbuf + (cur ^ 1) * C::kScFloats, e);
+          if (cn.valid(p)) copy_scale_chunk<BT, BN>(p, cn, scbuf + (cur ^ 1) * C::kScFloats, e);
         }
         const float *sc = scbuf + cur * C::kScFloats;
         for (int i = 0; i < nblk; ++i, ++g, cu.next(p)) {
@@ -405,21 +443,44 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
             continue;
           }
           tc_fence_after();
+          const uint32_t ta = lane_base + static_cast<uint32_t>(buf * C::kAccCols);
+          if constexpr (C::kTokMajor && !C::kLdAll) {
+            // kCW columns in 16-column loads, each waited for; the buffer
+            // is released after the last.
+            // acc[n] += (As[t,kb] * Ws[n/128,kb]) * D[t,n]
+            const float sa = sc[i * BT + q * 32 + lane] * sc[kChunk * BT + (col0 >> 7) * kChunk + i];
+#pragma unroll
+            for (int part = 0; part < C::kCW / 16; ++part) {
+              uint32_t d[16];
+              tc_ld_32x32b_x16h(ta + 16u * part, d);
+              wait_ld_into(d);
+              if (part == C::kCW / 16 - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acce_bar[buf]);
+              }
+#pragma unroll
+              for (int j = 0; j < 16; j += 2)
+                fma_f32x2(acc[16 * part + j], acc[16 * part + j + 1], sa, sa, __uint_as_float(d[j]),
+                          __uint_as_float(d[j + 1]));
+            }
+            continue;
+          }
           uint32_t d[C::kCW > 32 ? C::kCW : 32];
           if constexpr (C::kCW == 64) {
-            tc_ld_32x32b_x32(lane_base + static_cast<uint32_t>(buf * BT), *reinterpret_cast<uint32_t(*)[32]>(&d[0]));
-            tc_ld_32x32b_x32(lane_base + static_cast<uint32_t>(buf * BT) + 32u,
+            tc_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(&d[0]));
+            tc_ld_32x32b_x32(ta + 32u,
                              *reinterpret_cast<uint32_t(*)[32]>(&d[32]));
           } else if constexpr (C::kCW == 32) {
-            tc_ld_32x32b_x32(lane_base + static_cast<uint32_t>(buf * BT), *reinterpret_cast<uint32_t(*)[32]>(&d[0]));
+            tc_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(&d[0]));
           } else {
-            tc_ld_32x32b_x16(lane_base + static_cast<uint32_t>(buf * BT), *reinterpret_cast<uint32_t(*)[32]>(&d[0]));
+            tc_ld_32x32b_x16(ta, *reinterpret_cast<uint32_t(*)[32]>(&d[0]));
           }
           tc_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce_bar[buf]);
-          const float ws = sc[kChunk * BT + i];
+          const float ws = sc[kChunk * BT + (C::kTokMajor ? (col0 >> 7) * kChunk : 0) + i];
           if constexpr (C::kTokMajor) {
             // acc[n] += (As[t,kb] * Ws[kb]) * D[t,n]
             const float sa = sc[i * BT + q * 32 + lane] * ws;
@@ -459,9 +520,9 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
       }
       const int tcol = t0 + col0;
       if constexpr (C::kTokMajor) {
-        // Thread = token t0 + 32q + lane, its 32 values = n nt*128 + col0 + j.
+        // Thread = token t0 + 32q + lane, its kCW values = n nt*BN + col0 + j.
         const int t = t0 + q * 32 + lane;
-        const int nc = nt * 128 + col0;
+        const int nc = nt * BN + col0;
         if (p.splits == 1 && p.tma_store) {
           // [32 tokens][32 n] in the 64-byte swizzle (row r's 16-byte unit u at
           // u ^ ((r >> 1) & 3): conflict-free rows); the store clips tokens past M.
@@ -495,9 +556,9 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
             for (int j = 0; j < C::kCW; ++j) dst[j] = f32_to_bf16_rn(acc[j]);
           }
         } else {
-          // partial tile [token][128 n], as the reduction reads it
-          float4 *part = reinterpret_cast<float4 *>(p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (128 * BT) +
-                                                    (q * 32 + lane) * 128 + col0);
+          // partial tile [n / 128][token][128 n], as the reduction reads it
+          float4 *part = reinterpret_cast<float4 *>(p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (BN * BT) +
+                                                    (col0 >> 7) * (128 * BT) + (q * 32 + lane) * 128 + (col0 & 127));
 #pragma unroll
           for (int j4 = 0; j4 < C::kCW / 4; ++j4)
             part[j4] = make_float4(acc[4 * j4], acc[4 * j4 + 1], acc[4 * j4 + 2], acc[4 * j4 + 3]);
@@ -512,7 +573,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tm_c, ob, nt * 128 + q * 32, tcol);
+          tma_store_2d(&tm_c, ob, nt * BN + q * 32, tcol);
           bulk_commit();
         }
       } else if (p.splits == 1) {
@@ -520,7 +581,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
         for (int j = 0; j < C::kCW; ++j)
           if (tcol + j < p.M) p.c[static_cast<size_t>(tcol + j) * p.ldc + n] = f32_to_bf16_rn(acc[j]);
       } else {
-        float *part = p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (128 * BT);
+        float *part = p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (BN * BT);
 #pragma unroll
         for (int j = 0; j < C::kCW; ++j) part[(col0 + j) * 128 + q * 32 + lane] = acc[j];
       }
@@ -535,11 +596,15 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
         named_bar_sync(2, C::kEpiThreads);
         if (*is_last == 1) {
           __threadfence();
-          const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (128 * BT);
-          // (the 128-token tile runs 19 warps at 96 registers: a lighter
-          // reduction keeps the whole kernel free of spills)
-          reduce_partials_store<BT, C::kRedU, C::kRedU>(base, p.splits, min(BT, p.M - t0), nt * 128, nt * 128 + 128,
-                                                        nullptr, t0, p.c, p.ldc, e, C::kEpiThreads);
+          const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (BN * BT);
+          // (the token-major tile holds its accumulators in up to 128
+          // registers a thread: a lighter reduction keeps it free of spills)
+#pragma unroll 1
+          for (int h = 0; h < C::kNB; ++h)
+            reduce_slots_store<C::kRedU, C::kRedU>(
+                [&](int s2) { return base + static_cast<size_t>(s2) * (BN * BT) + h * (128 * BT); }, p.splits,
+                min(BT, p.M - t0), nt * BN + h * 128, nt * BN + h * 128 + 128, nullptr, t0, p.c, p.ldc, e,
+                C::kEpiThreads);
         }
         if (*is_last && e == 0) p.counters[tile] = 0;
         named_bar_sync(2, C::kEpiThreads);
@@ -565,10 +630,11 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) __maxnreg__((Cfg<BT>::kM
   }
 }
 
-template <int BT>
+template <int BT, int BN>
 int launch_bt(const uint8_t *q, const float *As, const uint8_t *packed, int64_t M, int64_t N, int64_t K,
               uint16_t *c, int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st) {
-  using C = Cfg<BT>;
+  using C = Cfg<BT, BN>;
+  if (N % BN != 0) return R4_ERR_UNSUPPORTED_SHAPE;
   CUtensorMap tm_w, tm_x;
   {
     const uint64_t dims[3] = {128, 128, static_cast<uint64_t>((N / 128) * (K / 128))};
@@ -616,13 +682,14 @@ int launch_bt(const uint8_t *q, const float *As, const uint8_t *packed, int64_t 
   p.counters = reinterpret_cast<int *>(ws);
   p.partials = ws ? reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) + pl.counters_bytes) : nullptr;
   p.err = device_error_word();
-  auto kern = blockfp8_f8f6f4_kernel<BT>;
+  auto kern = blockfp8_f8f6f4_kernel<BT, BN>;
   if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::kSmemBytes) != cudaSuccess) return R4_ERR_CUDA;
   if (launch_pdl(kern, dim3(pl.grid), dim3(C::kThreads), C::kSmemBytes, st, tm_w, tm_x, tm_c, p) != cudaSuccess)
     return R4_ERR_CUDA;
   set_last_kernel(BT == 16   ? "blockfp8_f8f6f4_kernel<16>"
                   : BT == 32 ? "blockfp8_f8f6f4_kernel<32>"
                   : BT == 64 ? "blockfp8_f8f6f4_kernel<64>"
+                  : BN == 256 ? "blockfp8_f8f6f4_kernel<128, 256>"
                              : "blockfp8_f8f6f4_kernel<128>");
   return cudaGetLastError() == cudaSuccess ? R4_OK : R4_ERR_CUDA;
 }
@@ -639,14 +706,24 @@ GemmPlan plan_blockfp8(int64_t M, int64_t N, int64_t K, int sms) {
   // 10.96 us; 4096x4096 14.0 vs 15.5 us).
   if (bt == 0) bt = M <= 16 ? 16 : M <= 64 ? 32 : 128;
   pl.BT = bt;
-  pl.n_tiles = static_cast<int>(N / 128);
+  // Token-major tiles take 256 weight rows when N allows and the 256-row
+  // tiles still occupy half of the SMs: each per-K-block handshake
+  // (accumulator ready, promoted, released) then covers twice the tensor
+  // work. (Measured on GB300, 128 -> 256 rows: M=2048 6144x2048 44.9 ->
+  // 33.6 us, 2048x6144 41.5 -> 30.3, 4096x4096 56.0 -> 40.8; at M=256,
+  // 48 or fewer tiles, 9.6 -> 12.5 us.)
+  int bn = options().fp8_n_tile;
+  if (bn == 0) bn = (N / 256) * ceil_div(M, 128) * 2 >= sms ? 256 : 128;
+  if (bt != 128 || N % 256 != 0) bn = 128;
+  pl.BN = bn;
+  pl.n_tiles = static_cast<int>(N / bn);
   pl.t_tiles = static_cast<int>(ceil_div(M, bt));
   pl.KB = static_cast<int>(K / 128);
   const int64_t tiles = static_cast<int64_t>(pl.n_tiles) * pl.t_tiles;
   const double hbm = 6.0e12, sm_bw = 70e9, sm_flops = 4.5e15 / 152.0, red_bw = 20e9;
-  const double kb_bytes = 128.0 * 128 + 128.0 * bt;
-  const double kb_flops = 2.0 * 128 * bt * 128;
-  const double part_bytes = 128.0 * bt * 4;
+  const double kb_bytes = 128.0 * bn + 128.0 * bt;
+  const double kb_flops = 2.0 * bn * bt * 128;
+  const double part_bytes = static_cast<double>(bn) * bt * 4;
   const int max_s = (bt >= 128 && tiles * 4 >= sms && !options().fp8_splits) ? 1 : std::min(pl.KB, 64);
   int best_s = 1;
   double best_t = 1e30;
@@ -680,7 +757,7 @@ GemmPlan plan_blockfp8(int64_t M, int64_t N, int64_t K, int sms) {
   pl.grid = std::min(pl.units, sms);
   if (pl.splits > 1) {
     pl.counters_bytes = kCounterBytes;
-    pl.ws_bytes = pl.counters_bytes + static_cast<size_t>(pl.units) * 128 * bt * 4;
+    pl.ws_bytes = pl.counters_bytes + static_cast<size_t>(pl.units) * bn * bt * 4;
   }
   return pl;
 }
@@ -688,10 +765,12 @@ GemmPlan plan_blockfp8(int64_t M, int64_t N, int64_t K, int sms) {
 int launch_gemm_blockfp8(const uint8_t *q, const float *As, const uint8_t *packed, int64_t M, int64_t N,
                          int64_t K, uint16_t *c, int64_t ldc, void *ws, const GemmPlan &pl, cudaStream_t st) {
   switch (pl.BT) {
-    case 16: return fp8::launch_bt<16>(q, As, packed, M, N, K, c, ldc, ws, pl, st);
-    case 32: return fp8::launch_bt<32>(q, As, packed, M, N, K, c, ldc, ws, pl, st);
-    case 64: return fp8::launch_bt<64>(q, As, packed, M, N, K, c, ldc, ws, pl, st);
-    case 128: return fp8::launch_bt<128>(q, As, packed, M, N, K, c, ldc, ws, pl, st);
+    case 16: return fp8::launch_bt<16, 128>(q, As, packed, M, N, K, c, ldc, ws, pl, st);
+    case 32: return fp8::launch_bt<32, 128>(q, As, packed, M, N, K, c, ldc, ws, pl, st);
+    case 64: return fp8::launch_bt<64, 128>(q, As, packed, M, N, K, c, ldc, ws, pl, st);
+    case 128:
+      return pl.BN == 256 ? fp8::launch_bt<128, 256>(q, As, packed, M, N, K, c, ldc, ws, pl, st)
+                          : fp8::launch_bt<128, 128>(q, As, packed, M, N, K, c, ldc, ws, pl, st);
     default: return R4_ERR_INVALID_ARG;
   }
 }

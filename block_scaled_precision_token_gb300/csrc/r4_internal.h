@@ -31,7 +31,7 @@ struct Options {
   int w4a8_token_tile = 0;  // 0 = automatic
   int fp8_splits = 0;       // 0 = automatic
   int fp8_token_tile = 0;   // 0 = automatic, else 16/32/64/128
-  int fp8_stage_scales = 1; // block-FP8: activation scales ride with the pipeline stage when possible
+  int fp8_n_tile = 0;       // block-FP8 128-token tiles: weight rows per tile, 0 = automatic, else 128/256
   int inject_stall = 0;     // tests only: the next W4A8 launches withhold one copy (bounded-wait test)
   int pdl = 1;              // launch with programmatic stream serialization
   int early_weights = 1;    // GEMMs read their weight operand before waiting for the preceding kernel
@@ -93,10 +93,11 @@ cudaError_t launch_pdl_cluster(Kern kernel, dim3 grid, dim3 block, size_t smem, 
 }
 
 // ------------------------------------------------------------------ plans
-// One output tile = 128 weight rows (n) x BT tokens (t). A work unit is a
+// One output tile = BN weight rows (n) x BT tokens (t). A work unit is a
 // tile and a contiguous range of 128-K blocks (its split).
 struct GemmPlan {
-  int BT = 0;            // token tile (MMA N)
+  int BT = 0;            // token tile
+  int BN = 128;          // weight rows per tile (block-FP8 token-major tiles: 128 or 256)
   int n_tiles = 0, t_tiles = 0;
   int KB = 0;            // number of 128-K blocks (K padded to 128)
   int splits = 1, kb_per_split = 0;

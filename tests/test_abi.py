@@ -46,6 +46,7 @@ def test_prepack_sizes(r4q):
 def test_options(r4q):
     lib = r4q.lib()
     assert lib.r4_set_option(99, 0) == r4q.R4_ERR_INVALID_ARG
+    assert lib.r4_set_option(9, 1) == r4q.R4_ERR_INVALID_ARG   # unassigned
     assert lib.r4_set_option(2, 48) == r4q.R4_ERR_INVALID_ARG
     assert lib.r4_set_option(2, 64) == 0 and lib.r4_set_option(2, 0) == 0
     assert lib.r4_set_option(2, 192) == 0 and lib.r4_set_option(2, 0) == 0
@@ -170,7 +171,7 @@ def test_validation_of_the_w4a4_entry_points_and_the_probe(r4q):
 def test_row_kernel_options(r4q):
     lib = r4q.lib()
     for key, bad, ok in [(11, 3, 8), (11, 16, 1), (13, 96, 128), (13, 512, 64), (5, 3, 1), (5, -1, 2),
-                         (15, 5, 1), (15, -1, 4)]:
+                         (15, 5, 1), (15, -1, 4), (8, 64, 256), (8, 192, 128)]:
         assert lib.r4_set_option(key, bad) == r4q.R4_ERR_INVALID_ARG
         assert lib.r4_set_option(key, ok) == 0
         assert lib.r4_set_option(key, 0) == 0

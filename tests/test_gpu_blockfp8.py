@@ -17,6 +17,7 @@ def r4q():
     m = require_gpu()
     yield m
     m.r4_set_option(3, 0)
+    m.r4_set_option(8, 0)
 
 
 def _run(r4q, q_np, As_np, w_np, Ws_np, N, K):
@@ -82,6 +83,41 @@ def test_forced_splits_ragged_m(r4q, splits, M):
     c64, _ = G.gemm_blockfp8(q, As, w, Ws)
     assert_gemm_matches(c, c64, f"splits={splits}")
     assert torch.equal(c, c2)
+
+
+# the 128-token tile's variants: (weight rows, kernel)
+VARIANTS_128 = [(128, "blockfp8_f8f6f4_kernel<128>"), (256, "blockfp8_f8f6f4_kernel<128, 256>")]
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 768, 2048), (300, 1024, 1024), (129, 2048, 512), (1000, 512, 4096)])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_weight_tile_widths(r4q, M, N, K, splits):
+    """The 128-token tile with 128 and with 256 weight rows (two weight scale
+    blocks side by side, one N = 256 MMA per K step, two 256-column
+    accumulators): both give the oracle's result and the same bits -- every
+    output's K-block sums and promotion steps are the same -- unsplit and
+    with K split (fp32 partials per 128-row half), with a ragged last token
+    tile and several units per CTA."""
+    q = random_e4m3_codes((M, K), seed=M + K)
+    As = np.random.default_rng(M + 21).uniform(1e-3, 1e-2, (M, K // 128)).astype(np.float32)
+    w = random_e4m3_codes((N, K), seed=N + 22)
+    Ws = np.random.default_rng(N + 23).uniform(1e-4, 1e-3, (N // 128, K // 128)).astype(np.float32)
+    outs = {}
+    r4q.r4_set_option(3, splits)
+    try:
+        for bn, name in VARIANTS_128:
+            r4q.r4_set_option(8, bn)
+            outs[name] = _run(r4q, q, As, w, Ws, N, K)
+            assert r4q.r4_last_kernel_name() == name
+    finally:
+        r4q.r4_set_option(8, 0)
+        r4q.r4_set_option(3, 0)
+    c64, _ = G.gemm_blockfp8(q, As, w, Ws)
+    for name, c in outs.items():
+        assert_gemm_matches(c, c64, f"{name} splits={splits}")
+    first = outs[VARIANTS_128[0][1]]
+    for name, c in outs.items():
+        assert torch.equal(c, first), name
 
 
 def test_end_to_end_group_quant(r4q):

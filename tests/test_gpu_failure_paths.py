@@ -125,10 +125,11 @@ def test_prefill_stall_reports_and_recovers(r4q, mode, bt):
     assert_gemm_matches(c[:, torch.from_numpy(rows).cuda()], exact(), f"{mode} bt={bt} after the stalled launch")
 
 
-def test_blockfp8_prefill_stall_reports_and_recovers(r4q):
+@pytest.mark.parametrize("bn", [128, 256])
+def test_blockfp8_prefill_stall_reports_and_recovers(r4q, bn):
     """The block-FP8 128-token tile (token-major accumulator, spinning
-    per-K-block handshakes, TMA-stored output): CTA 0 withholds its first
-    activation copy. The spinning waits are bounded like the others: they
+    per-K-block handshakes, TMA-stored output), with 128 and with 256 weight
+    rows: CTA 0 withholds its first activation copy. The spinning waits are bounded like the others: they
     must expire and return, the error must be reported, and the next call
     must give the oracle's result. K = 512 keeps every slot within the ring,
     so the producer reaches its drain at once."""
@@ -140,6 +141,7 @@ def test_blockfp8_prefill_stall_reports_and_recovers(r4q):
     pk = r4q.prepack_blockfp8(torch.from_numpy(wq).cuda(), torch.from_numpy(Ws).cuda(), N, K)
     qd, Ad = torch.from_numpy(q).cuda(), torch.from_numpy(As).cuda()
     r4q.r4_set_option(3, 1)
+    r4q.r4_set_option(8, bn)
     try:
         r4q.r4_device_error(clear=True)
         r4q.r4_set_option(10, 1)
@@ -156,9 +158,11 @@ def test_blockfp8_prefill_stall_reports_and_recovers(r4q):
         c = r4q.gemm_blockfp8(qd, Ad, pk, N, K)
         torch.cuda.synchronize()
         assert r4q.r4_device_error(clear=True) == 0
+        name = r4q.r4_last_kernel_name()
     finally:
         r4q.r4_set_option(3, 0)
-    assert r4q.r4_last_kernel_name() == "blockfp8_f8f6f4_kernel<128>"
+        r4q.r4_set_option(8, 0)
+    assert name == ("blockfp8_f8f6f4_kernel<128, 256>" if bn == 256 else "blockfp8_f8f6f4_kernel<128>")
     c64, _ = G.gemm_blockfp8(q, As, wq, Ws)
     assert_gemm_matches(c, c64, "block-FP8 128-token tile after the stalled launch")
 
