@@ -195,7 +195,7 @@ def mma_peaks(r4q, sms, reps=5):
     the SM clock sampled while it runs. TFLOP/s per instruction shape."""
     import torch
     shapes = (("mxf8f6f4_n256", 1, 256, 32), ("mxf8f6f4_n128", 1, 128, 32), ("f8f6f4_n128", 2, 128, 32),
-              ("mxf4_n256", 3, 256, 64))
+              ("f8f6f4_n256", 2, 256, 32), ("mxf4_n256", 3, 256, 64))
     out = {}
     with ClockSampler(torch.cuda.current_device()) as clk:
         t_end = time.perf_counter() + 1.0
@@ -390,8 +390,12 @@ def run_sections(r4q, synth, device, sweep, l2_bytes, peaks, mma):
             tf = 2.0 * M * N * K / ms / 1e9
             bf[f"M{M}_N{N}_K{K}"] = {"us": round(ms * 1e3, 2), "TFLOPs": round(tf, 1),
                                      "weight_GBps": round(N * K / ms / 1e6, 1)}
-            if M >= 2048 and mma.get("f8f6f4_n128"):
-                bf[f"M{M}_N{N}_K{K}"]["frac_fp8_peak"] = round(tf / mma["f8f6f4_n128"], 3)
+            # the 128-token tile issues M=128, N=256 kind::f8f6f4 MMAs (N=128
+            # where N is not a multiple of 256)
+            pk_name = "f8f6f4_n256" if N % 256 == 0 else "f8f6f4_n128"
+            if M >= 2048 and mma.get(pk_name):
+                bf[f"M{M}_N{N}_K{K}"]["frac_fp8_peak"] = round(tf / mma[pk_name], 3)
+                bf[f"M{M}_N{N}_K{K}"]["peak"] = pk_name
             del g, pool
     out["blockfp8"] = bf
     # skinny bf16
@@ -778,7 +782,8 @@ def digest(per, sec, hbm):
     d["prefill_TFLOPs"] = {_shape_key(k): round(v["TFLOPs"]) for k, v in pre.items()}
     d["prefill_frac"] = {_shape_key(k): v["frac_fp8_peak"] for k, v in pre.items()}
     mma = sec.get("mma_peak_TFLOPs", {})
-    d["mma_peak_TFLOPs"] = {k: mma.get(k) for k in ("mxf8f6f4_n256", "f8f6f4_n128", "mxf4_n256", "sm_mhz")}
+    d["mma_peak_TFLOPs"] = {k: mma.get(k) for k in ("mxf8f6f4_n256", "f8f6f4_n128", "f8f6f4_n256", "mxf4_n256",
+                                                    "sm_mhz")}
     bf = sec.get("blockfp8", {})
     d["blockfp8_TFLOPs_M2048_GBps_else"] = {
         _shape_key(k): (round(v["TFLOPs"]) if k.startswith("M2048") else round(v["weight_GBps"])) for k, v in bf.items()}
