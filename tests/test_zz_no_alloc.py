@@ -61,17 +61,24 @@ def test_noalloc_matches_workspace_entry_point_twice(r4q):
 
 
 def test_noalloc_rejects_schedules_beyond_its_scratch(r4q):
-    M, N, K = 256, 34816, 5120
+    M, N, K = 64, 34816, 5120
     q = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
     s = torch.ones((M,), dtype=torch.float32, device="cuda")
     pk = torch.zeros(r4q.r4_prepack_mxfp4_bytes(N, K), dtype=torch.uint8, device="cuda")
     c = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
-    r4q.r4_set_option(1, 16)                      # 272 tiles x 16 splits x 128 KiB of partials
+    # decode tiles, K split 4 ways through the scratch (not a cluster):
+    # 272 weight tiles x 4 splits of fp32 partial tiles, over 16 MiB. (Prefill
+    # tiles take a split only while each CTA holds one split unit, which a
+    # forced factor does not override, so they no longer reach this size.)
+    r4q.r4_set_option(1, 4)
+    r4q.r4_set_option(6, 0)
     try:
+        assert r4q.r4_gemm_workspace_bytes(r4q.R4_OP_W4A8_MXFP4, M, N, K) > (16 << 20)
         with pytest.raises(r4q.R4Error) as ei:
             r4q.r4_gemm_w4a8_mxfp4_noalloc(q, s, pk, M, N, K, c, N)
         assert ei.value.status == r4q.R4_ERR_WORKSPACE
     finally:
         r4q.r4_set_option(1, 0)
+        r4q.r4_set_option(6, 1)
     torch.cuda.synchronize()
     assert torch.count_nonzero(c) == 0            # nothing was launched
