@@ -38,6 +38,35 @@ __device__ __forceinline__ uint32_t bf16_rn_bits(float v) {
 }
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return bf16_rn_bits(lo) | (bf16_rn_bits(hi) << 16); }
 
+// Two floats to a bf16x2 word in one instruction, each rounded to nearest
+// even: lo in bits 0-15.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Elementwise product of two bf16x2 words, each the exact product rounded
+// once to bf16 (nearest even) -- what rounding the exact fp32 product of two
+// bf16 values to bf16 gives.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Largest magnitude among 8 bf16 values, as a bf16x2 word of two candidates:
+// the magnitudes' bit patterns order as the values do (finite or infinite),
+// so a packed 16-bit integer maximum finds it.
+__device__ __forceinline__ uint32_t absmax8_bits(const uint4 &v) {
+  const uint32_t m = 0x7FFF7FFFu;
+  uint32_t a, b;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x & m), "r"(v.y & m));
+  asm("max.u16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z & m), "r"(v.w & m));
+  asm("max.u16x2 %0, %1, %2;" : "=r"(a) : "r"(a), "r"(b));
+  return a;
+}
+
 // Block-wide sum / max of one float per thread (fixed order: deterministic).
 __device__ __forceinline__ float block_sum(float a, float *red) {
 #pragma unroll
@@ -68,9 +97,10 @@ template <int VPT>
 __device__ __forceinline__ void quant_row(const uint4 (&h)[VPT], int c0, int c1, int C, bool first, uint8_t *qr,
                                           float *s_row, float *red, float *slot) {
   const int tid = threadIdx.x, nt = blockDim.x;
-  float a = 0.f;
+  uint32_t ab = 0;                     // padding vectors are zero
 #pragma unroll
-  for (int i = 0; i < VPT; ++i) a = fmaxf(a, absmax8(h[i]));   // padding vectors are zero
+  for (int i = 0; i < VPT; ++i) asm("max.u16x2 %0, %1, %2;" : "=r"(ab) : "r"(ab), "r"(absmax8_bits(h[i])));
+  float a = fmaxf(bf16lo(ab), bf16hi(ab));
   a = block_max(a, red);
   if (C > 1) {
     a = cluster_combine<true>(a, slot, C);
@@ -145,13 +175,84 @@ __global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_kernel(const uint1
   if (C > 1) cluster_wait();
 }
 
-// g * sigmoid(g) to a few float32 ulps: CUDA's expf, then __fdividef (within
-// 2 ulps while the denominator is below 2^126); larger denominators
-// (g < -87.3) take the correctly rounded division, and exp(-g) = inf gives
-// -0 as the exact value does.
+// g * sigmoid(g) to a few float32 ulps: CUDA's expf, then g times the
+// approximate reciprocal of 1 + exp(-g) (rcp.approx without flush to zero:
+// within an ulp, subnormal reciprocals of denominators from 2^126 included;
+// exp(-g) = inf gives -0 as the exact value rounds to). No branch.
 __device__ __forceinline__ float silu_f32(float g) {
   const float t = 1.f + expf(-g);
-  return t < 0x1p126f ? __fdividef(g, t) : __fdiv_rn(g, t);
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(t));
+  return g * r;
+}
+
+// h = bf16(bf16(silu(g)) * u) for 8 columns: one rounding each.
+__device__ __forceinline__ uint4 silu_mul8(const uint4 &g4, const uint4 &u4) {
+  const uint32_t gv[4] = {g4.x, g4.y, g4.z, g4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
+  uint32_t hv[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) hv[j] = mul_bf16x2(bf16x2_rn(silu_f32(bf16lo(gv[j])), silu_f32(bf16hi(gv[j]))), uv[j]);
+  return make_uint4(hv[0], hv[1], hv[2], hv[3]);
+}
+
+// One row per CTA, [g | u] staged in shared memory by bulk asynchronous
+// copies: one pair per pass of the block's threads (pass i holds vectors
+// [i * nt, (i + 1) * nt) of g and of u), each pass on its own mbarrier, all
+// issued at once by one thread. The whole row is in flight without holding
+// registers, and a pass is promoted as soon as it lands. (Three CTAs per SM
+// at up to six passes.)
+template <int VPT>
+__global__ void __launch_bounds__(kSiluThreads, VPT <= 6 ? 3 : 2)
+    silu_mul_quant_staged_kernel(const uint16_t *__restrict__ gu, int N, uint8_t *__restrict__ q,
+                                 float *__restrict__ s, int *err) {
+  extern __shared__ __align__(16) uint8_t smem_rows[];   // g row, then u row (bf16)
+  __shared__ float red[kSiluThreads / 32];
+  __shared__ float slot;
+  __shared__ __align__(8) uint64_t bar[VPT];
+  __shared__ int abort_flag;
+  const int row = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+  const int nvec = N >> 3;
+  uint16_t *gs = reinterpret_cast<uint16_t *>(smem_rows);
+  uint16_t *us = gs + N;
+  if (tid == 0) {
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) mbar_init(&bar[i], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    pdl_launch_dependents();
+  }
+  __syncthreads();
+  pdl_wait();   // gu comes from the preceding kernel
+  if (tid == 0) {
+    const uint16_t *gr = gu + static_cast<size_t>(row) * 2 * N;
+    const uint64_t pol = policy_evict_first();
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v0 = i * nt;
+      if (v0 < nvec) {
+        const uint32_t bytes = static_cast<uint32_t>(min(nt, nvec - v0)) * 16u;
+        mbar_arrive_expect_tx(&bar[i], 2u * bytes);
+        bulk_load(gs + v0 * 8, gr + v0 * 8, bytes, &bar[i], pol);
+        bulk_load(us + v0 * 8, gr + N + v0 * 8, bytes, &bar[i], pol);
+      }
+    }
+  }
+  uint4 h[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = i * nt + tid;
+    h[i] = make_uint4(0, 0, 0, 0);
+    if (v < nvec && mbar_wait(&bar[i], 0, &abort_flag, err, DEV_ERR_WAIT_FULL))
+      h[i] = silu_mul8(*reinterpret_cast<const uint4 *>(gs + v * 8), *reinterpret_cast<const uint4 *>(us + v * 8));
+  }
+  quant_row<VPT>(h, 0, N, 1, true, q + static_cast<size_t>(row) * N, s + row, red, &slot);
+  // Never leave a copy in flight (returns at once unless a wait above gave up).
+  if (tid == 0) {
+    volatile int dummy = 0;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+      if (i * nt < nvec) mbar_wait(&bar[i], 0, &dummy, err, DEV_ERR_WAIT_DRAIN);
+  }
 }
 
 template <int VPT>
@@ -170,17 +271,7 @@ __global__ void __launch_bounds__(kSiluThreads) silu_mul_quant_kernel(const uint
   for (int i = 0; i < VPT; ++i) {
     const int k = c0 + (i * nt + tid) * 8;
     if (k < c1) {
-      const uint4 g4 = __ldg(reinterpret_cast<const uint4 *>(gr + k));
-      const uint4 u4 = __ldg(reinterpret_cast<const uint4 *>(gr + N + k));
-      const uint32_t gv[4] = {g4.x, g4.y, g4.z, g4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
-      uint32_t hv[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t av = pack2(silu_f32(bf16lo(gv[j])), silu_f32(bf16hi(gv[j])));
-        // bf16 x bf16 is exact in fp32: one rounding, to bf16
-        hv[j] = pack2(bf16lo(av) * bf16lo(uv[j]), bf16hi(av) * bf16hi(uv[j]));
-      }
-      h[i] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      h[i] = silu_mul8(__ldg(reinterpret_cast<const uint4 *>(gr + k)), __ldg(reinterpret_cast<const uint4 *>(gr + N + k)));
     } else {
       h[i] = make_uint4(0, 0, 0, 0);
     }
@@ -243,6 +334,22 @@ cudaError_t launch_silu_mul_quant(const uint16_t *gu, int64_t M, int64_t N, uint
   const RowSplit rs = split_row(M, N, RowKind::kSilu);
   const dim3 grid(static_cast<unsigned>(M * rs.C));
   const int n = static_cast<int>(N);
+  if (rs.C == 1) {   // one CTA per row: the row staged in shared memory
+    const size_t smem = static_cast<size_t>(4) * N;
+#define R4_SMQS(V)                                                                                           \
+  {                                                                                                          \
+    auto kern = silu_mul_quant_staged_kernel<V>;                                                             \
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);                            \
+    if (e == cudaSuccess) e = launch_pdl(kern, grid, dim3(rs.threads), smem, st, gu, n, q, s, device_error_word()); \
+    if (e != cudaSuccess) return e;                                                                          \
+    set_last_kernel("silu_mul_quant_staged_kernel<" #V ">");                                                 \
+  }
+    const int64_t per = rs.per;
+    if (per <= 1) R4_SMQS(1) else if (per <= 2) R4_SMQS(2) else if (per <= 4) R4_SMQS(4) else if (per <= 6) R4_SMQS(6)
+    else if (per <= 9) R4_SMQS(9) else R4_SMQS(12)
+#undef R4_SMQS
+    return cudaGetLastError();
+  }
 #define R4_SMQ(V)                                                                                            \
   {                                                                                                          \
     const cudaError_t e =                                                                                    \
