@@ -55,6 +55,16 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   return r;
 }
 
+// Elementwise sum of two bf16x2 words, each the exact sum rounded once to
+// bf16 (nearest even) -- what rounding their fp32 sum to bf16 gives: two
+// bf16 values whose exponents differ by at most 16 add exactly in fp32, and
+// a farther one lies below half a bf16 ulp of the larger either way.
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // Largest magnitude among 8 bf16 values, as a bf16x2 word of two candidates:
 // the magnitudes' bit patterns order as the values do (finite or infinite),
 // so a packed 16-bit integer maximum finds it.
@@ -116,6 +126,97 @@ __device__ __forceinline__ void quant_row(const uint4 (&h)[VPT], int c0, int c1,
   }
 }
 
+// The norm's output for 8 columns: h = bf16(RN(RN(r * inv) * (1 + w))) each.
+__device__ __forceinline__ uint4 norm8(const uint4 &r4, const uint4 &w4, float inv) {
+  const uint32_t rv[4] = {r4.x, r4.y, r4.z, r4.w}, wv[4] = {w4.x, w4.y, w4.z, w4.w};
+  uint32_t hv[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    hv[j] = bf16x2_rn(__fmul_rn(__fmul_rn(bf16lo(rv[j]), inv), 1.f + bf16lo(wv[j])),
+                      __fmul_rn(__fmul_rn(bf16hi(rv[j]), inv), 1.f + bf16hi(wv[j])));
+  return make_uint4(hv[0], hv[1], hv[2], hv[3]);
+}
+
+// One row per CTA, y and the residual staged in shared memory by bulk
+// asynchronous copies, one pair per pass of the block's threads on its own
+// mbarrier (as in the staged SiLU producer). The residual row is read into
+// shared memory before any of it is written back, so ro may alias res.
+template <int VPT>
+__global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_staged_kernel(const uint16_t *__restrict__ y,
+                                                                          const uint16_t *res,
+                                                                          const uint16_t *__restrict__ w, float eps,
+                                                                          int K, uint16_t *ro,
+                                                                          uint8_t *__restrict__ q,
+                                                                          float *__restrict__ s, int *err) {
+  extern __shared__ __align__(16) uint8_t smem_rows[];   // y row, then residual row (bf16)
+  __shared__ float red[kThreads / 32];
+  __shared__ float slot;
+  __shared__ __align__(8) uint64_t bar[VPT];
+  __shared__ int abort_flag;
+  const int row = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+  const int nvec = K >> 3;
+  const size_t base = static_cast<size_t>(row) * K;
+  uint16_t *ys = reinterpret_cast<uint16_t *>(smem_rows);
+  uint16_t *rs = ys + K;
+  if (tid == 0) {
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) mbar_init(&bar[i], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    pdl_launch_dependents();
+  }
+  __syncthreads();
+  pdl_wait();   // y and the residual come from the preceding kernels
+  if (tid == 0) {
+    const uint64_t pol = policy_evict_first();
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v0 = i * nt;
+      if (v0 < nvec) {
+        const uint32_t bytes = static_cast<uint32_t>(min(nt, nvec - v0)) * 16u;
+        mbar_arrive_expect_tx(&bar[i], 2u * bytes);
+        bulk_load(ys + v0 * 8, y + base + v0 * 8, bytes, &bar[i], pol);
+        bulk_load(rs + v0 * 8, res + base + v0 * 8, bytes, &bar[i], pol);
+      }
+    }
+  }
+  uint4 r[VPT];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = i * nt + tid;
+    r[i] = make_uint4(0, 0, 0, 0);
+    if (v < nvec && mbar_wait(&bar[i], 0, &abort_flag, err, DEV_ERR_WAIT_FULL)) {
+      const uint4 a = *reinterpret_cast<const uint4 *>(ys + v * 8);
+      const uint4 b = *reinterpret_cast<const uint4 *>(rs + v * 8);
+      r[i] = make_uint4(add_bf16x2(a.x, b.x), add_bf16x2(a.y, b.y), add_bf16x2(a.z, b.z), add_bf16x2(a.w, b.w));
+      const uint32_t rv[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = bf16lo(rv[j]), hi = bf16hi(rv[j]);
+        ss = fmaf(lo, lo, ss);
+        ss = fmaf(hi, hi, ss);
+      }
+      *reinterpret_cast<uint4 *>(ro + base + v * 8) = r[i];
+    }
+  }
+  ss = block_sum(ss, red);
+  const float inv = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), eps));
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = i * nt + tid;
+    if (v < nvec) r[i] = norm8(r[i], __ldg(reinterpret_cast<const uint4 *>(w + v * 8)), inv);
+  }
+  quant_row<VPT>(r, 0, K, 1, true, q + base, s + row, red, &slot);
+  // Never leave a copy in flight (returns at once unless a wait above gave up).
+  if (tid == 0) {
+    volatile int dummy = 0;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+      if (i * nt < nvec) mbar_wait(&bar[i], 0, &dummy, err, DEV_ERR_WAIT_DRAIN);
+  }
+}
+
 // Row `blockIdx.x / C`, columns [part * cols, part * cols + cols) of it.
 template <int VPT>
 __global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_kernel(const uint16_t *__restrict__ y,
@@ -161,14 +262,7 @@ __global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_kernel(const uint1
   for (int i = 0; i < VPT; ++i) {
     const int k = c0 + (i * nt + tid) * 8;
     if (k < c1) {
-      const uint4 wv4 = __ldg(reinterpret_cast<const uint4 *>(w + k));
-      const uint32_t wv[4] = {wv4.x, wv4.y, wv4.z, wv4.w};
-      uint32_t rv[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        rv[j] = pack2(__fmul_rn(__fmul_rn(bf16lo(rv[j]), inv), 1.f + bf16lo(wv[j])),
-                      __fmul_rn(__fmul_rn(bf16hi(rv[j]), inv), 1.f + bf16hi(wv[j])));
-      r[i] = make_uint4(rv[0], rv[1], rv[2], rv[3]);
+      r[i] = norm8(r[i], __ldg(reinterpret_cast<const uint4 *>(w + k)), inv);
     }
   }
   quant_row<VPT>(r, c0, c1, C, part == 0, q + base, s + row, red, &slot[1]);
@@ -313,6 +407,23 @@ cudaError_t launch_add_rmsnorm_quant(const uint16_t *y, const uint16_t *res, con
   const RowSplit rs = split_row(M, K, RowKind::kNorm);
   const dim3 grid(static_cast<unsigned>(M * rs.C));
   const int k = static_cast<int>(K);
+  if (rs.C == 1) {   // one CTA per row: y and the residual staged in shared memory
+    const size_t smem = static_cast<size_t>(4) * K;
+#define R4_ARQS(V)                                                                                           \
+  {                                                                                                          \
+    auto kern = add_rmsnorm_quant_staged_kernel<V>;                                                          \
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);                            \
+    if (e == cudaSuccess)                                                                                    \
+      e = launch_pdl(kern, grid, dim3(rs.threads), smem, st, y, res, w, eps, k, ro, q, s, device_error_word()); \
+    if (e != cudaSuccess) return e;                                                                          \
+    set_last_kernel("add_rmsnorm_quant_staged_kernel<" #V ">");                                              \
+  }
+    const int64_t per = rs.per;
+    if (per <= 1) R4_ARQS(1) else if (per <= 2) R4_ARQS(2) else if (per <= 4) R4_ARQS(4) else if (per <= 6) R4_ARQS(6)
+    else if (per <= 9) R4_ARQS(9) else R4_ARQS(12)
+#undef R4_ARQS
+    return cudaGetLastError();
+  }
 #define R4_ARQ(V)                                                                                            \
   {                                                                                                          \
     const cudaError_t e =                                                                                    \
