@@ -401,8 +401,9 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * sums exchanged in distributed shared memory (1, default) or through the
  * caller's workspace (0); key 7: force the block-FP8 token tile (0 =
  * automatic, else 16/32/64/128); key 8: weight rows per block-FP8 128-token
- * tile, 0 (default) 256 when N is a multiple of 256, else 128; 128 or 256
- * forces it (256 only applies where N is a multiple of 256);
+ * tile, 0 (default) 256 when N is a multiple of 256 and the 256-row tiles
+ * occupy at least half of the SMs, else 128; 128 or 256 forces it (256 only
+ * applies where N is a multiple of 256);
  * key 10 (tests of failure detection only):
  * 1 makes the next W4A8 and block-FP8 launches withhold one activation copy
  * in their first CTA, so a pipeline wait never completes, expires after
