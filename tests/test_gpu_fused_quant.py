@@ -88,13 +88,19 @@ def test_add_rmsnorm_quant(r4q, M, K):
     assert r4q.r4_last_kernel_name().startswith(("add_rmsnorm_quant_staged_kernel", "add_rmsnorm_quant_kernel"))
 
 
-def test_add_rmsnorm_quant_in_place_and_zero_row(r4q):
-    M, K = 4, 512
-    y = _randn((M, K), 1, 1.0)
-    res = _randn((M, K), 2, 1.0)
+@pytest.mark.parametrize("M,K", [(4, 512), (400, 5120), (5, 24576)])
+def test_add_rmsnorm_quant_in_place_and_zero_row(r4q, M, K):
+    """residual_out = residual: one CTA per row staged in shared memory (one
+    pass of the block's threads, and five, where later passes are still being
+    copied in while earlier columns of the same row are written back) and a
+    row spread over a cluster."""
+    y = _randn((M, K), 1 + M, 1.0)
+    res = _randn((M, K), 2 + M, 1.0)
     res[2] = -y[2]                                   # r = 0: minimum scale, all-zero codes
-    w = _randn((K,), 3, 0.1)
+    w = _randn((K,), 3 + M, 0.1)
     q, s, ro = _run_arq(r4q, y, res, w, 1e-6, inplace=True)
+    name = r4q.r4_last_kernel_name()
+    assert name.startswith("add_rmsnorm_quant_kernel" if K == 24576 else "add_rmsnorm_quant_staged_kernel"), name
     r, h64 = U.add_rmsnorm(y.float().numpy(), res.float().numpy(), w.float().numpy(), 1e-6)
     assert np.array_equal(bf16_to_np(ro), r)
     assert np.all(np_u8(q)[2] == 0) and np_f32(s)[2] == Q.MIN_SCALE
