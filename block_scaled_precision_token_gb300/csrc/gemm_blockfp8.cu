@@ -122,7 +122,10 @@ struct Cfg {
   // the warp and handed to a TMA tensor store, so the next unit's promotion
   // starts without waiting for global stores.
   static constexpr bool kTmaOut = kCW >= 32;
-  static constexpr int kRedU = BT == 128 ? 1 : 4;          // split-K reduction unroll (registers)
+  // Split-K reduction: 4 x 4 loads in flight; for the 128-token tile in a
+  // separate (not inlined) function, whose registers then do not add to
+  // the promotion loop's.
+  static constexpr bool kRedCall = BT == 128;
   static constexpr uint32_t kOutBytes = kTmaOut ? static_cast<uint32_t>(kEpiWarps * kCW) * 64u : 0u;
   static constexpr int kStagesRaw =
       static_cast<int>((227u * 1024u - 1024u - kMiscBytes - kScBytes - kOutBytes) / kStageBytes);
@@ -204,6 +207,16 @@ __device__ __forceinline__ void wait_ld_into(uint32_t (&r)[16]) {
         "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
       :
       : "memory");
+}
+
+// Sum of `splits` partial tiles [BT][128] of one 128-row block, stored
+// `stride` floats apart, to bf16 C (reduce_slots_store with 4 x 4 loads in
+// flight). Not inlined: the caller keeps its own register budget.
+template <int BT>
+__device__ __noinline__ void reduce_block_call(const float *base, size_t stride, int splits, int tmax, int n0, int N,
+                                               int t0, uint16_t *c, int ldc, int tid, int nthreads) {
+  reduce_slots_store<4, 4>([&](int s2) { return base + static_cast<size_t>(s2) * stride; }, splits, tmax, n0, N,
+                           nullptr, t0, c, ldc, tid, nthreads);
 }
 
 // 4-byte asynchronous copy global -> shared; src_bytes = 0 writes zero.
@@ -597,14 +610,17 @@ __global__ void __launch_bounds__(Cfg<BT, BN>::kThreads, 1) __maxnreg__((Cfg<BT,
         if (*is_last == 1) {
           __threadfence();
           const float *base = p.partials + static_cast<size_t>(tile) * p.splits * (BN * BT);
-          // (the token-major tile holds its accumulators in up to 128
-          // registers a thread: a lighter reduction keeps it free of spills)
 #pragma unroll 1
-          for (int h = 0; h < C::kNB; ++h)
-            reduce_slots_store<C::kRedU, C::kRedU>(
-                [&](int s2) { return base + static_cast<size_t>(s2) * (BN * BT) + h * (128 * BT); }, p.splits,
-                min(BT, p.M - t0), nt * BN + h * 128, nt * BN + h * 128 + 128, nullptr, t0, p.c, p.ldc, e,
-                C::kEpiThreads);
+          for (int h = 0; h < C::kNB; ++h) {
+            if constexpr (C::kRedCall)
+              reduce_block_call<BT>(base + h * (128 * BT), static_cast<size_t>(BN) * BT, p.splits, min(BT, p.M - t0),
+                                    nt * BN + h * 128, nt * BN + h * 128 + 128, t0, p.c, p.ldc, e, C::kEpiThreads);
+            else
+              reduce_slots_store<4, 4>(
+                  [&](int s2) { return base + static_cast<size_t>(s2) * (BN * BT) + h * (128 * BT); }, p.splits,
+                  min(BT, p.M - t0), nt * BN + h * 128, nt * BN + h * 128 + 128, nullptr, t0, p.c, p.ldc, e,
+                  C::kEpiThreads);
+          }
         }
         if (*is_last && e == 0) p.counters[tile] = 0;
         named_bar_sync(2, C::kEpiThreads);
