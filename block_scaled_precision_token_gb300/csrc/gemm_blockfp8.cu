@@ -64,6 +64,7 @@ struct Params {
   int tma_store;       // 1: unsplit tiles leave through shared memory and TMA tensor stores
   int inject_stall;    // test of the bounded waits: CTA 0 withholds its first activation copy
   int early_w;         // 1: weight tiles are requested before waiting for the preceding kernel
+  int c_vec4;          // 1: C rows start 8-byte aligned (4 bf16 per store in the split-K sum)
   const float *As;     // [M, KB]
   const float *Ws;     // [N/128, KB]
   uint16_t *c;
@@ -209,14 +210,71 @@ __device__ __forceinline__ void wait_ld_into(uint32_t (&r)[16]) {
       : "memory");
 }
 
-// Sum of `splits` partial tiles [BT][128] of one 128-row block, stored
-// `stride` floats apart, to bf16 C (reduce_slots_store with 4 x 4 loads in
-// flight). Not inlined: the caller keeps its own register budget.
-template <int BT>
-__device__ __noinline__ void reduce_block_call(const float *base, size_t stride, int splits, int tmax, int n0, int N,
-                                               int t0, uint16_t *c, int ldc, int tid, int nthreads) {
-  reduce_slots_store<4, 4>([&](int s2) { return base + static_cast<size_t>(s2) * stride; }, splits, tmax, n0, N,
-                           nullptr, t0, c, ldc, tid, nthreads);
+// Sum of `splits` partial tiles [tokens][128] of one 128-row block, stored
+// `stride` floats apart, to bf16 C rows t0 .. t0 + tmax - 1, columns n0 ..
+// n0 + 127. A thread takes groups of four columns, 32 groups to a token row
+// (coalesced loads), with up to 4 groups x 4 partials in flight; each sum
+// runs in split order (deterministic) and its four bf16 leave in one 8-byte
+// store when C's rows allow it (vec4), else one at a time.
+__device__ __forceinline__ void reduce_block(const float *base, size_t stride, int splits, int tmax, int n0, int t0,
+                                             uint16_t *c, int ldc, int vec4, int tid, int nthreads) {
+  constexpr int U = 4, S = 4;
+  const int total = tmax * 32;
+  for (int g0 = tid; g0 < total; g0 += nthreads * U) {
+    float4 acc[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int idx = g0 + k * nthreads;
+      acc[k] = idx < total ? __ldcg(reinterpret_cast<const float4 *>(base + (idx >> 5) * 128 + (idx & 31) * 4))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int s0 = 1; s0 < splits; s0 += S) {
+      float4 v[S][U];
+#pragma unroll
+      for (int ss = 0; ss < S; ++ss) {
+        const float *sp = base + static_cast<size_t>(s0 + ss) * stride;
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          const int idx = g0 + k * nthreads;
+          v[ss][k] = (s0 + ss < splits && idx < total)
+                         ? __ldcg(reinterpret_cast<const float4 *>(sp + (idx >> 5) * 128 + (idx & 31) * 4))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int ss = 0; ss < S; ++ss)
+        if (s0 + ss < splits) {
+#pragma unroll
+          for (int k = 0; k < U; ++k) {
+            acc[k].x += v[ss][k].x;
+            acc[k].y += v[ss][k].y;
+            acc[k].z += v[ss][k].z;
+            acc[k].w += v[ss][k].w;
+          }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int idx = g0 + k * nthreads;
+      if (idx >= total) continue;
+      uint16_t *dst = c + static_cast<size_t>(t0 + (idx >> 5)) * ldc + n0 + (idx & 31) * 4;
+      if (vec4) {
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(acc[k].x, acc[k].y), pack_bf16x2(acc[k].z, acc[k].w));
+      } else {
+        dst[0] = f32_to_bf16_rn(acc[k].x);
+        dst[1] = f32_to_bf16_rn(acc[k].y);
+        dst[2] = f32_to_bf16_rn(acc[k].z);
+        dst[3] = f32_to_bf16_rn(acc[k].w);
+      }
+    }
+  }
+}
+
+// The same, not inlined: the 168-register 128-token kernel keeps its own
+// register budget around the call.
+__device__ __noinline__ void reduce_block_call(const float *base, size_t stride, int splits, int tmax, int n0, int t0,
+                                               uint16_t *c, int ldc, int vec4, int tid, int nthreads) {
+  reduce_block(base, stride, splits, tmax, n0, t0, c, ldc, vec4, tid, nthreads);
 }
 
 // 4-byte asynchronous copy global -> shared; src_bytes = 0 writes zero.
@@ -569,12 +627,31 @@ __global__ void __launch_bounds__(Cfg<BT, BN>::kThreads, 1) __maxnreg__((Cfg<BT,
             for (int j = 0; j < C::kCW; ++j) dst[j] = f32_to_bf16_rn(acc[j]);
           }
         } else {
-          // partial tile [n / 128][token][128 n], as the reduction reads it
-          float4 *part = reinterpret_cast<float4 *>(p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (BN * BT) +
-                                                    (col0 >> 7) * (128 * BT) + (q * 32 + lane) * 128 + (col0 & 127));
+          // partial tile [n / 128][token][128 n], as the reduction reads it.
+          // The warp's 32 tokens x kCW columns pass through its output
+          // buffer in 16-column pieces ([32][20] floats: conflict-free
+          // writes), so each global store covers 8 token rows x 64 bytes;
+          // stored straight from the registers, one token row per thread,
+          // every store touched 32 sectors and the load/store queue backed up.
+          float *pw = p.partials + (static_cast<size_t>(tile) * p.splits + sp) * (BN * BT) +
+                      (col0 >> 7) * (128 * BT) + (q * 32) * 128 + (col0 & 127);
+          float *ob = reinterpret_cast<float *>(outbuf + ew * (C::kCW * 64));
 #pragma unroll
-          for (int j4 = 0; j4 < C::kCW / 4; ++j4)
-            part[j4] = make_float4(acc[4 * j4], acc[4 * j4 + 1], acc[4 * j4 + 2], acc[4 * j4 + 3]);
+          for (int c16 = 0; c16 < C::kCW / 16; ++c16) {
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              *reinterpret_cast<float4 *>(ob + lane * 20 + 4 * k) =
+                  make_float4(acc[16 * c16 + 4 * k], acc[16 * c16 + 4 * k + 1], acc[16 * c16 + 4 * k + 2],
+                              acc[16 * c16 + 4 * k + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int r8 = 0; r8 < 4; ++r8) {
+              const int row = r8 * 8 + (lane >> 2);
+              *reinterpret_cast<float4 *>(pw + row * 128 + 16 * c16 + 4 * (lane & 3)) =
+                  *reinterpret_cast<const float4 *>(ob + row * 20 + 4 * (lane & 3));
+            }
+          }
         }
       } else if (C::kTmaOut && p.splits == 1 && p.tma_store) {
         // [token][n] rows of 64 bytes; the store clips tokens past M.
@@ -613,13 +690,11 @@ __global__ void __launch_bounds__(Cfg<BT, BN>::kThreads, 1) __maxnreg__((Cfg<BT,
 #pragma unroll 1
           for (int h = 0; h < C::kNB; ++h) {
             if constexpr (C::kRedCall)
-              reduce_block_call<BT>(base + h * (128 * BT), static_cast<size_t>(BN) * BT, p.splits, min(BT, p.M - t0),
-                                    nt * BN + h * 128, nt * BN + h * 128 + 128, t0, p.c, p.ldc, e, C::kEpiThreads);
+              reduce_block_call(base + h * (128 * BT), static_cast<size_t>(BN) * BT, p.splits, min(BT, p.M - t0),
+                                nt * BN + h * 128, t0, p.c, p.ldc, p.c_vec4, e, C::kEpiThreads);
             else
-              reduce_slots_store<4, 4>(
-                  [&](int s2) { return base + static_cast<size_t>(s2) * (BN * BT) + h * (128 * BT); }, p.splits,
-                  min(BT, p.M - t0), nt * BN + h * 128, nt * BN + h * 128 + 128, nullptr, t0, p.c, p.ldc, e,
-                  C::kEpiThreads);
+              reduce_block(base + h * (128 * BT), static_cast<size_t>(BN) * BT, p.splits, min(BT, p.M - t0),
+                           nt * BN + h * 128, t0, p.c, p.ldc, p.c_vec4, e, C::kEpiThreads);
           }
         }
         if (*is_last && e == 0) p.counters[tile] = 0;
@@ -687,6 +762,7 @@ int launch_bt(const uint8_t *q, const float *As, const uint8_t *packed, int64_t 
   p.tma_store = use_tma_store;
   p.inject_stall = options().inject_stall;
   p.early_w = options().early_weights;
+  p.c_vec4 = (reinterpret_cast<uintptr_t>(c) % 8) == 0 && ldc % 4 == 0;
   p.t_tiles = pl.t_tiles;
   p.splits = pl.splits;
   p.kb_per_split = pl.kb_per_split;
