@@ -39,7 +39,9 @@
 //    full) spin on a non-blocking mbarrier test, bounded like every wait;
 //  * unsplit tiles of 32- and 64-column warps store through shared memory
 //    and TMA tensor stores, so the next unit's promotion starts at once.
-// Split-K and the last-arriving-CTA reduction are as in the W4A8 kernel.
+// Split-K and the last-arriving-CTA reduction follow the W4A8 kernel, with
+// the partials staged for coalesced stores, one acq_rel fence per CTA
+// around the arrival and a sum that stores four bf16 at a time.
 
 #include <cuda_bf16.h>
 
