@@ -950,6 +950,11 @@ def run_one(spec):
         x = synth.activations(M, K, synth.CFG_PREFILL, outliers=True).to(dev)
         for _ in range(3):
             r4q.quant_fp8(x)
+    elif kind == "quant_mxfp4":
+        M, K = dims
+        x = synth.activations(M, K, synth.CFG_DECODE, outliers=True).to(dev)
+        for _ in range(3):
+            r4q.quant_mxfp4(x)
     elif kind == "w4a8":
         M, N, K = dims
         w = synth.weights_fp32(N, K, synth.CFG_DECODE).to(dev)

@@ -192,6 +192,28 @@ __global__ void quant_mxfp4_weight_kernel(const float *__restrict__ w, int64_t N
 //   atoms of a 256-token tile are one contiguous 1 KB copy.
 // Blocks past K and padding tokens (M .. the atoms' end) get code 127 (x1).
 // Blocks of the grid past `real_blocks` write those padding tokens' words.
+// Two fp32 -> two e2m1 codes in one instruction (round to nearest even,
+// saturating to +-6): lo in bits 0-3, hi in bits 4-7.
+__device__ __forceinline__ uint32_t e2m1x2_of(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Largest magnitude among 8 bf16 values: the magnitudes' bit patterns order
+// as the values do (finite or infinite), so packed 16-bit integer maxima
+// find it without unpacking.
+__device__ __forceinline__ float absmax8_packed(const uint4 &v) {
+  const uint32_t m = 0x7FFF7FFFu;
+  uint32_t a, b;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x & m), "r"(v.y & m));
+  asm("max.u16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z & m), "r"(v.w & m));
+  asm("max.u16x2 %0, %1, %2;" : "=r"(a) : "r"(a), "r"(b));
+  return fmaxf(bf16lo(a), bf16hi(a));
+}
+
 template <int SEGW>
 __global__ void __launch_bounds__(256) quant_mxfp4_act_kernel(const uint16_t *__restrict__ x, int M, int K,
                                                               int64_t ldx, int segs, int KB, int A, int real_blocks,
@@ -226,7 +248,7 @@ __global__ void __launch_bounds__(256) quant_mxfp4_act_kernel(const uint16_t *__
     const int seg = seg0 + g;
     if (seg >= segs) break;   // warp-uniform
     const int k = seg * 256 + lane * 8;
-    float a = absmax8(v[g]);
+    float a = absmax8_packed(v[g]);
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
     int X = 0;
@@ -244,14 +266,10 @@ __global__ void __launch_bounds__(256) quant_mxfp4_act_kernel(const uint16_t *__
       // the exact scaling it stands for
       const float p = -X >= -126 ? __uint_as_float(static_cast<uint32_t>(127 - X) << 23) : __uint_as_float(0x00400000u);
       const uint32_t w[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
-      uint32_t out = 0;
+      uint32_t out = 0;   // element i in nibble i, two per conversion
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float f = (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
-        const uint32_t c =
-            static_cast<uint32_t>(__nv_cvt_float_to_fp4(__fmul_rn(f, p), __NV_E2M1, cudaRoundNearest)) & 0xFu;
-        out |= c << (4 * i);
-      }
+      for (int i = 0; i < 4; ++i)
+        out |= e2m1x2_of(__fmul_rn(bf16lo(w[i]), p), __fmul_rn(bf16hi(w[i]), p)) << (8 * i);
       *reinterpret_cast<uint32_t *>(q + static_cast<size_t>(row) * (K / 2) + k / 2) = out;
     }
     uint32_t word = static_cast<uint32_t>(code) << (8 * ((lane >> 2) & 3));
