@@ -202,18 +202,6 @@ __device__ __forceinline__ uint32_t e2m1x2_of(float lo, float hi) {
   return r;
 }
 
-// Largest magnitude among 8 bf16 values: the magnitudes' bit patterns order
-// as the values do (finite or infinite), so packed 16-bit integer maxima
-// find it without unpacking.
-__device__ __forceinline__ float absmax8_packed(const uint4 &v) {
-  const uint32_t m = 0x7FFF7FFFu;
-  uint32_t a, b;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x & m), "r"(v.y & m));
-  asm("max.u16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z & m), "r"(v.w & m));
-  asm("max.u16x2 %0, %1, %2;" : "=r"(a) : "r"(a), "r"(b));
-  return fmaxf(bf16lo(a), bf16hi(a));
-}
-
 template <int SEGW>
 __global__ void __launch_bounds__(256) quant_mxfp4_act_kernel(const uint16_t *__restrict__ x, int M, int K,
                                                               int64_t ldx, int segs, int KB, int A, int real_blocks,
@@ -248,7 +236,7 @@ __global__ void __launch_bounds__(256) quant_mxfp4_act_kernel(const uint16_t *__
     const int seg = seg0 + g;
     if (seg >= segs) break;   // warp-uniform
     const int k = seg * 256 + lane * 8;
-    float a = absmax8_packed(v[g]);
+    float a = absmax8(v[g]);
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
     int X = 0;

@@ -23,13 +23,16 @@ constexpr float kMinScale = 1.0f / 229376.0f;  // 1 / (448 * 512)
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// Largest magnitude among 8 bf16 values: the magnitudes' bit patterns order
+// as the values do (finite or infinite), so packed 16-bit integer maxima
+// find it without unpacking.
 __device__ __forceinline__ float absmax8(const uint4 &v) {
   const uint32_t m = 0x7FFF7FFFu;
-  float a = fmaxf(bf16lo(v.x & m), bf16hi(v.x & m));
-  a = fmaxf(a, fmaxf(bf16lo(v.y & m), bf16hi(v.y & m)));
-  a = fmaxf(a, fmaxf(bf16lo(v.z & m), bf16hi(v.z & m)));
-  a = fmaxf(a, fmaxf(bf16lo(v.w & m), bf16hi(v.w & m)));
-  return a;
+  uint32_t a, b;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x & m), "r"(v.y & m));
+  asm("max.u16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z & m), "r"(v.w & m));
+  asm("max.u16x2 %0, %1, %2;" : "=r"(a) : "r"(a), "r"(b));
+  return fmaxf(bf16lo(a), bf16hi(a));
 }
 
 __device__ __forceinline__ uint32_t e4m3_of(float v) {
