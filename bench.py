@@ -1019,6 +1019,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--one", nargs="+", metavar="ARG",
                     help="one small fixed call for ncu captures: KIND M N K (KIND = w4a8 | w4a4 | fp8 | skinny), quant M K, "
+                         "quant_mxfp4 M K (MXFP4 activation quantization), "
                          "arq M K (add + RMS norm + quant) or smq M N (SiluAndMul + quant); "
                          "runs three launches of that one call and exits")
     args = ap.parse_args(argv)
