@@ -147,7 +147,8 @@ __global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_staged_kernel(cons
                                                                           const uint16_t *__restrict__ w, float eps,
                                                                           int K, uint16_t *ro,
                                                                           uint8_t *__restrict__ q,
-                                                                          float *__restrict__ s, int *err) {
+                                                                          float *__restrict__ s, int *err,
+                                                                          int inject) {
   extern __shared__ __align__(16) uint8_t smem_rows[];   // y row, then residual row (bf16)
   __shared__ float red[kThreads / 32];
   __shared__ float slot;
@@ -175,6 +176,9 @@ __global__ void __launch_bounds__(kThreads) add_rmsnorm_quant_staged_kernel(cons
       if (v0 < nvec) {
         const uint32_t bytes = static_cast<uint32_t>(min(nt, nvec - v0)) * 16u;
         mbar_arrive_expect_tx(&bar[i], 2u * bytes);
+        // (failure-detection test: CTA 0 withholds its first pass, so that
+        // pass's wait and the final drain run out)
+        if (inject && blockIdx.x == 0 && i == 0) continue;
         bulk_load(ys + v0 * 8, y + base + v0 * 8, bytes, &bar[i], pol);
         bulk_load(rs + v0 * 8, res + base + v0 * 8, bytes, &bar[i], pol);
       }
@@ -298,7 +302,7 @@ __device__ __forceinline__ uint4 silu_mul8(const uint4 &g4, const uint4 &u4) {
 template <int VPT>
 __global__ void __launch_bounds__(kSiluThreads, VPT <= 6 ? 3 : 2)
     silu_mul_quant_staged_kernel(const uint16_t *__restrict__ gu, int N, uint8_t *__restrict__ q,
-                                 float *__restrict__ s, int *err) {
+                                 float *__restrict__ s, int *err, int inject) {
   extern __shared__ __align__(16) uint8_t smem_rows[];   // g row, then u row (bf16)
   __shared__ float red[kSiluThreads / 32];
   __shared__ float slot;
@@ -326,6 +330,8 @@ __global__ void __launch_bounds__(kSiluThreads, VPT <= 6 ? 3 : 2)
       if (v0 < nvec) {
         const uint32_t bytes = static_cast<uint32_t>(min(nt, nvec - v0)) * 16u;
         mbar_arrive_expect_tx(&bar[i], 2u * bytes);
+        // (failure-detection test: CTA 0 withholds its first pass)
+        if (inject && blockIdx.x == 0 && i == 0) continue;
         bulk_load(gs + v0 * 8, gr + v0 * 8, bytes, &bar[i], pol);
         bulk_load(us + v0 * 8, gr + N + v0 * 8, bytes, &bar[i], pol);
       }
@@ -414,7 +420,8 @@ cudaError_t launch_add_rmsnorm_quant(const uint16_t *y, const uint16_t *res, con
     auto kern = add_rmsnorm_quant_staged_kernel<V>;                                                          \
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);                            \
     if (e == cudaSuccess)                                                                                    \
-      e = launch_pdl(kern, grid, dim3(rs.threads), smem, st, y, res, w, eps, k, ro, q, s, device_error_word()); \
+      e = launch_pdl(kern, grid, dim3(rs.threads), smem, st, y, res, w, eps, k, ro, q, s, device_error_word(), \
+                     options().inject_stall);                                                                \
     if (e != cudaSuccess) return e;                                                                          \
     set_last_kernel("add_rmsnorm_quant_staged_kernel<" #V ">");                                              \
   }
@@ -451,7 +458,8 @@ cudaError_t launch_silu_mul_quant(const uint16_t *gu, int64_t M, int64_t N, uint
   {                                                                                                          \
     auto kern = silu_mul_quant_staged_kernel<V>;                                                             \
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);                            \
-    if (e == cudaSuccess) e = launch_pdl(kern, grid, dim3(rs.threads), smem, st, gu, n, q, s, device_error_word()); \
+    if (e == cudaSuccess)                                                                                    \
+      e = launch_pdl(kern, grid, dim3(rs.threads), smem, st, gu, n, q, s, device_error_word(), options().inject_stall); \
     if (e != cudaSuccess) return e;                                                                          \
     set_last_kernel("silu_mul_quant_staged_kernel<" #V ">");                                                 \
   }

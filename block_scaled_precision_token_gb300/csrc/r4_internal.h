@@ -32,7 +32,8 @@ struct Options {
   int fp8_splits = 0;       // 0 = automatic
   int fp8_token_tile = 0;   // 0 = automatic, else 16/32/64/128
   int fp8_n_tile = 0;       // block-FP8 128-token tiles: weight rows per tile, 0 = automatic, else 128/256
-  int inject_stall = 0;     // tests only: the next W4A8 launches withhold one copy (bounded-wait test)
+  int inject_stall = 0;     // tests only: the next W4A8/W4A4, block-FP8 and staged producer launches withhold one
+                            // copy (bounded-wait test)
   int pdl = 1;              // launch with programmatic stream serialization
   int early_weights = 1;    // GEMMs read their weight operand before waiting for the preceding kernel
   int l2_prefetch = 2;      // W4A8/W4A4 decode tiles: 2 rolling L2 prefetch ahead of the ring, 1 whole range at

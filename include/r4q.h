@@ -405,8 +405,9 @@ int r4_gemm_w4a8_mxfp4_noalloc(const uint8_t *q, const float *s, const void *pac
  * occupy at least half of the SMs, else 128; 128 or 256 forces it (256 only
  * applies where N is a multiple of 256);
  * key 10 (tests of failure detection only):
- * 1 makes the next W4A8 and block-FP8 launches withhold one activation copy
- * in their first CTA, so a pipeline wait never completes, expires after
+ * 1 makes the next W4A8, W4A4 and block-FP8 launches, and the fused
+ * producers' one-CTA-per-row launches, withhold one activation copy in
+ * their first CTA, so a pipeline wait never completes, expires after
  * ~2 s and is reported by r4_device_error (the launch itself returns R4_OK,
  * the output is unspecified, the workspace counters end at zero and the
  * context stays usable); 0 (default) turns it off;

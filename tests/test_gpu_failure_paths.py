@@ -167,6 +167,52 @@ def test_blockfp8_prefill_stall_reports_and_recovers(r4q, bn):
     assert_gemm_matches(c, c64, "block-FP8 128-token tile after the stalled launch")
 
 
+@pytest.mark.parametrize("op", ["silu", "norm"])
+def test_staged_producer_stall_reports_and_recovers(r4q, op):
+    """The fused producers' one-CTA-per-row kernels stage each row with bulk
+    copies, one mbarrier per pass of the block's threads: with option 10,
+    CTA 0 arms its first pass but withholds the copies. That wait and the
+    final drain must run out and return (no copy is left in flight), the
+    error must be reported, and the next call must give the same bits as
+    the call before the stall."""
+    if op == "silu":
+        M, N = 200, 2048
+        gu = synth.activations(M, 2 * N, synth.CFG_PREFILL).cuda()
+
+        def run():
+            return r4q.silu_mul_quant(gu)
+        name = "silu_mul_quant_staged_kernel"
+    else:
+        M, K = 300, 5120
+        y = synth.activations(M, K, synth.CFG_PREFILL).cuda()
+        res = synth.activations(M, K, synth.CFG_DECODE).cuda()
+        wn = (synth.activations(1, K, synth.CFG_TINY)[0] * 0.1).to(torch.bfloat16).cuda()
+
+        def run():
+            q, s, _ = r4q.add_rmsnorm_quant(y, res, wn, 1e-6)
+            return q, s
+        name = "add_rmsnorm_quant_staged_kernel"
+    q0, s0 = run()
+    torch.cuda.synchronize()
+    assert r4q.r4_last_kernel_name().startswith(name), r4q.r4_last_kernel_name()
+    r4q.r4_device_error(clear=True)
+    r4q.r4_set_option(10, 1)
+    try:
+        t0 = time.time()
+        run()
+        torch.cuda.synchronize()
+        elapsed = time.time() - t0
+    finally:
+        r4q.r4_set_option(10, 0)
+    code = r4q.r4_device_error(clear=True)
+    assert code in (WAIT_FULL, WAIT_DRAIN), f"device error word {code}"
+    assert 1.0 < elapsed < 30.0, f"the stalled launch took {elapsed:.1f} s"
+    q1, s1 = run()
+    torch.cuda.synchronize()
+    assert r4q.r4_device_error(clear=True) == 0
+    assert torch.equal(q0, q1) and torch.equal(s0, s1)
+
+
 def _blockfp8_inputs(r4q, M, N, K):
     x = synth.activations(M, K, synth.CFG_BLOCKFP8)
     w = synth.weights_fp32(N, K, synth.CFG_BLOCKFP8)
