@@ -8,14 +8,19 @@
 //  * SiluAndMul + quant on [g | u]: h = bf16(bf16(silu(g)) * u), then the
 //    per-token rule.
 //
-// HBM-bound row kernels: the CTAs of a row hold it in registers (16-byte
-// vectors, read once), reduce it twice (sum of squares, then amax) and write
-// the codes -- one launch where the unfused chain takes two or three. A
-// short batch spreads each row over a thread-block cluster whose CTAs
-// combine their partial sums and maxima through distributed shared memory.
-// The norm is fp32 with correctly rounded division and reciprocal square
-// root; SiLU uses CUDA's expf and a fast quotient (a few ulps); the codes
-// come from correctly rounded quotients (quant_common.cuh).
+// Row kernels, one launch where the unfused chain takes two or three: the
+// row is read once, reduced (sum of squares, then the maximum magnitude)
+// and written as codes. Where one CTA holds a whole row, the row is staged
+// in shared memory by bulk asynchronous copies (one mbarrier per pass of the
+// block's threads) and each thread keeps its results in registers; a short
+// batch instead spreads each row over a thread-block cluster whose CTAs load
+// their columns into registers and combine partial sums and maxima through
+// distributed shared memory. Pairs of bf16 values are added, multiplied and
+// rounded with packed bf16x2 instructions where that rounds as the
+// definition does. The norm is fp32 with correctly rounded division and
+// reciprocal square root; SiLU uses CUDA's expf and an approximate
+// reciprocal (a few ulps); the codes come from correctly rounded quotients
+// (quant_common.cuh).
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
