@@ -14,7 +14,8 @@ def test_digest_carries_every_row_compactly():
     per = {"M6_N34816_K5120": {"us": 18.0, "weight_GBps": 5282.2}}
     sec = {
         "prefill_w4a8": {"M256_N34816_K5120": {"us": 40.6, "TFLOPs": 2246.4, "frac_fp8_peak": 0.512}},
-        "mma_peak_TFLOPs": {"mxf8f6f4_n256": 4383.5, "f8f6f4_n128": 4006.6, "mxf4_n256": 8752.5, "sm_mhz": 2070.0},
+        "mma_peak_TFLOPs": {"mxf8f6f4_n256": 4383.5, "f8f6f4_n128": 4006.6, "f8f6f4_n256": 4388.3, "mxf4_n256": 8752.5,
+                            "sm_mhz": 2070.0},
         "blockfp8": {"M2048_N6144_K2048": {"us": 67.2, "TFLOPs": 766.9, "weight_GBps": 187.2},
                      "M8_N6144_K2048": {"us": 7.3, "TFLOPs": 27.5, "weight_GBps": 1720.4}},
         "skinny_bf16_graph": {"M6_N256_K2048": {"hot_us": 2.834, "pooled_us": 3.011}},
@@ -31,5 +32,7 @@ def test_digest_carries_every_row_compactly():
     assert d["skinny_hot_us"] == {"6x256x2048": 2.834}
     assert d["w4a4"] == {"decode_GBps": {"6x34816x5120": 4998}}
     assert d["mma_peak_TFLOPs"]["mxf4_n256"] == 8752.5
+    # the block-FP8 128-token tile's instruction shape (M=128, N=256)
+    assert d["mma_peak_TFLOPs"]["f8f6f4_n256"] == 4388.3
     # numbers only, short keys: the full line of the real run stays a few KB
     assert len(json.dumps(d, separators=(",", ":"))) < 1200
