@@ -358,6 +358,32 @@ size_t r4_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
   }
 }
 
+int r4_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sms, int32_t *out) {
+  if (!out || M < 1 || N < 1 || K < 1 || sms < 1 || M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff)
+    return R4_ERR_INVALID_ARG;
+  GemmPlan pl;
+  switch (op) {
+    case R4_OP_W4A8_MXFP4:
+    case R4_OP_LINEAR_W4A8_MXFP4:
+      if (K % 32 || K < 128) return R4_ERR_UNSUPPORTED_SHAPE;
+      pl = plan_w4a8(M, N, K, sms);
+      break;
+    case R4_OP_W4A4_MXFP4:
+      if (K % 32 || K < 128) return R4_ERR_UNSUPPORTED_SHAPE;
+      pl = plan_w4a4(M, N, K, sms);
+      break;
+    case R4_OP_BLOCKFP8:
+      if (N % 128 || K % 128) return R4_ERR_UNSUPPORTED_SHAPE;
+      pl = plan_blockfp8(M, N, K, sms);
+      break;
+    default: return R4_ERR_INVALID_ARG;
+  }
+  const int32_t v[10] = {pl.BT, pl.BN, pl.n_tiles, pl.t_tiles, pl.splits, pl.kb_per_split, pl.units, pl.grid,
+                         pl.cluster, pl.sk};
+  for (int i = 0; i < 10; ++i) out[i] = v[i];
+  return R4_OK;
+}
+
 int r4_gemm_w4a8_mxfp4(const uint8_t *q, const float *s, const void *packed, int64_t M, int64_t N, int64_t K,
                        uint16_t *c, int64_t ldc, void *workspace, size_t workspace_bytes, r4_stream_t stream) {
   if (!q || !s || !packed || !c) return R4_ERR_INVALID_ARG;

@@ -48,6 +48,7 @@ _SIGS = {
     "r4_prepack_blockfp8_bytes": ([_I64, _I64], _SZ),
     "r4_prepack_blockfp8": ([_P, _P, _I64, _I64, _P, _SZ, _P], _I),
     "r4_gemm_workspace_bytes": ([_I, _I64, _I64, _I64], _SZ),
+    "r4_plan_gemm": ([_I, _I64, _I64, _I64, _I, _P], _I),
     "r4_gemm_w4a8_mxfp4": ([_P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
     "r4_linear_w4a8_mxfp4": ([_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
     "r4_gemm_blockfp8": ([_P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], _I),
@@ -192,6 +193,18 @@ def r4_prepack_blockfp8(w, w_scale, N, K, packed, stream=None):
 
 def r4_gemm_workspace_bytes(op, M, N, K):
     return int(lib().r4_gemm_workspace_bytes(op, M, N, K))
+
+
+PLAN_FIELDS = ("token_tile", "weight_rows", "n_tiles", "t_tiles", "splits", "kb_per_split", "units", "grid",
+               "cluster", "stream_k")
+
+
+def r4_plan_gemm(op, M, N, K, sms):
+    """The schedule a GEMM call would launch on `sms` SMs (host arithmetic),
+    as a dict keyed by PLAN_FIELDS."""
+    out = (ctypes.c_int32 * len(PLAN_FIELDS))()
+    _check(lib().r4_plan_gemm(op, M, N, K, sms, ctypes.cast(out, ctypes.c_void_p)), "r4_plan_gemm")
+    return dict(zip(PLAN_FIELDS, list(out)))
 
 
 def _ws(workspace):

@@ -279,6 +279,23 @@ int r4_prepack_blockfp8(const uint8_t *w, const float *w_scale, int64_t N, int64
 size_t r4_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
 
 /*
+ * r4_plan_gemm -- the schedule a GEMM call of `op` (R4_OP_W4A8_MXFP4,
+ * R4_OP_BLOCKFP8, R4_OP_W4A4_MXFP4, R4_OP_LINEAR_W4A8_MXFP4: its GEMM) would
+ * launch for (M, N, K) on a GPU with `sms` streaming multiprocessors, under
+ * the current r4_set_option overrides. Host arithmetic: the block-FP8
+ * planner touches no device; the W4A8/W4A4 planners ask the current device
+ * how many thread-block clusters of a split fit, and without one take no
+ * cluster split. out: int32[10], host memory, written on R4_OK:
+ *   [0] token tile  [1] weight rows per tile  [2] weight-row tiles
+ *   [3] token tiles  [4] K splits  [5] 128-K blocks per split
+ *   [6] work units  [7] grid (CTAs)  [8] split across a cluster (0/1)
+ *   [9] stream-K schedule (0/1; then [6] counts stream-K segments)
+ * R4_ERR_INVALID_ARG for a null out, non-positive sizes or another op;
+ * R4_ERR_UNSUPPORTED_SHAPE where the GEMM call would refuse the shape.
+ */
+int r4_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sms, int32_t *out);
+
+/*
  * r4_gemm_w4a8_mxfp4 -- C = bf16( s[m] * sum_k e4m3(q[m,k]) * e2m1(w[n,k]) * 2^(e[n,k/32]-127) ).
  * Source: "radiance_mxfp4.py", module docstring and _exact_ref.
  * Runs on tcgen05 block-scaled MMA (kind::mxf8f6f4, ue8m0 scale per 32 K) with
