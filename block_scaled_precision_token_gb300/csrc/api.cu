@@ -143,7 +143,9 @@ using namespace r4;
 
 extern "C" {
 
-int r4_version(void) { return (0 << 16) | 3; }   // 0.3: W4A4 (MXFP4 activations, kind::mxf4), option 14, r4_mma_peak
+// 0.3: W4A4 (MXFP4 activations, kind::mxf4), option 14, r4_mma_peak;
+// 0.4: r4_plan_gemm, option 8 (block-FP8 weight rows per tile), option 9 unassigned
+int r4_version(void) { return (0 << 16) | 4; }
 
 const char *r4_status_string(int status) {
   switch (status) {
